@@ -1,0 +1,512 @@
+"""Pins of the CPU oracle against things other than itself (CPU only).
+
+* storage decoders against the OCP E4M3 table and torch's own casts;
+* RMSNorm / RoPE / attention / the whole forward against an independent
+  re-expression built from torch.nn.functional library routines in float64
+  (``F.rms_norm``, ``F.linear``, ``F.scaled_dot_product_attention`` with
+  ``repeat_interleave`` for GQA, complex multiplication for RoPE);
+* closed forms, special cases and the invariants the pages state (the cached
+  round equals the first-light forward; chunked ingest equals one-shot
+  ingest; the cache is unchanged by a round);
+* brute force with scalar Python loops on a micro drafter;
+* planted mistakes in the oracle must be caught by these pins.
+"""
+import dataclasses
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import dflash_oracle as O
+from speculative_decoding_block_ingest_gb300 import synth
+from _common import oracle_weights, rel_err
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+MICRO = synth.DraftConfig(n_layers=2, hidden=32, n_heads=4, n_kv_heads=2, head_dim=8,
+                          intermediate=48, n_taps=2, weight_dtype="f32", kv_dtype="f32")
+MICRO_YARN = dataclasses.replace(MICRO, rope_type="yarn", yarn_factor=4.0,
+                                 yarn_original_max_pos=256, yarn_beta_fast=8.0,
+                                 yarn_beta_slow=1.0, rope_theta=100.0)
+MICRO_BF16 = dataclasses.replace(MICRO, weight_dtype="bf16", kv_dtype="bf16")
+MICRO_FP8 = dataclasses.replace(MICRO, weight_dtype="fp8", kv_dtype="bf16")
+
+
+def _inputs(cfg, ctx, seed=11):
+    taps = synth.taps_rows(cfg, seq=seed, row0=0, nrows=ctx).double().numpy()
+    noise = synth.noise_rows(cfg, seq=seed, round_idx=0).double().numpy()
+    pos = list(range(ctx + cfg.block))
+    return taps, noise, pos
+
+
+def _drafter(cfg, seed=0):
+    W = synth.make_weights(cfg, seed=seed)
+    return O.Drafter(cfg, oracle_weights(W)), W
+
+
+# ------------------------------------------------------------- independent re-expression
+def _torch_weight(w):
+    if isinstance(w, tuple):          # fp8 codes + per-row scale, decoded by torch
+        return w[0].to(torch.float64) * w[1].to(torch.float64)[:, None]
+    return w.to(torch.float64)
+
+
+def _rope_complex(x, pos, inv_freq, mscale):
+    half = x.shape[-1] // 2
+    z = torch.complex(x[..., :half].contiguous(), x[..., half:].contiguous())
+    ang = torch.as_tensor(pos, dtype=torch.float64)[:, None] * inv_freq[None, :]
+    z = z * torch.polar(torch.ones_like(ang), ang)[:, None, :]
+    return mscale * torch.cat([z.real, z.imag], dim=-1)
+
+
+def torch_forward(cfg, W, taps, noise, pos, inv_freq, mscale):
+    """The drafter forward expressed with torch.nn.functional routines."""
+    H, d, eps = cfg.hidden, cfg.head_dim, cfg.rms_eps
+    G = cfg.n_heads // cfg.n_kv_heads
+    taps = torch.as_tensor(taps, dtype=torch.float64)
+    h = torch.as_tensor(noise, dtype=torch.float64).clone()
+    inv_freq = torch.as_tensor(inv_freq, dtype=torch.float64)
+    ctx, b = taps.shape[0], h.shape[0]
+    feats = F.rms_norm(F.linear(taps, _torch_weight(W["fc"])), (H,), W["hidden_norm"].double(), eps)
+    for L in W["layers"]:
+        w = {k: (_torch_weight(v) if k in synth.PROJ_TENSORS else v.double()) for k, v in L.items()}
+        kc = F.rms_norm(F.linear(feats, w["k"]).view(ctx, -1, d), (d,), w["k_norm"], eps)
+        kc = _rope_complex(kc, pos[:ctx], inv_freq, mscale)
+        vc = F.linear(feats, w["v"]).view(ctx, -1, d)
+        x = F.rms_norm(h, (H,), w["input_ln"], eps)
+        q = _rope_complex(F.rms_norm(F.linear(x, w["q"]).view(b, -1, d), (d,), w["q_norm"], eps),
+                          pos[ctx:], inv_freq, mscale)
+        kb = _rope_complex(F.rms_norm(F.linear(x, w["k"]).view(b, -1, d), (d,), w["k_norm"], eps),
+                           pos[ctx:], inv_freq, mscale)
+        vb = F.linear(x, w["v"]).view(b, -1, d)
+        K = torch.cat([kc, kb]).repeat_interleave(G, dim=1)
+        V = torch.cat([vc, vb]).repeat_interleave(G, dim=1)
+        o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], K.transpose(0, 1)[None],
+                                           V.transpose(0, 1)[None], is_causal=False)
+        o = o[0].transpose(0, 1).reshape(b, -1)
+        h = h + F.linear(o, w["o"])
+        y = F.rms_norm(h, (H,), w["post_ln"], eps)
+        h = h + F.linear(F.silu(F.linear(y, w["gate"])) * F.linear(y, w["up"]), w["down"])
+    return F.rms_norm(h, (H,), W["norm"].double(), eps).numpy()
+
+
+# ------------------------------------------------------------- storage decoders
+def test_e4m3_ocp_table():
+    for line in open(os.path.join(GOLDEN, "e4m3_ocp.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        code, val = line.split()
+        got = O.e4m3_to_f64(np.array([int(code, 16)], dtype=np.uint8))[0]
+        if val == "nan":
+            assert np.isnan(got)
+        else:
+            assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+
+
+def test_e4m3_all_codes_match_torch_cast():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_to_f64(codes.numpy())
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    m = ~np.isnan(ref)
+    assert np.array_equal(ref[m], got[m])
+
+
+def test_bf16_decode_matches_torch():
+    g = torch.Generator().manual_seed(5)
+    x = torch.randn(4096, generator=g) * torch.exp(torch.randn(4096, generator=g) * 8)
+    b = x.to(torch.bfloat16)
+    got = O.bf16_bits_to_f64(b.view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(got, b.to(torch.float64).numpy())
+
+
+# ------------------------------------------------------------- elementwise pieces
+def test_rms_norm_matches_torch():
+    g = torch.Generator().manual_seed(1)
+    x = torch.randn(7, 33, generator=g, dtype=torch.float64) * 3
+    w = torch.randn(33, generator=g, dtype=torch.float64)
+    ref = F.rms_norm(x, (33,), w, 1e-6).numpy()
+    assert np.allclose(O.rms_norm(x.numpy(), w.numpy(), 1e-6), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_rms_norm_zero_vector_is_zero():
+    assert np.all(O.rms_norm(np.zeros((2, 8)), np.ones(8), 1e-6) == 0.0)
+
+
+def test_rope_is_complex_rotation_of_half_pairs():
+    g = torch.Generator().manual_seed(2)
+    x = torch.randn(5, 3, 16, generator=g, dtype=torch.float64)
+    pos = [0, 1, 7, 1000, 65535]
+    inv, _ = O.rope_tables(MICRO)
+    inv = O.rope_tables(dataclasses.replace(MICRO, head_dim=16))[0]
+    ref = _rope_complex(x, pos, torch.as_tensor(inv), 1.3).numpy()
+    got = O.rope_neox(x.numpy(), np.array(pos), inv, 1.3)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_rope_neox_pairing_on_unit_vector():
+    d = 8
+    e0 = np.zeros((1, 1, d)); e0[0, 0, 0] = 1.0
+    inv = np.array([0.5, 0.1, 0.01, 0.001])
+    out = O.rope_neox(e0, np.array([1]), inv, 1.0)[0, 0]
+    # rotate-half: e_0 -> cos e_0 + sin e_{d/2}; nothing else moves
+    assert out[0] == pytest.approx(math.cos(0.5)) and out[d // 2] == pytest.approx(math.sin(0.5))
+    assert np.count_nonzero(np.abs(out) > 1e-15) == 2
+
+
+def test_rope_relative_position_property():
+    g = torch.Generator().manual_seed(3)
+    q = torch.randn(1, 1, 16, generator=g, dtype=torch.float64).numpy()
+    k = torch.randn(1, 1, 16, generator=g, dtype=torch.float64).numpy()
+    inv = O.rope_tables(dataclasses.replace(MICRO, head_dim=16))[0]
+    dots = []
+    for base in (0, 17, 4000):
+        qr = O.rope_neox(q, np.array([base + 9]), inv, 1.0)
+        kr = O.rope_neox(k, np.array([base + 2]), inv, 1.0)
+        dots.append(float(np.sum(qr * kr)))
+    assert np.allclose(dots, dots[0], rtol=1e-10)
+
+
+# ------------------------------------------------------------- YaRN table
+def test_yarn_page_constants():
+    facts = json.load(open(os.path.join(GOLDEN, "page_facts.json")))
+    y = facts["yarn"]["value"]
+    cfg = dataclasses.replace(synth.QWEN3_5L_YARN)
+    assert (cfg.yarn_factor, cfg.yarn_original_max_pos, cfg.yarn_beta_fast, cfg.yarn_beta_slow) == \
+        (y["factor"], y["original_max_pos"], y["beta_fast"], y["beta_slow"])
+    _, m = O.rope_tables(cfg)
+    assert m == pytest.approx(0.1 * math.log(32.0) + 1.0, rel=1e-15)
+
+
+@pytest.mark.parametrize("cfg", [synth.QWEN3_5L_YARN, MICRO_YARN])
+def test_yarn_divisors_by_wavelength(cfg):
+    """Dims that turn more than beta_fast times over the original context keep
+    their frequency; dims that turn fewer than beta_slow times are divided by
+    the factor (YaRN's by-wavelength rule); between, 1/ff is affine in j."""
+    d, base = cfg.head_dim, cfg.rope_theta
+    inv, _ = O.rope_tables(cfg)
+    plain = base ** (-2.0 * np.arange(d // 2) / d)
+    ff = plain / inv
+    turns = cfg.yarn_original_max_pos * plain / (2 * math.pi)
+    assert np.allclose(ff[turns > cfg.yarn_beta_fast], 1.0, rtol=1e-14)
+    assert np.allclose(ff[turns < cfg.yarn_beta_slow], cfg.yarn_factor, rtol=1e-14)
+    assert np.all(np.diff(ff) >= -1e-12) and ff.min() >= 1 - 1e-14 and ff.max() <= cfg.yarn_factor + 1e-12
+    inner = np.where((ff > 1 + 1e-12) & (ff < cfg.yarn_factor - 1e-9))[0]
+    assert len(inner) >= 1
+    if cfg.head_dim >= 64:
+        assert len(inner) >= 3
+        assert np.allclose(np.diff(1.0 / ff[inner], 2), 0.0, atol=1e-12)
+
+
+def test_yarn_factor_one_is_plain_rope():
+    cfg1 = dataclasses.replace(MICRO_YARN, yarn_factor=1.0)
+    inv1, m1 = O.rope_tables(cfg1)
+    inv0, m0 = O.rope_tables(dataclasses.replace(MICRO_YARN, rope_type="plain"))
+    assert m1 == 1.0 and m0 == 1.0
+    assert np.allclose(inv1, inv0, rtol=1e-15)
+
+
+# ------------------------------------------------------------- whole forward
+@pytest.mark.parametrize("cfg", [MICRO, MICRO_YARN, MICRO_BF16, MICRO_FP8,
+                                 dataclasses.replace(synth.TINY_F32, n_layers=1)])
+def test_forward_full_matches_torch_functional(cfg):
+    D, W = _drafter(cfg)
+    ctx = 64 if cfg.hidden == 256 else 11
+    taps, noise, pos = _inputs(cfg, ctx)
+    got = D.forward_full(taps, noise, pos)
+    ref = torch_forward(cfg, W, taps, noise, pos, D.inv_freq, D.mscale)
+    assert rel_err(got, ref) < 1e-12
+
+
+def test_tensor_census_matches_page():
+    facts = json.load(open(os.path.join(GOLDEN, "page_facts.json")))
+    cfg = dataclasses.replace(MICRO, n_layers=facts["first_light_layers"]["value"])
+    W = synth.make_weights(cfg)
+    n = 3 + sum(len(L) for L in W["layers"])
+    assert n == facts["backbone_tensors_5_layer"]["value"]
+
+
+# ------------------------------------------------------------- closed forms
+def test_zero_output_projections_give_normed_noise():
+    cfg = MICRO
+    W = synth.make_weights(cfg)
+    for L in W["layers"]:
+        L["o"] = torch.zeros_like(L["o"])
+        L["down"] = torch.zeros_like(L["down"])
+    D = O.Drafter(cfg, oracle_weights(W))
+    taps, noise, pos = _inputs(cfg, 9)
+    ref = F.rms_norm(torch.as_tensor(noise), (cfg.hidden,), W["norm"].double(), cfg.rms_eps).numpy()
+    assert rel_err(D.forward_full(taps, noise, pos), ref) < 1e-13
+
+
+def test_zero_keys_give_mean_of_values():
+    D, _ = _drafter(MICRO)
+    g = np.random.default_rng(0)
+    q = g.standard_normal((5, MICRO.n_heads, MICRO.head_dim))
+    vals = g.standard_normal((13, MICRO.n_kv_heads, MICRO.head_dim))
+    out = D.attention(q, np.zeros_like(vals), vals).reshape(5, MICRO.n_heads, MICRO.head_dim)
+    G = MICRO.n_heads // MICRO.n_kv_heads
+    for h in range(MICRO.n_heads):
+        assert np.allclose(out[:, h], vals[:, h // G].mean(axis=0)[None], atol=1e-14)
+
+
+def test_single_key_returns_its_value():
+    D, _ = _drafter(MICRO)
+    g = np.random.default_rng(1)
+    q = g.standard_normal((3, MICRO.n_heads, MICRO.head_dim))
+    k = g.standard_normal((1, MICRO.n_kv_heads, MICRO.head_dim))
+    v = g.standard_normal((1, MICRO.n_kv_heads, MICRO.head_dim))
+    out = D.attention(q, k, v).reshape(3, MICRO.n_heads, MICRO.head_dim)
+    G = MICRO.n_heads // MICRO.n_kv_heads
+    for h in range(MICRO.n_heads):
+        assert np.allclose(out[:, h], v[0, h // G][None], atol=1e-15)
+
+
+# ------------------------------------------------------------- invariants from the pages
+def test_cached_round_equals_first_light_forward():
+    """forward_round over the cached ctx K/V == first-light forward with fresh
+    ctx recompute (DflashDraft page, forward_round), with chunked ingest."""
+    cfg = MICRO_YARN
+    D, _ = _drafter(cfg)
+    taps, noise, pos = _inputs(cfg, 23)
+    kv = O.DraftKV(D)
+    for lo, hi in [(0, 5), (5, 6), (6, 6), (6, 23)]:
+        kv.ingest(3, taps[lo:hi], pos[lo:hi])
+    assert kv.length(3) == 23
+    got = kv.forward_round([3], noise[None], np.array([pos[23:]]))[0]
+    assert kv.length(3) == 23
+    assert rel_err(got, D.forward_full(taps, noise, pos)) < 1e-13
+
+
+def test_chunked_ingest_equals_one_shot():
+    D, _ = _drafter(MICRO)
+    taps, _, pos = _inputs(MICRO, 19)
+    a, b = O.DraftKV(D), O.DraftKV(D)
+    a.ingest(0, taps, pos[:19])
+    for lo in range(0, 19, 4):
+        hi = min(lo + 4, 19)
+        b.ingest(0, taps[lo:hi], pos[lo:hi])
+    for li in range(MICRO.n_layers):
+        assert np.allclose(a.k[0][li], b.k[0][li], rtol=1e-13, atol=1e-13)
+        assert np.allclose(a.v[0][li], b.v[0][li], rtol=1e-13, atol=1e-13)
+
+
+def test_gqa_with_replicated_kv_heads_equals_mha():
+    cfg = MICRO
+    G = cfg.n_heads // cfg.n_kv_heads
+    W = synth.make_weights(cfg)
+    cfg_mha = dataclasses.replace(cfg, n_kv_heads=cfg.n_heads)
+    W2 = {k: v for k, v in W.items()}
+    W2["layers"] = []
+    d = cfg.head_dim
+    for L in W["layers"]:
+        L2 = dict(L)
+        for name in ("k", "v"):
+            blocks = L[name].view(cfg.n_kv_heads, d, -1)
+            L2[name] = blocks.repeat_interleave(G, dim=0).reshape(cfg.n_heads * d, -1)
+        W2["layers"].append(L2)
+    taps, noise, pos = _inputs(cfg, 10)
+    a = O.Drafter(cfg, oracle_weights(W)).forward_full(taps, noise, pos)
+    b = O.Drafter(cfg_mha, oracle_weights(W2)).forward_full(taps, noise, pos)
+    assert rel_err(a, b) < 1e-13
+
+
+def test_ctx_row_permutation_invariance():
+    D, _ = _drafter(MICRO_YARN)
+    taps, noise, pos = _inputs(MICRO_YARN, 12)
+    perm = np.random.default_rng(4).permutation(12)
+    pos2 = [pos[i] for i in perm] + pos[12:]
+    a = D.forward_full(taps, noise, pos)
+    b = D.forward_full(taps[perm], noise, pos2)
+    assert rel_err(a, b) < 1e-13
+
+
+def test_block_row_permutation_equivariance():
+    D, _ = _drafter(MICRO)
+    taps, noise, pos = _inputs(MICRO, 12)
+    perm = np.random.default_rng(5).permutation(16)
+    pos2 = pos[:12] + [pos[12 + i] for i in perm]
+    a = D.forward_full(taps, noise, pos)
+    b = D.forward_full(taps, noise[perm], pos2)
+    assert rel_err(a[perm], b) < 1e-13
+
+
+@pytest.mark.parametrize("cfg", [MICRO, MICRO_YARN])
+def test_position_shift_invariance(cfg):
+    D, _ = _drafter(cfg)
+    taps, noise, pos = _inputs(cfg, 12)
+    a = D.forward_full(taps, noise, pos)
+    b = D.forward_full(taps, noise, [p + 4099 for p in pos])
+    assert rel_err(a, b) < 1e-9
+
+
+def test_batch_independence():
+    D, _ = _drafter(MICRO)
+    kv = O.DraftKV(D)
+    tA, nA, pA = _inputs(MICRO, 7, seed=1)
+    tB, nB, pB = _inputs(MICRO, 13, seed=2)
+    kv.ingest(0, tA, pA[:7])
+    kv.ingest(1, tB, pB[:13])
+    both = kv.forward_round([0, 1], np.stack([nA, nB]), np.array([pA[7:], pB[13:]]))
+    solo = kv.forward_round([1], nB[None], np.array([pB[13:]]))
+    assert np.array_equal(both[1], solo[0])
+
+
+def test_fp8_decoded_weights_equal_bf16_path_on_the_same_values():
+    """FP8 decoding is exact: feeding the dequantised values as plain f64
+    weights gives the same output."""
+    cfg = MICRO_FP8
+    W = synth.make_weights(cfg)
+    D = O.Drafter(cfg, oracle_weights(W))
+    W64 = {"fc": _torch_weight(W["fc"]).numpy(), "hidden_norm": W["hidden_norm"].double().numpy(),
+           "norm": W["norm"].double().numpy(),
+           "layers": [{k: (_torch_weight(v).numpy() if k in synth.PROJ_TENSORS else v.double().numpy())
+                       for k, v in L.items()} for L in W["layers"]]}
+    D2 = O.Drafter(dataclasses.replace(cfg, weight_dtype="f32"), W64)
+    taps, noise, pos = _inputs(cfg, 9)
+    assert rel_err(D.forward_full(taps, noise, pos), D2.forward_full(taps, noise, pos)) < 1e-14
+
+
+# ------------------------------------------------------------- brute force on a micro drafter
+def _scalar_forward(cfg, W, taps, noise, pos, inv, mscale):
+    """Scalar Python loops, no numpy linear algebra."""
+    H, d, eps, Hq, Hkv, I = cfg.hidden, cfg.head_dim, cfg.rms_eps, cfg.n_heads, cfg.n_kv_heads, cfg.intermediate
+    G = Hq // Hkv
+
+    def mat(w):
+        return _torch_weight(w).tolist()
+
+    def lin(Wm, x):
+        return [sum(Wm[o][i] * x[i] for i in range(len(x))) for o in range(len(Wm))]
+
+    def norm(x, g):
+        r = 1.0 / math.sqrt(sum(v * v for v in x) / len(x) + eps)
+        return [g[i] * x[i] * r for i in range(len(x))]
+
+    def rope(x, p):
+        half = d // 2
+        out = [0.0] * d
+        for j in range(half):
+            t = p * inv[j]
+            out[j] = mscale * (x[j] * math.cos(t) - x[j + half] * math.sin(t))
+            out[j + half] = mscale * (x[j + half] * math.cos(t) + x[j] * math.sin(t))
+        return out
+
+    ctx = len(taps)
+    fc = mat(W["fc"])
+    feats = [norm(lin(fc, list(taps[r])), W["hidden_norm"].tolist()) for r in range(ctx)]
+    hs = [list(noise[i]) for i in range(len(noise))]
+    for L in W["layers"]:
+        Wq, Wk, Wv, Wo = mat(L["q"]), mat(L["k"]), mat(L["v"]), mat(L["o"])
+        Wg, Wu, Wd = mat(L["gate"]), mat(L["up"]), mat(L["down"])
+        qn, kn = L["q_norm"].tolist(), L["k_norm"].tolist()
+        keys, vals = [], []
+        for r in range(ctx):
+            k, v = lin(Wk, feats[r]), lin(Wv, feats[r])
+            keys.append([rope(norm(k[g * d:(g + 1) * d], kn), pos[r]) for g in range(Hkv)])
+            vals.append([v[g * d:(g + 1) * d] for g in range(Hkv)])
+        xs = [norm(h, L["input_ln"].tolist()) for h in hs]
+        qs = []
+        for i, x in enumerate(xs):
+            q, k, v = lin(Wq, x), lin(Wk, x), lin(Wv, x)
+            qs.append([rope(norm(q[h * d:(h + 1) * d], qn), pos[ctx + i]) for h in range(Hq)])
+            keys.append([rope(norm(k[g * d:(g + 1) * d], kn), pos[ctx + i]) for g in range(Hkv)])
+            vals.append([v[g * d:(g + 1) * d] for g in range(Hkv)])
+        new = []
+        for i in range(len(hs)):
+            o = []
+            for h in range(Hq):
+                g = h // G
+                s = [sum(qs[i][h][j] * keys[n][g][j] for j in range(d)) / math.sqrt(d) for n in range(len(keys))]
+                m = max(s)
+                e = [math.exp(z - m) for z in s]
+                z = sum(e)
+                o += [sum(e[n] / z * vals[n][g][j] for n in range(len(keys))) for j in range(d)]
+            h1 = [a + b for a, b in zip(hs[i], lin(Wo, o))]
+            y = norm(h1, L["post_ln"].tolist())
+            gg, uu = lin(Wg, y), lin(Wu, y)
+            act = [gg[j] / (1 + math.exp(-gg[j])) * uu[j] for j in range(I)]
+            new.append([a + b for a, b in zip(h1, lin(Wd, act))])
+        hs = new
+    return np.array([norm(h, W["norm"].tolist()) for h in hs])
+
+
+def test_brute_force_micro():
+    cfg = synth.DraftConfig(n_layers=1, hidden=8, n_heads=2, n_kv_heads=1, head_dim=4,
+                            intermediate=8, n_taps=2, block=2, weight_dtype="f32",
+                            kv_dtype="f32", rope_theta=100.0)
+    D, W = _drafter(cfg, seed=9)
+    g = torch.Generator().manual_seed(3)
+    taps = torch.randn(2, 16, generator=g, dtype=torch.float64).numpy()
+    noise = torch.randn(2, 8, generator=g, dtype=torch.float64).numpy()
+    pos = [0, 1, 2, 3]
+    ref = _scalar_forward(cfg, W, taps, noise, pos, list(D.inv_freq), D.mscale)
+    assert rel_err(D.forward_full(taps, noise, pos), ref) < 1e-12
+
+
+# ------------------------------------------------------------- planted mistakes are caught
+def _micro_vs_torch(cfg):
+    D, W = _drafter(cfg)
+    taps, noise, pos = _inputs(cfg, 11)
+    return rel_err(D.forward_full(taps, noise, pos),
+                   torch_forward(cfg, W, taps, noise, pos, D.inv_freq, D.mscale))
+
+
+def test_planted_rope_direction_error_is_caught(monkeypatch):
+    good = O.rope_neox
+    monkeypatch.setattr(O, "rope_neox", lambda x, pos, inv, m: good(x, -np.asarray(pos), inv, m))
+    assert _micro_vs_torch(MICRO) > 1e-3
+
+
+def test_planted_rope_pair_shift_is_caught(monkeypatch):
+    good = O.rope_neox
+    monkeypatch.setattr(O, "rope_neox", lambda x, pos, inv, m: good(x, pos, np.roll(inv, 1), m))
+    assert _micro_vs_torch(MICRO) > 1e-3
+
+
+def test_planted_gqa_map_error_is_caught(monkeypatch):
+    cfg = MICRO
+    G = cfg.n_heads // cfg.n_kv_heads
+
+    def bad_attention(self, q, keys, vals):
+        b = q.shape[0]
+        out = np.empty((b, cfg.n_heads, cfg.head_dim))
+        for h in range(cfg.n_heads):
+            g = h % cfg.n_kv_heads          # wrong map
+            s = (q[:, h, :] @ keys[:, g, :].T) / math.sqrt(cfg.head_dim)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            out[:, h, :] = (p / p.sum(axis=1, keepdims=True)) @ vals[:, g, :]
+        return out.reshape(b, -1)
+    assert G > 1 and cfg.n_kv_heads > 1
+    monkeypatch.setattr(O.Drafter, "attention", bad_attention)
+    assert _micro_vs_torch(cfg) > 1e-3
+
+
+def test_planted_missing_k_norm_is_caught(monkeypatch):
+    good = O.Drafter.ctx_kv
+
+    def bad(self, li, feats, pos):
+        L = self.layers[li]
+        saved = L["k_norm"]
+        L["k_norm"] = saved * 1.5
+        try:
+            return good(self, li, feats, pos)
+        finally:
+            L["k_norm"] = saved
+    monkeypatch.setattr(O.Drafter, "ctx_kv", bad)
+    assert _micro_vs_torch(MICRO) > 1e-3
+
+
+def test_planted_transposed_operand_is_caught(monkeypatch):
+    cfg = dataclasses.replace(MICRO, n_taps=1)      # fc is square: a transpose still runs
+    good = O.Drafter.ctx_features
+
+    def bad(self, taps):
+        c = np.asarray(taps, dtype=np.float64) @ self.fc
+        return O.rms_norm(c, self.hidden_norm, self.cfg.rms_eps)
+    monkeypatch.setattr(O.Drafter, "ctx_features", bad)
+    assert _micro_vs_torch(cfg) > 1e-3
