@@ -1,0 +1,333 @@
+#!/usr/bin/env python
+"""Benchmark of the DFlash drafting round on GB300.
+
+A step is one drafting round of the 8-layer hidden-2048 drafter (GQA 32:4,
+head_dim 128, SwiGLU 6144, 5 taps, bf16 weights and KV, plain RoPE): ingest
+of t ~ U{1..16} newly committed context rows into a cache that starts at
+8192 rows, then the gamma=16 block forward over the cached context.
+
+value  = rounds/s with inputs resident in HBM (CUDA events, launching stream)
+e2e    = rounds/s through the public API with pinned HOST inputs: each step
+         copies its taps and noise host->device and reads the drafted hidden
+         states back, all inside the timed region
+roofline = the projection kernel (weight-streaming GEMM, the dominant
+         kernel): algorithmic bytes per launch / mean launch time, from CUDA
+         event pairs the library records around each launch of a profiled
+         pass of the same steps
+cpu_baseline = the f64 CPU oracle on this host's cores, a bounded sample of
+         the same workload (one-time cache build excluded)
+
+Multi-GPU: ranks are independent replicas (sequences shard with no exchange);
+value sums all ranks' rounds over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "draft rounds/s (γ=16 block fwd over cached ctx KV); % of HBM roofline"
+DEFAULT_WORKLOAD = "qwen3_8l_ctx8192"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-rounds", type=int, default=3)
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d["hbm_gbs"], "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out = self.proc.communicate(timeout=10)[0]
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        loaded = [s for s in sm if smax and s >= 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_rounds(wl, steps: int, warmup: int, budget_s: float = None):
+    """Time the f64 oracle on this host: cache built to the workload's context
+    (untimed), then `warmup` + `steps` rounds of ingest(t) + forward_round."""
+    import numpy as np
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle import dflash_oracle as O
+    from _common import oracle_weights
+    from speculative_decoding_block_ingest_gb300 import synth
+    cfg = wl.cfg
+    D = O.Drafter(cfg, oracle_weights(synth.make_weights(cfg)))
+    kv = O.DraftKV(D)
+    ctx = wl.ctx_lengths()[0]
+    for r0 in range(0, ctx, 2048):
+        n = min(2048, ctx - r0)
+        kv.ingest(0, synth.taps_rows(cfg, 0, r0, n).double().numpy(), list(range(r0, r0 + n)))
+    counts = wl.ingest_counts(warmup + steps)
+    length = ctx
+    done = 0
+    t_timed = 0.0
+    for k in range(warmup + steps):
+        t = counts[k][0]
+        taps = synth.taps_rows(cfg, 0, length, t).double().numpy()
+        noise = synth.noise_rows(cfg, 0, k).double().numpy()
+        t0 = time.perf_counter()
+        kv.ingest(0, taps, list(range(length, length + t)))
+        length += t
+        kv.forward_round([0], noise[None], np.arange(length, length + 16)[None])
+        dt = time.perf_counter() - t0
+        if k >= warmup:
+            t_timed += dt
+            done += 1
+            if budget_s is not None and t_timed > budget_s:
+                break
+    return done, t_timed
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, wl):
+    done, secs = oracle_rounds(wl, args.steps, args.warmup)
+    value = done / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": args.gpus,
+            "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * secs / done, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+            "config": workload_config(wl),
+            "cpu_baseline": {"value": value, "unit": "rounds/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": f"{done} full rounds (ingest t~U{{1..16}} + 16-row forward) after a "
+                                       f"{wl.ctx}-row cache build"},
+            "e2e": {"value": value, "unit": "rounds/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def workload_config(wl):
+    c = wl.cfg
+    return {"workload": wl.name, "layers": c.n_layers, "hidden": c.hidden, "heads": f"{c.n_heads}:{c.n_kv_heads}",
+            "head_dim": c.head_dim, "intermediate": c.intermediate, "taps": c.n_taps, "block": c.block,
+            "batch": wl.batch, "ctx": wl.ctx, "ingest_rows": f"U{{{wl.ingest_lo}..{wl.ingest_hi}}}",
+            "weights": c.weight_dtype, "kv": c.kv_dtype, "rope": c.rope_type,
+            "l2": "no flush: every round streams >1 GB of weights and KV, far above the 129 MB L2"}
+
+
+# ---------------------------------------------------------------- GPU leg
+def main():
+    args = parse()
+    from speculative_decoding_block_ingest_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return
+
+    import torch
+    from speculative_decoding_block_ingest_gb300 import dflash
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+    cfg = wl.cfg
+    if wl.batch != 1:
+        raise SystemExit("bench.py times the single-sequence drafting round")
+    K, Wm = args.steps, args.warmup
+    counts = [c[0] for c in wl.ingest_counts(Wm + K)]
+    ctx = wl.ctx
+    SLOTS = 3                                    # device-timed, e2e, profiled passes
+    grow = sum(counts) + 16
+    max_len = ctx + grow + 64
+    pages_per = (max_len + 63) // 64
+    dr = dflash.Drafter(cfg, synth.make_weights(cfg), max_seqs=SLOTS, max_pages=SLOTS * pages_per,
+                        max_seq_len=max_len, max_batch=1, max_ingest_rows=512, device=dev)
+    stream = torch.cuda.current_stream()
+    # untimed cache build: the same ctx rows into every slot
+    per_call = 512 // SLOTS
+    for r0 in range(0, ctx, per_call):
+        n = min(per_call, ctx - r0)
+        taps = synth.taps_rows(cfg, 0, r0, n).to(dev)
+        dr.ingest(list(range(SLOTS)), [n] * SLOTS, list(range(r0, r0 + n)) * SLOTS,
+                  torch.cat([taps] * SLOTS))
+    torch.cuda.synchronize()
+    # per-step inputs, resident in HBM
+    taps_steps, noise_steps, lens = [], [], []
+    length = ctx
+    for k in range(Wm + K):
+        taps_steps.append(synth.taps_rows(cfg, 0, length, counts[k]).to(dev))
+        noise_steps.append(synth.noise_rows(cfg, 0, k)[None].to(dev))
+        lens.append(length)
+        length += counts[k]
+    out = torch.empty(1, 16, cfg.hidden, device=dev)
+
+    def step(slot, k):
+        t, L0 = counts[k], lens[k]
+        dr.ingest([slot], [t], list(range(L0, L0 + t)), taps_steps[k])
+        dr.forward_round([slot], list(range(L0 + t, L0 + t + 16)), noise_steps[k], out)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-timed pass (slot 0)
+    for k in range(Wm):
+        step(0, k)
+    clocks = ClockSampler(local)
+    time.sleep(0.3)
+    barrier()
+    n0 = dr.launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    ev0.record(stream)
+    for k in range(Wm, Wm + K):
+        step(0, k)
+    ev1.record(stream)
+    barrier()
+    clocks.mark(False)
+    launches = dr.launch_count() - n0
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * K / (ms / 1e3)
+
+    # ---- end-to-end pass (slot 1): pinned host inputs, copies inside the timed region
+    host_taps = [t.cpu().pin_memory() for t in taps_steps]
+    host_noise = [n.cpu().pin_memory() for n in noise_steps]
+    host_out = torch.empty(1, 16, cfg.hidden).pin_memory()
+    dev_taps = torch.empty(16, cfg.n_taps * cfg.hidden, device=dev)
+    dev_noise = torch.empty(1, 16, cfg.hidden, device=dev)
+
+    def step_e2e(k):
+        t, L0 = counts[k], lens[k]
+        dt = dev_taps[:t]
+        dt.copy_(host_taps[k], non_blocking=True)
+        dev_noise.copy_(host_noise[k], non_blocking=True)
+        dr.ingest([1], [t], list(range(L0, L0 + t)), dt)
+        dr.forward_round([1], list(range(L0 + t, L0 + t + 16)), dev_noise, out)
+        host_out.copy_(out, non_blocking=True)
+
+    for k in range(Wm):
+        step_e2e(k)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(Wm, Wm + K):
+        step_e2e(k)
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    h2d = sum(counts[Wm:]) * cfg.n_taps * cfg.hidden * 4 / K + 16 * cfg.hidden * 4
+    d2h = 16 * cfg.hidden * 4
+
+    # ---- profiled pass (slot 2): per-launch event pairs, same steps
+    for k in range(Wm):
+        step(2, k)
+    barrier()
+    dr.profile(True)
+    for k in range(Wm, Wm + K):
+        step(2, k)
+    barrier()
+    prof = dr.profile_read()
+    dr.profile(False)
+    dr.device_status()
+    g_n, g_ms, g_b = prof["gemm"]
+    peak, peak_kind = peaks()
+    achieved = (g_b / 1e9) / (g_ms / 1e3) if g_ms > 0 else 0.0
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": None, "kernel": "gemm_swapab (all projections)",
+                "launches": g_n, "bytes_per_launch": g_b / max(g_n, 1), "peak_source": peak_kind}
+    breakdown = {k: {"launches": n, "ms_per_step": m / K, "GB/s": (b / 1e9) / (m / 1e3) if m else None}
+                 for k, (n, m, b) in prof.items()}
+
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+        return
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        done, secs = oracle_rounds(wl, args.cpu_rounds, 0)
+        cpu = {"value": done / secs, "unit": "rounds/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{done} rounds (ingest t~U{{1..16}} + 16-row forward over the {ctx}-row cache), "
+                         f"f64 numpy on host cores; cache build excluded"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded N(0,1/fan_in) weights, N(0,1) taps/noise)",
+        "config": workload_config(wl), "roofline": roofline, "cpu_baseline": cpu,
+        "e2e": {"value": world * K / (ms_e2e / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "clocks": clk, "gpu_launches": launches,
+        "drafted_tokens_per_s": 15 * value, "block_rows_per_s": 16 * value,
+        "kernel_breakdown": breakdown,
+    }
+    print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,205 @@
+/*
+ * dflash.h -- C ABI of the GB300 DFlash drafter round.
+ *
+ * The DFlash drafter (memra_engine::dflash module summary) is a small
+ * Qwen3-class transformer that drafts a block of 16 tokens in ONE non-causal
+ * forward, conditioned on the target model's hidden states at n tapped layers
+ * (concatenated, then fc, then hidden_norm).  A drafting round has two halves:
+ *
+ *   dflash_ingest_ctx     appends newly committed context rows to the
+ *                         per-layer draft KV cache (memra_engine::dflash::
+ *                         DflashDraft, items ctx_features and ingest_ctx);
+ *   dflash_forward_round  runs the 16 block rows through every layer over the
+ *                         cached context K/V and returns the final normed
+ *                         hidden states (DflashDraft, item forward_round).
+ *
+ * dflash_forward_full is the first-light path of the DflashDraft page (item
+ * ctx_features, whose text carries the forward contract): context K/V are
+ * recomputed on every call and no cache state is touched.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Device pointers are CUDA device addresses on the device that was
+ *    current when dflash_create ran; host pointers are ordinary host memory
+ *    that the call reads before it returns.
+ *  - Calls are asynchronous on the given stream (a cudaStream_t passed as
+ *    void*, NULL = the legacy default stream).  Calls on one handle must be
+ *    issued on one stream, or ordered by the caller.
+ *  - The library never allocates device memory: the caller allocates the
+ *    workspace (dflash_workspace_bytes) and owns every buffer.
+ *  - Every call validates all of its arguments before it launches anything.
+ *    On error it changes no state and returns a negative DFLASH_ERR_* code;
+ *    dflash_last_error() gives a message (thread-local).  This mirrors the
+ *    Result<_, Box<dyn Error>> of every DflashDraft method.
+ *  - Layouts are row-major.  Weights are [out_features, in_features] (the
+ *    nn.Linear convention of the checkpoint that DflashDraft::load reads);
+ *    head h of a projection occupies rows [h*d, (h+1)*d); tap k occupies
+ *    taps columns [k*H, (k+1)*H).
+ */
+#ifndef DFLASH_H
+#define DFLASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dflash_handle dflash_t;
+
+enum dflash_status {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = -1,  /* bad pointer, shape, id or count           */
+  DFLASH_ERR_CAPACITY = -2,     /* pages, rows, batch or workspace too small  */
+  DFLASH_ERR_CUDA = -3,         /* a CUDA runtime call failed                 */
+  DFLASH_ERR_TIMEOUT = -4,      /* a bounded device-side wait gave up         */
+  DFLASH_ERR_UNSUPPORTED = -5   /* a shape or format this build does not run  */
+};
+
+enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_FP8_E4M3 = 2 };
+enum dflash_rope { DFLASH_ROPE_PLAIN = 0, DFLASH_ROPE_YARN = 1 };
+
+/* Drafter shape and capacity (the pages' DflashCfg plus storage sizes). */
+typedef struct dflash_config {
+  int32_t n_layers;      /* L                                              */
+  int32_t hidden;        /* H, a multiple of 128                           */
+  int32_t n_heads;       /* Hq query heads                                 */
+  int32_t n_kv_heads;    /* Hkv, divides Hq, Hq/Hkv <= 8                   */
+  int32_t head_dim;      /* d: 64 or 128                                   */
+  int32_t intermediate;  /* I (SwiGLU), a multiple of 64                   */
+  int32_t n_taps;        /* n tapped target layers                         */
+  int32_t block;         /* b, must be 16                                  */
+  double rms_eps;        /* RMSNorm epsilon                                */
+  double rope_theta;     /* RoPE base                                      */
+  int32_t rope_type;     /* DFLASH_ROPE_PLAIN or DFLASH_ROPE_YARN          */
+  int32_t yarn_original_max_pos;
+  double yarn_factor, yarn_beta_fast, yarn_beta_slow;
+  int32_t weight_dtype;  /* DFLASH_F32, DFLASH_BF16 or DFLASH_FP8_E4M3     */
+  int32_t kv_dtype;      /* DFLASH_F32 or DFLASH_BF16                      */
+  int32_t page_size;     /* KV page rows, must be 64                       */
+  int32_t max_seqs;      /* sequence slots: ids 0 .. max_seqs-1            */
+  int32_t max_pages;     /* pages in the shared pool (all seqs, all calls) */
+  int32_t max_seq_len;   /* committed rows + 16 a sequence may reach       */
+  int32_t max_batch;     /* n_seq per dflash_forward_round, <= 64          */
+  int32_t max_ingest_rows; /* sum of t per dflash_ingest_ctx, <= 512       */
+} dflash_config;
+
+/* One decoder layer's tensors (DflashLayer).  Projections have the dtype
+ * weight_dtype; *_scale are per-output-row f32 scales, required for
+ * DFLASH_FP8_E4M3 and ignored otherwise (spark_model::layers::dflash_head,
+ * DflashQuantization).  Norm gains are f32. */
+typedef struct dflash_layer_weights {
+  const void *q, *k, *v, *o, *gate, *up, *down;
+  const float *q_scale, *k_scale, *v_scale, *o_scale, *gate_scale, *up_scale, *down_scale;
+  const float *q_norm;    /* [d]  */
+  const float *k_norm;    /* [d]  */
+  const float *input_ln;  /* [H]  */
+  const float *post_ln;   /* [H]  */
+} dflash_layer_weights;
+
+/* Backbone tensors (DflashDraft fields fc, hidden_norm, norm, layers): no fc
+ * bias, no embedding or lm_head (the round reuses the target's). */
+typedef struct dflash_weights {
+  const void *fc;                     /* [H, n_taps*H]                   */
+  const float *fc_scale;              /* [H] for fp8                     */
+  const float *hidden_norm;           /* [H]                             */
+  const float *norm;                  /* [H]                             */
+  const dflash_layer_weights *layers; /* host array of n_layers          */
+} dflash_weights;
+
+/* Bytes of device workspace the handle needs for this config (256-byte
+ * aligned start required).  Holds the repacked weights, the paged KV pools,
+ * page tables, activations and reduction scratch. */
+int dflash_workspace_bytes(const dflash_config *cfg, size_t *bytes);
+
+/* Validate cfg, carve the caller's workspace, copy and repack the weights
+ * into it (the caller may free its weight buffers once the stream has
+ * passed this call), resolve every kernel once and build the RoPE table.
+ * Returns a handle in *out. */
+int dflash_create(const dflash_config *cfg, const dflash_weights *w, void *workspace,
+                  size_t workspace_bytes, void *stream, dflash_t **out);
+
+/* Append newly committed context rows to n_seq sequences (DflashDraft,
+ * ctx_features then ingest_ctx): per row, feats = hidden_norm(fc(taps)); per
+ * layer K = rope(k_norm(W_k feats)) * mscale and V = W_v feats are written at
+ * rows len .. len+t-1 of that sequence, then len += t.
+ *   seq_ids   host [n_seq]  distinct slot ids
+ *   t_per_seq host [n_seq]  rows per sequence (0 allowed)
+ *   pos_new   host [sum t]  absolute positions, sequence by sequence
+ *   taps      device f32 [sum t, n_taps*H], rows in the same order */
+int dflash_ingest_ctx(dflash_t *h, int32_t n_seq, const int32_t *seq_ids,
+                      const int32_t *t_per_seq, const int32_t *pos_new,
+                      const float *taps, void *stream);
+
+/* One drafting forward of the 16-row block of each of n_seq sequences over
+ * its cached context (DflashDraft, forward_round).  Block K/V land in the
+ * cache rows len .. len+15 for the duration of the call only; len is not
+ * changed.
+ *   seq_ids   host [n_seq]
+ *   pos_block host [n_seq, 16] absolute positions of the block rows
+ *   noise_emb device f32 [n_seq, 16, H] (target embeddings of the block)
+ *   out       device f32 [n_seq, 16, H] final normed hidden states */
+int dflash_forward_round(dflash_t *h, int32_t n_seq, const int32_t *seq_ids,
+                         const int32_t *pos_block, const float *noise_emb,
+                         float *out, void *stream);
+
+/* First-light forward: full non-causal attention over [ctx features ;
+ * block] with the context K/V recomputed (no cache state touched).
+ *   taps      device f32 [ctx, n_taps*H]
+ *   noise_emb device f32 [16, H]
+ *   pos       host [ctx + 16]: ctx rows' positions then the block rows'
+ *   out       device f32 [16, H] */
+int dflash_forward_full(dflash_t *h, int32_t ctx, const float *taps, const float *noise_emb,
+                        const int32_t *pos, float *out, void *stream);
+
+/* Drop a sequence's cache (len = 0, pages back to the pool). */
+int dflash_seq_reset(dflash_t *h, int32_t seq_id);
+
+/* Committed rows of a sequence. */
+int dflash_seq_len(dflash_t *h, int32_t seq_id, int64_t *len);
+
+/* Copy cached rows row0 .. row0+nrows-1 of one layer of a sequence out of
+ * the paged pools as f32: k_out, v_out device [nrows, Hkv, d] (K normed and
+ * roped, V raw).  Inspection entry point for tests. */
+int dflash_kv_read(dflash_t *h, int32_t seq_id, int32_t layer, int32_t row0, int32_t nrows,
+                   float *k_out, float *v_out, void *stream);
+
+/* Synchronise the handle's last stream and report the device error word
+ * (0 = none; else a DFLASH_ERR_* code a kernel recorded). */
+int dflash_device_status(dflash_t *h, void *stream);
+
+/* Kernel kinds reported by the measurement calls below. */
+enum dflash_kernel_kind {
+  DFLASH_KERNEL_GEMM = 0,       /* weight-streaming projections (fc, K/V, QKV, O, gate/up, down) */
+  DFLASH_KERNEL_ATTENTION = 1,  /* split-KV block attention over the paged cache                 */
+  DFLASH_KERNEL_COMBINE = 2,    /* merge of the split-KV partial softmaxes                        */
+  DFLASH_KERNEL_INIT = 3,       /* per-call descriptor upload and residual / operand set-up       */
+  DFLASH_KERNEL_NORM = 4,       /* final RMSNorm                                                  */
+  DFLASH_KERNEL_KINDS = 5
+};
+
+/* Measurement (not needed to draft).  While enabled, every kernel launch
+ * of the handle is bracketed by a CUDA event pair on its stream, tagged with
+ * the launch's algorithmic bytes (weights, cached K/V, operands and outputs
+ * it must move).  Enabling or disabling discards earlier records (it
+ * synchronises the device if records exist). */
+int dflash_profile_enable(dflash_t *h, int32_t enable);
+
+/* Totals over the records of one kernel kind: launches, summed device time
+ * in ms and summed algorithmic bytes (waits for the recorded events). */
+int dflash_profile_read(dflash_t *h, int32_t kind, int64_t *launches, double *ms, double *bytes);
+
+/* Kernel launches issued by the handle since it was created. */
+int dflash_launch_count(dflash_t *h, int64_t *launches);
+
+/* Release the handle (the workspace stays the caller's). */
+void dflash_destroy(dflash_t *h);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char *dflash_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_H */

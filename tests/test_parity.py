@@ -1,0 +1,173 @@
+"""GPU parity: the CUDA path through the C ABI against the f64 CPU oracle.
+
+Bar (BASELINE tolerances): max|d|/rms(ref) <= 1e-4 for f32 drafters and
+<= 2e-2 for bf16 / fp8-weight drafters; greedy argmax through a seeded
+lm_head agrees on >= 99% of slots.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dflash_oracle as O
+from speculative_decoding_block_ingest_gb300 import synth
+from _common import oracle_weights, rel_err
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def tol(cfg):
+    return 1e-4 if cfg.weight_dtype == "f32" else 2e-2
+
+
+SMALL_BF16 = dataclasses.replace(synth.TINY_F32, weight_dtype="bf16", kv_dtype="bf16", hidden=512,
+                                 n_heads=8, n_kv_heads=2, head_dim=128, intermediate=1024, n_taps=2)
+SMALL_YARN = dataclasses.replace(SMALL_BF16, rope_type="yarn", yarn_factor=8.0, yarn_original_max_pos=256,
+                                 n_heads=4, n_kv_heads=1)
+SMALL_FP8 = dataclasses.replace(SMALL_BF16, weight_dtype="fp8", n_heads=16, n_kv_heads=2)
+SMALL_G8 = dataclasses.replace(SMALL_BF16, n_heads=16, n_kv_heads=2, hidden=1024)
+
+
+def _setup(cfg, **kw):
+    from speculative_decoding_block_ingest_gb300 import dflash
+    W = synth.make_weights(cfg)
+    D = O.Drafter(cfg, oracle_weights(W))
+    dr = dflash.Drafter(cfg, W, device=DEV, **kw)
+    return dr, D
+
+
+def _np(t):
+    return t.detach().double().cpu().numpy()
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY_F32, SMALL_BF16, SMALL_YARN, SMALL_FP8, SMALL_G8],
+                         ids=["tiny_f32", "small_bf16", "small_yarn", "small_fp8", "small_g8"])
+def test_forward_full_matches_oracle(cfg):
+    dr, D = _setup(cfg, max_seqs=1, max_pages=32, max_seq_len=1024, max_batch=1, max_ingest_rows=128)
+    for ctx in (0, 1, 64, 200):
+        taps = synth.taps_rows(cfg, 5, 0, ctx)
+        noise = synth.noise_rows(cfg, 5, ctx)
+        pos = list(range(ctx + 16))
+        got = dr.forward_full(taps.to(DEV), noise.to(DEV), pos)
+        torch.cuda.synchronize()
+        dr.device_status()
+        ref = D.forward_full(taps.double().numpy(), noise.double().numpy(), pos)
+        assert rel_err(_np(got), ref) <= tol(cfg), ctx
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY_F32, SMALL_YARN, SMALL_G8], ids=["tiny_f32", "small_yarn", "small_g8"])
+def test_batched_ragged_rounds_match_oracle(cfg):
+    """Three sequences with ragged lengths (len = 0, 1, 63 mod 64), chunked
+    ingest interleaved with rounds; every round compared with the oracle and
+    the cached K/V read back and compared row by row."""
+    dr, D = _setup(cfg, max_seqs=4, max_pages=64, max_seq_len=1024, max_batch=4, max_ingest_rows=256)
+    kv = O.DraftKV(D)
+    seqs = [2, 0, 3]
+    lens = {2: 0, 0: 0, 3: 0}
+    targets = [[64, 1, 63], [65, 128, 127], [70, 130, 200]]
+    for rnd, tgt in enumerate(targets):
+        ts = [tg - lens[s] for s, tg in zip(seqs, tgt)]
+        pos_new, taps = [], []
+        for s, t in zip(seqs, ts):
+            taps.append(synth.taps_rows(cfg, s, lens[s], t))
+            pos_new += list(range(lens[s], lens[s] + t))
+        taps_all = torch.cat(taps)
+        dr.ingest(seqs, ts, pos_new, taps_all.to(DEV))
+        r = 0
+        for s, t in zip(seqs, ts):
+            kv.ingest(s, taps_all[r:r + t].double().numpy(), pos_new[r:r + t])
+            r += t
+            lens[s] += t
+        for s in seqs:
+            assert dr.seq_len(s) == lens[s] == kv.length(s)
+        noise = torch.stack([synth.noise_rows(cfg, s, rnd) for s in seqs])
+        pos_block = [p for s in seqs for p in range(lens[s], lens[s] + 16)]
+        got = dr.forward_round(seqs, pos_block, noise.to(DEV))
+        torch.cuda.synchronize()
+        dr.device_status()
+        ref = kv.forward_round(seqs, noise.double().numpy(), np.array(pos_block).reshape(len(seqs), 16))
+        for i in range(len(seqs)):
+            assert rel_err(_np(got[i]), ref[i]) <= tol(cfg), (rnd, i)
+        for s in seqs:
+            assert dr.seq_len(s) == lens[s]           # a round commits nothing
+    for s in seqs:
+        for li in range(cfg.n_layers):
+            k, v = dr.kv_read(s, li, 0, lens[s])
+            torch.cuda.synchronize()
+            assert rel_err(_np(k), kv.k[s][li]) <= tol(cfg) / 4
+            assert rel_err(_np(v), kv.v[s][li]) <= tol(cfg) / 4
+
+
+def test_round_equals_forward_full_on_gpu():
+    cfg = SMALL_G8
+    dr, _ = _setup(cfg, max_seqs=2, max_pages=32, max_seq_len=1024, max_batch=1, max_ingest_rows=64)
+    ctx = 150
+    taps = synth.taps_rows(cfg, 1, 0, ctx)
+    noise = synth.noise_rows(cfg, 1, 0)
+    pos = list(range(ctx + 16))
+    full = dr.forward_full(taps.to(DEV), noise.to(DEV), pos)
+    for lo in range(0, ctx, 64):
+        hi = min(ctx, lo + 64)
+        dr.ingest([1], [hi - lo], pos[lo:hi], taps[lo:hi].to(DEV))
+    rnd = dr.forward_round([1], pos[ctx:], noise[None].to(DEV))
+    torch.cuda.synchronize()
+    assert rel_err(_np(rnd[0]), _np(full)) <= 2e-3
+
+
+def test_batch_independence_on_gpu():
+    cfg = SMALL_BF16
+    dr, _ = _setup(cfg, max_seqs=3, max_pages=32, max_seq_len=512, max_batch=3, max_ingest_rows=200)
+    lens = [40, 97, 130]
+    for s, n in enumerate(lens):
+        dr.ingest([s], [n], list(range(n)), synth.taps_rows(cfg, s, 0, n).to(DEV))
+    noise = torch.stack([synth.noise_rows(cfg, s, 0) for s in range(3)]).to(DEV)
+    pos = [p for n in lens for p in range(n, n + 16)]
+    both = dr.forward_round([0, 1, 2], pos, noise)
+    solo = dr.forward_round([1], pos[16:32], noise[1:2])
+    torch.cuda.synchronize()
+    assert rel_err(_np(both[1]), _np(solo[0])) <= 1e-5
+
+
+def test_argmax_agreement_small():
+    cfg = SMALL_G8
+    dr, D = _setup(cfg, max_seqs=1, max_pages=32, max_seq_len=1024, max_batch=1, max_ingest_rows=128)
+    lm = synth.lm_head(cfg, vocab=4096).double().numpy()
+    agree = total = 0
+    for k in range(6):
+        ctx = 30 + 40 * k
+        taps = synth.taps_rows(cfg, 10 + k, 0, ctx)
+        noise = synth.noise_rows(cfg, 10 + k, 0)
+        pos = list(range(ctx + 16))
+        got = _np(dr.forward_full(taps.to(DEV), noise.to(DEV), pos))
+        ref = D.forward_full(taps.double().numpy(), noise.double().numpy(), pos)
+        agree += int(np.sum(O.argmax_tokens(got, lm) == O.argmax_tokens(ref, lm)))
+        total += 16
+    assert agree / total >= 0.99
+
+
+def test_invalid_calls_change_no_state():
+    from speculative_decoding_block_ingest_gb300 import dflash
+    cfg = SMALL_BF16
+    dr, _ = _setup(cfg, max_seqs=2, max_pages=4, max_seq_len=256, max_batch=2, max_ingest_rows=64)
+    dr.ingest([0], [10], list(range(10)), synth.taps_rows(cfg, 0, 0, 10).to(DEV))
+    with pytest.raises(dflash.DflashError) as e:
+        dr.ingest([0, 0], [1, 1], [10, 11], synth.taps_rows(cfg, 0, 10, 2).to(DEV))
+    assert e.value.code == dflash.ERR_INVALID_ARG
+    with pytest.raises(dflash.DflashError) as e:
+        dr.ingest([5], [1], [0], synth.taps_rows(cfg, 0, 0, 1).to(DEV))
+    assert e.value.code == dflash.ERR_INVALID_ARG
+    with pytest.raises(dflash.DflashError) as e:       # past max_seq_len
+        dr.ingest([0], [240], list(range(10, 250)), synth.taps_rows(cfg, 0, 10, 240).to(DEV))
+    assert e.value.code == dflash.ERR_CAPACITY
+    with pytest.raises(dflash.DflashError) as e:       # out of pages (4 pages = 256 rows)
+        dr.ingest([1], [200], list(range(200)), synth.taps_rows(cfg, 1, 0, 200).to(DEV))
+    assert e.value.code in (dflash.ERR_CAPACITY,)
+    assert dr.seq_len(0) == 10 and dr.seq_len(1) == 0
+    dr.ingest([0], [0], [], None)                      # t = 0 is a no-op
+    assert dr.seq_len(0) == 10
+    dr.seq_reset(0)
+    assert dr.seq_len(0) == 0
+    torch.cuda.synchronize()
+    dr.device_status()
