@@ -75,7 +75,8 @@ struct Geo {
 struct EpiArgs {
   int kind;
   int layer;
-  int n_tok;
+  int n_tok;                  // token columns of this pass
+  int tok_base;               // first token of this pass (passes hold <= 256 tokens)
   const float* wscale;        // per weight row scale (fp8), or null
   const float* ss_in;         // per token sum of squares -> rsqrt(ss/H+eps) scale; null = 1
   float* ss_out;              // per token sum of squares of the epilogue's output
@@ -166,7 +167,7 @@ static __device__ void epi_heads(const EpiArgs& e, int tile, const float* red, i
   const int tasks = tc * heads_in_tile;
   for (int task = warp; task < tasks; task += kEpiThreads / 32) {
     const int t = task / heads_in_tile, sh = task % heads_in_tile;
-    const int tok = tok0 + t;
+    const int tok = e.tok_base + tok0 + t;      // global token index
     const int hh = (tile * kTileN) / d + sh;   // head index within the tile's GEMM rows
     int layer, kind, head;                     // kind 0 q, 1 k, 2 v
     int pos, slot, row;
@@ -268,7 +269,7 @@ static __device__ void tile_epilogue(const EpiArgs& e, int tile, int c_lo, int c
       // tile rows [0,64) = gate rows, [64,128) = up rows of act columns [64*tile, 64*tile+64)
       const int j = et & 63;
       for (int t = et >> 6; t < tc; t += 2) {
-        const int tok = tok0 + t;
+        const int tok = e.tok_base + tok0 + t;
         const float rs = e.ss_in ? rsqrtf(e.ss_in[tok] / (float)g.H + g.eps) : 1.f;
         const float gv = red[t * (kTileN + 1) + j] * rs;
         const float uv = red[t * (kTileN + 1) + 64 + j] * rs;
@@ -278,7 +279,7 @@ static __device__ void tile_epilogue(const EpiArgs& e, int tile, int c_lo, int c
     } else {  // EPI_FC, EPI_RESID
       const int col = tile * kTileN + f;
       for (int t = 0; t < tc; ++t) {
-        const int tok = tok0 + t;
+        const int tok = e.tok_base + tok0 + t;
         float v = red[t * (kTileN + 1) + f];
         if (e.kind == EPI_RESID) {
           float* hp = e.h + (long)tok * e.h_ld + col;
@@ -299,7 +300,7 @@ static __device__ void tile_epilogue(const EpiArgs& e, int tile, int c_lo, int c
             s += v * v;
           }
           s = warp_sum(s);
-          if (lane == 0) atomicAdd(e.ss_out + tok0 + t, s);
+          if (lane == 0) atomicAdd(e.ss_out + e.tok_base + tok0 + t, s);
         }
       }
     }

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(GemmArgs a) {
         }
         for (int idx = tid; idx < kSimtTok * kTileK; idx += 128) {
           const int t = idx / kTileK, k = idx % kTileK;
-          Xs[idx] = (tok0 + t < a.e.n_tok) ? load_x(a, tok0 + t, kbi * kTileK + k) : 0.f;
+          Xs[idx] = (tok0 + t < a.e.n_tok) ? load_x(a, a.e.tok_base + tok0 + t, kbi * kTileK + k) : 0.f;
         }
         __syncthreads();
 #pragma unroll 4

@@ -17,6 +17,9 @@
 #include <string>
 #include <vector>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "../../include/dflash.h"
 #include "kernels.cuh"
 
@@ -186,6 +189,34 @@ void rope_table(const dflash_config& c, std::vector<double>& inv, float& mscale)
   mscale = (float)(0.1 * std::log(c.yarn_factor) + 1.0);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    ck(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q),
+       "driver entry point cuTensorMapEncodeTiled");
+    if (q != cudaDriverEntryPointSuccess || !p) throw CudaError{"cuTensorMapEncodeTiled unavailable"};
+    fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map over a row-major [rows][cols] matrix, box [box_rows][64] in
+// the 128-byte swizzle (the layout the MMA descriptors expect).
+CUtensorMap make_map_bf16(const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  CUtensorMap m;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = tensor_map_encoder()(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) throw CudaError{"cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")"};
+  return m;
+}
+
 }  // namespace
 
 struct dflash_handle {
@@ -200,6 +231,10 @@ struct dflash_handle {
   cudaStream_t last_stream = nullptr;
   // measurement: kernel launches issued, and (when enabled) per-kind event pairs
   int64_t launches = 0;
+  // tensor maps of the tensor-core projections: weights per GEMM site, operands per buffer
+  std::vector<CUtensorMap> wmap;
+  CUtensorMap xmap_taps, xmap_h, xmap_o, xmap_a;
+  bool use_tc = false;
   bool prof_on = false;
   struct Rec {
     int kind;
@@ -286,37 +321,46 @@ EpiArgs base_epi(dflash_t* h) {
   return e;
 }
 
+// One projection: passes of <= 256 token columns; tensor cores for bf16
+// weights, CUDA cores for f32 weights (and, for now, fp8 weights).
 void run_gemm(dflash_t* h, int site, const void* W, const float* wscale, int N, int K, const void* X,
-              EpiArgs e, cudaStream_t s) {
-  GemmArgs a{};
-  a.W = W;
-  a.N = N;
-  a.K = K;
-  a.X = X;
-  a.x_ld = K;
-  a.x_plane = (long)h->lo.Mt * K;
-  a.x_f32 = h->cfg.weight_dtype == DFLASH_F32;
-  a.n_tiles = N / kTileN;
-  a.p.kb = K / kTileK;
-  a.p.units = a.n_tiles * a.p.kb;
-  a.p.grid = std::min(a.p.units, h->lo.grid_max);
-  a.part = h->at<float>(h->lo.part);
-  a.counters = h->at<int>(h->lo.counters) + (size_t)site * h->lo.max_tiles;
-  e.wscale = wscale;
-  a.e = e;
+              const CUtensorMap* xmap, EpiArgs e, cudaStream_t s) {
   const Geo& g = h->g;
-  const double nt = e.n_tok;
-  double out_b = 0;
-  switch (e.kind) {
-    case EPI_FC: out_b = nt * N * 4; break;
-    case EPI_KV: out_b = nt * N * (g.kvtype == KV_F32 ? 4 : 2); break;
-    case EPI_QKV: out_b = nt * N * (g.kvtype == KV_F32 ? 4 : 2); break;
-    case EPI_RESID: out_b = nt * N * 12; break;
-    default: out_b = nt * N / 2 * 4; break;
+  const int n_all = e.n_tok;
+  for (int base = 0; base < n_all; base += 256) {
+    GemmArgs a{};
+    a.W = W;
+    a.N = N;
+    a.K = K;
+    a.X = X;
+    a.x_ld = K;
+    a.x_plane = (long)h->lo.Mt * K;
+    a.x_f32 = h->cfg.weight_dtype == DFLASH_F32;
+    a.n_tiles = N / kTileN;
+    a.p.kb = K / kTileK;
+    a.p.units = a.n_tiles * a.p.kb;
+    a.p.grid = std::min(a.p.units, h->use_tc ? h->n_sm : h->lo.grid_max);
+    a.part = h->at<float>(h->lo.part);
+    a.counters = h->at<int>(h->lo.counters) + (size_t)site * h->lo.max_tiles;
+    e.wscale = wscale;
+    e.tok_base = base;
+    e.n_tok = std::min(256, n_all - base);
+    a.e = e;
+    const double nt = e.n_tok;
+    double out_b = 0;
+    switch (e.kind) {
+      case EPI_FC: out_b = nt * N * 4; break;
+      case EPI_KV: out_b = nt * N * (g.kvtype == KV_F32 ? 4 : 2); break;
+      case EPI_QKV: out_b = nt * N * (g.kvtype == KV_F32 ? 4 : 2); break;
+      case EPI_RESID: out_b = nt * N * 12; break;
+      default: out_b = nt * N / 2 * 4; break;
+    }
+    const double bytes =
+        (double)N * K * esize_w(g.wtype) + (g.wtype == W_FP8 ? N * 4.0 : 0.0) + nt * K * 4 + out_b;
+    Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
+    if (h->use_tc) launch_gemm_tc(a, &h->wmap[site], xmap, s);
+    else launch_gemm_simt(a, s);
   }
-  const double bytes = (double)N * K * esize_w(g.wtype) + (g.wtype == W_FP8 ? N * 4.0 : 0.0) + nt * K * 4 + out_b;
-  Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
-  launch_gemm_simt(a, s);
   ck(cudaGetLastError(), "gemm launch");
 }
 
@@ -359,7 +403,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   e.op_plane = (long)h->lo.Mt * g.H;
   const bool fp8 = h->cfg.weight_dtype == DFLASH_FP8_E4M3;
   run_gemm(h, 0, h->at<void>(h->lo.fc), fp8 ? h->at<float>(h->lo.s_fc) : nullptr, g.H, width,
-           h->at<void>(h->lo.op_taps), e, s);
+           h->at<void>(h->lo.op_taps), &h->xmap_taps, e, s);
 
   // K/V of every layer in one projection; epilogue: hidden_norm scale,
   // k head-norm + RoPE, paged write.
@@ -369,7 +413,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   k.ss_in = ss_feat;
   k.kn = h->at<float>(h->lo.kn);
   run_gemm(h, 1, h->at<void>(h->lo.kvall), fp8 ? h->at<float>(h->lo.s_kvall) : nullptr, g.L * g.kv_n, g.H,
-           h->at<void>(h->lo.op_h), k, s);
+           h->at<void>(h->lo.op_h), &h->xmap_h, k, s);
 }
 
 int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens) {
@@ -426,7 +470,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     e.q_out = h->at<void>(h->lo.q);
     run_gemm(h, 2 + 4 * l, h->at<char>(h->lo.qkv) + (size_t)l * g.qkv_n * g.H * ew,
              fp8 ? h->at<float>(h->lo.s_qkv) + (size_t)l * g.qkv_n : nullptr, g.qkv_n, g.H,
-             h->at<void>(h->lo.op_h), e, s);
+             h->at<void>(h->lo.op_h), &h->xmap_h, e, s);
 
     // attention over [cached ctx ; block] K/V, split over keys, then merge
     AttnArgs a{};
@@ -473,7 +517,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     o.op_plane = (long)Mt * g.H;
     run_gemm(h, 3 + 4 * l, h->at<char>(h->lo.o) + (size_t)l * g.H * g.Hq * g.d * ew,
              fp8 ? h->at<float>(h->lo.s_o) + (size_t)l * g.H : nullptr, g.H, g.Hq * g.d,
-             h->at<void>(h->lo.op_o), o, s);
+             h->at<void>(h->lo.op_o), &h->xmap_o, o, s);
 
     // gate/up (interleaved per 64 rows) + SwiGLU
     EpiArgs gu = base_epi(h);
@@ -485,7 +529,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     gu.op_plane = (long)Mt * g.I;
     run_gemm(h, 4 + 4 * l, h->at<char>(h->lo.gu) + (size_t)l * 2 * g.I * g.H * ew,
              fp8 ? h->at<float>(h->lo.s_gu) + (size_t)l * 2 * g.I : nullptr, 2 * g.I, g.H,
-             h->at<void>(h->lo.op_h), gu, s);
+             h->at<void>(h->lo.op_h), &h->xmap_h, gu, s);
 
     // down + residual; operand for the next layer = h * input_ln[l+1]
     EpiArgs dn = base_epi(h);
@@ -501,7 +545,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     dn.op_plane = (long)Mt * g.H;
     run_gemm(h, 5 + 4 * l, h->at<char>(h->lo.down) + (size_t)l * g.H * g.I * ew,
              fp8 ? h->at<float>(h->lo.s_down) + (size_t)l * g.H : nullptr, g.H, g.I,
-             h->at<void>(h->lo.op_a), dn, s);
+             h->at<void>(h->lo.op_a), &h->xmap_a, dn, s);
   }
   {
     Launch L(h, DFLASH_KERNEL_NORM, (double)n_tok * g.H * 8, s);
@@ -748,6 +792,23 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       }
     }
     ck(cudaMemcpyAsync(h->ws + lo.inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s), "rope table");
+    h->use_tc = cfg->weight_dtype == DFLASH_BF16;
+    if (h->use_tc) {
+      const uint64_t Mt2 = 2ull * lo.Mt;
+      h->wmap.resize(lo.n_sites);
+      h->wmap[0] = make_map_bf16(h->ws + lo.fc, H, (uint64_t)g.n * H, kTileN);
+      h->wmap[1] = make_map_bf16(h->ws + lo.kvall, (uint64_t)L * g.kv_n, H, kTileN);
+      for (int l = 0; l < L; ++l) {
+        h->wmap[2 + 4 * l] = make_map_bf16(h->ws + lo.qkv + (size_t)l * g.qkv_n * H * 2, g.qkv_n, H, kTileN);
+        h->wmap[3 + 4 * l] = make_map_bf16(h->ws + lo.o + (size_t)l * H * Hq * d * 2, H, (uint64_t)Hq * d, kTileN);
+        h->wmap[4 + 4 * l] = make_map_bf16(h->ws + lo.gu + (size_t)l * 2 * I * H * 2, 2ull * I, H, kTileN);
+        h->wmap[5 + 4 * l] = make_map_bf16(h->ws + lo.down + (size_t)l * H * I * 2, H, I, kTileN);
+      }
+      h->xmap_taps = make_map_bf16(h->ws + lo.op_taps, Mt2, (uint64_t)g.n * H, 16);
+      h->xmap_h = make_map_bf16(h->ws + lo.op_h, Mt2, H, 16);
+      h->xmap_o = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, 16);
+      h->xmap_a = make_map_bf16(h->ws + lo.op_a, Mt2, I, 16);
+    }
     ck(cudaMemsetAsync(h->ws + lo.btab, 0xff, (size_t)(cfg->max_seqs + 1) * lo.pps * 4, s), "block table");
     ck(cudaMemsetAsync(h->ws + lo.counters, 0, (size_t)lo.n_sites * lo.max_tiles * 4, s), "counters");
     ck(cudaMemsetAsync(h->ws + lo.err, 0, 256, s), "error word");
