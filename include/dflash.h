@@ -190,6 +190,21 @@ int dflash_profile_enable(dflash_t *h, int32_t enable);
  * in ms and summed algorithmic bytes (waits for the recorded events). */
 int dflash_profile_read(dflash_t *h, int32_t kind, int64_t *launches, double *ms, double *bytes);
 
+/* Launch trace (measurement).  While a buffer is set, every tensor-core
+ * projection and attention launch writes, per CTA, 16 u64 words into the next
+ * free region of `device_buffer`: the SM id, the %globaltimer (ns) at entry,
+ * then SM clock cycles since entry at fixed points of the kernel (set-up
+ * done, launch wait passed, last MMA issued, epilogue steps, exit; unused
+ * stamps stay as they were).  Launches that no longer fit are not traced.  NULL stops
+ * tracing.  The buffer is the caller's; the library never reads it. */
+int dflash_trace_begin(dflash_t *h, void *device_buffer, size_t bytes);
+
+/* Traced launches so far: kernel kind (dflash_kernel_kind), CTA count and the
+ * word offset of each launch's region, up to max_launches entries;
+ * *n_launches gets the total. */
+int dflash_trace_launches(dflash_t *h, int32_t max_launches, int32_t *kinds, int32_t *grids, int64_t *offsets,
+                          int32_t *n_launches);
+
 /* Kernel launches issued by the handle since it was created. */
 int dflash_launch_count(dflash_t *h, int64_t *launches);
 

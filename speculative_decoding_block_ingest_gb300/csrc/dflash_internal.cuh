@@ -3,11 +3,18 @@
 // Every projection of the drafter is a "swap-AB" weight-streaming product:
 // the weight's output features are the tile rows (128 per tile) and the
 // (few) token rows are the columns.  A tile's K range is split over CTAs
-// (stream-K over units of 64 K-columns); each contributor writes an f32
-// partial [tokens][128] and the last one to arrive reduces the partials and
-// runs the tile's fused epilogue (norm scale, head RMSNorm + RoPE, SwiGLU,
-// residual, KV-page write).  Both GEMM mainloops (CUDA-core for f32 weights,
-// tcgen05 for bf16/fp8 weights) share this epilogue.
+// (stream-K over units of 64 K-columns).  Each contributor adds its f32
+// partial into the tile's accumulator with fire-and-forget reductions
+// (red.global.add), fences, and takes a ticket; the last one to arrive reads
+// the accumulated tile once (and clears it for the next call) and runs the
+// tile's fused epilogue (norm scale, head RMSNorm + RoPE, SwiGLU, residual,
+// KV-page write).
+//
+// The last arriver's epilogue sits on the kernel's critical path and runs
+// once per SM on cold instruction caches, so it is kept short and loop-shaped:
+// per-token constants (RoPE cos/sin, KV destination rows) are prepared
+// beforehand by the per-call init kernels and the host, and no global load in
+// it waits on another.
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -20,17 +27,47 @@ constexpr int kBlock = 16;        // block rows per sequence (gamma = 16)
 constexpr int kPage = 64;         // KV rows per page
 constexpr int kTileN = 128;       // weight rows per tile
 constexpr int kTileK = 64;        // K columns per unit
+constexpr int kPassTok = 256;     // token columns per GEMM pass (one MMA N)
 constexpr int kMaxBatch = 64;
 constexpr int kMaxIngestRows = 512;
 constexpr int kMaxPtUpdates = 160;
 constexpr int kEpiThreads = 128;  // threads running a tile epilogue
-constexpr int kEpiTokChunk = 32;  // tokens reduced per epilogue pass
+constexpr int kEpiTokChunk = 32;  // tokens per epilogue pass
 constexpr int kEpiBar = 1;        // named barrier id used by the epilogue
+constexpr int kRedFloats = kEpiTokChunk * (kTileN + 1) + kEpiTokChunk;   // epilogue shared scratch
 
 enum WType { W_F32 = 0, W_BF16 = 1, W_FP8 = 2 };
 enum KvType { KV_F32 = 0, KV_BF16 = 1 };
 enum EpiKind { EPI_FC = 0, EPI_KV = 1, EPI_QKV = 2, EPI_RESID = 3, EPI_SWIGLU = 4 };
 enum DevErr { DERR_NONE = 0, DERR_TIMEOUT = 4, DERR_BAD_PAGE = 6 };
+
+// Optional launch trace.  Per CTA, kTraceWords u64: {smid, %globaltimer at
+// entry (ns), then SM clock64 cycles since entry at fixed points 1..14 of the
+// kernel (see each kernel)}.  Points written by one warp compare exactly;
+// points of different warps only roughly.
+constexpr int kTraceWords = 16;
+__device__ __forceinline__ unsigned long long trace_clock() {
+  unsigned long long c;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(c)::"memory");
+  return c;
+}
+__device__ __forceinline__ void trace_entry(unsigned long long* tr, int cta, unsigned long long* c0) {
+  *c0 = trace_clock();
+  if (tr) {
+    unsigned int smid;
+    unsigned long long t;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    tr[(long)cta * kTraceWords] = smid;
+    tr[(long)cta * kTraceWords + 1] = t;
+  }
+}
+__device__ __forceinline__ void trace_mark(unsigned long long* tr, int cta, int point, unsigned long long c0) {
+  if (tr) {
+    const unsigned long long v = trace_clock() - c0;
+    asm volatile("st.global.u64 [%0], %1;" ::"l"(tr + (long)cta * kTraceWords + 1 + point), "l"(v) : "memory");
+  }
+}
 
 // Per-call descriptor of a drafting round (device copy lives in the workspace).
 struct RoundDesc {
@@ -38,15 +75,14 @@ struct RoundDesc {
   int seq_slot[kMaxBatch];
   int len[kMaxBatch];
   int item0[kMaxBatch + 1];        // attention work items of seq s: [item0[s], item0[s+1])
-  int pos[kMaxBatch * kBlock];
+  int pos[kMaxBatch * kBlock];     // absolute position of each block row
 };
 
 // Per-call descriptor of an ingest (rows in call order).
 struct IngestDesc {
   int n_rows;
-  int row_slot[kMaxIngestRows];
-  int row_dst[kMaxIngestRows];
-  int row_pos[kMaxIngestRows];
+  int row_pos[kMaxIngestRows];     // absolute position
+  int row_dest[kMaxIngestRows];    // page*64 + offset of the row's cached K/V
 };
 
 // Kernel-parameter blob of an init kernel: the descriptor plus page-table
@@ -76,7 +112,7 @@ struct EpiArgs {
   int kind;
   int layer;
   int n_tok;                  // token columns of this pass
-  int tok_base;               // first token of this pass (passes hold <= 256 tokens)
+  int tok_base;               // first token of this pass
   const float* wscale;        // per weight row scale (fp8), or null
   const float* ss_in;         // per token sum of squares -> rsqrt(ss/H+eps) scale; null = 1
   float* ss_out;              // per token sum of squares of the epilogue's output
@@ -92,10 +128,8 @@ struct EpiArgs {
   void* q_out;                // QKV: q buffer [Mt][Hq][d]
   void* kpool;                // K pool base (all layers)
   void* vpool;                // V^T pool base (all layers)
-  const int* block_table;
-  const RoundDesc* rd;
-  const IngestDesc* id;
-  const double* inv_freq;     // [d/2] RoPE inverse frequencies (f64)
+  const int* dest;            // QKV/KV: per token page*64+offset (descriptor copy)
+  const float2* rope_cs;      // QKV/KV: per token [d/2] (cos, sin), mscale folded in
   int* err;
   Geo g;
 };
@@ -115,8 +149,11 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Named barrier of the epilogue threads.  The non-aligned form counts each
+// arriving thread, so it stays correct when lanes reach it at different times
+// (after per-lane work such as the stream-K ticket).
 __device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync %0, %1;" ::"r"(kEpiBar), "r"(kEpiThreads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(kEpiBar), "r"(kEpiThreads) : "memory");
 }
 
 __device__ __forceinline__ void put_operand(void* op, long idx, long plane, float v, int f32) {
@@ -147,163 +184,260 @@ __device__ __forceinline__ long v_index(const Geo& g, int layer, int page, int h
   return layer * pool_layer_elems(g) + (((long)page * g.Hkv + head) * g.d + dim) * kPage + off;
 }
 
-// NeoX rotation angle for pair j at position p, reduced to [-pi, pi] in f64.
+// NeoX rotation angle for pair j at position p, reduced to [-pi, pi] in f64
+// (positions reach ~66k, where an f32 product would be off by ~1e-2 rad).
 __device__ __forceinline__ void rope_sincos(int pos, const double* inv_freq, int j, float* s, float* c) {
   double th = (double)pos * inv_freq[j];
   const double two_pi = 6.283185307179586476925286766559;
-  th -= two_pi * rint(th / two_pi);
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+  th = fma(-two_pi, rint(th * inv_two_pi), th);
   sincosf((float)th, s, c);
+}
+
+// Locate attention work item `item`: sequence s, kv head, its range of
+// cached context keys [k0, k1), and whether it is the sequence's last split
+// (which also attends the 16 block rows).
+__device__ __forceinline__ void attn_item(const RoundDesc* rd, int Hkv, int item, int* s_out, int* g_out,
+                                          int* k0, int* k1, bool* last) {
+  int s = 0;
+  while (s + 1 < rd->n_seq && rd->item0[s + 1] <= item) ++s;
+  const int local = item - rd->item0[s];
+  const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / Hkv;
+  const int g = local / nsplit, sp = local % nsplit;
+  const int len = rd->len[s];
+  *s_out = s;
+  *g_out = g;
+  *k0 = min(len, sp * rd->split_pages * kPage);
+  *k1 = min(len, (sp + 1) * rd->split_pages * kPage);
+  *last = sp == nsplit - 1;
+}
+
+// One head row for the attention, read from the QKV accumulator (token-major
+// [tok][(Hq+2Hkv)*d], pre-norm and unscaled): x = acc[tok][col0 .. col0+d) *
+// rs; for q and k (norm_rope) a head RMSNorm with `gain` and the NeoX
+// rotation by (cos, sin) of the token's position (mscale folded in).  Called
+// by a whole warp; lane l returns dims l*PER .. l*PER+PER-1 (lanes 0..15 the
+// first half, so the partner of dim j is dim j + d/2 in lane l + 16).
+template <int PER>
+__device__ __forceinline__ void qkv_head_row(const float* __restrict__ acc, int ld, int tok, int col0, float rs,
+                                             const float* __restrict__ gain, const float2* __restrict__ cs_row,
+                                             bool norm_rope, float eps, float* x) {
+  constexpr int d = 32 * PER, half = d / 2;
+  const int lane = threadIdx.x & 31;
+  const int dim0 = lane * PER;
+  const float* src = acc + (long)tok * ld + col0 + dim0;
+  if (PER == 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+    x[0] = v.x; x[1] = v.y;
+  }
+  if (!norm_rope) {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) x[q] *= rs;
+    return;
+  }
+  float gn[PER];
+  float2 cs[PER];
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    gn[q] = gain[dim0 + q];
+    cs[q] = cs_row[(dim0 + q) % half];
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    x[q] *= rs;
+    ss += x[q] * x[q];
+  }
+  ss = warp_sum(ss);
+  const float r = rsqrtf(ss / (float)d + eps);
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    const float y = x[q] * r * gn[q];
+    const float partner = __shfl_xor_sync(0xffffffffu, y, 16);
+    x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
+  }
+}
+
+// ------------------------------------------------------------------ stream-K reduction
+// Tile accumulator layout: acc[tile][128 features][nt tokens] f32 (nt = the
+// pass's tokens rounded up to 16), so a thread owning feature f adds and
+// reads its tokens as contiguous float4s.
+
+// Add one contributor's values v[0..15] (tokens j0..j0+15 of one feature).
+__device__ __forceinline__ void acc_add16(float* acc_f, int j0, int n_tok, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (j0 + 4 * q < n_tok) {
+      float* p = acc_f + j0 + 4 * q;
+      asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v[4 * q]), "f"(v[4 * q + 1]),
+                   "f"(v[4 * q + 2]), "f"(v[4 * q + 3])
+                   : "memory");
+    }
+  }
 }
 
 // ------------------------------------------------------------------ epilogue
 // Head-wise epilogue (QKV of a round, K/V of an ingest) on a reduced chunk
-// red[t][0..127] for tokens tok0 .. tok0+tc-1.  One warp per (token, head).
-static __device__ void epi_heads(const EpiArgs& e, int tile, const float* red, int tok0, int tc, int et) {
+// red[t][0..127] for tokens tok0 .. tok0+tc-1.  One warp per (token, head);
+// lane l holds PER = d/32 consecutive dims, lanes 0..15 the first half (so a
+// dim's RoPE partner j + d/2 sits in lane l + 16).  Every global load of a
+// task is issued before any of its stores.
+template <int PER>
+static __device__ void epi_heads_t(const EpiArgs& e, int tile, const float* red, const float* rsc, int tok0, int tc,
+                                   int et) {
   const Geo& g = e.g;
-  const int d = g.d;
-  const int per = d / 32;                 // values per lane
-  const int heads_in_tile = kTileN / d;
+  constexpr int d = 32 * PER, half = d / 2, heads_in_tile = kTileN / d;
   const int warp = et >> 5, lane = et & 31;
+  const int dim0 = lane * PER;
   const int tasks = tc * heads_in_tile;
   for (int task = warp; task < tasks; task += kEpiThreads / 32) {
     const int t = task / heads_in_tile, sh = task % heads_in_tile;
-    const int tok = e.tok_base + tok0 + t;      // global token index
+    const int tok = e.tok_base + tok0 + t;     // global token index
     const int hh = (tile * kTileN) / d + sh;   // head index within the tile's GEMM rows
     int layer, kind, head;                     // kind 0 q, 1 k, 2 v
-    int pos, slot, row;
     if (e.kind == EPI_QKV) {
       layer = e.layer;
-      if (hh < g.Hq) { kind = 0; head = hh; }
-      else if (hh < g.Hq + g.Hkv) { kind = 1; head = hh - g.Hq; }
-      else { kind = 2; head = hh - g.Hq - g.Hkv; }
-      const int s = tok / kBlock;
-      pos = e.rd->pos[tok];
-      slot = e.rd->seq_slot[s];
-      row = e.rd->len[s] + (tok % kBlock);
+      kind = hh < g.Hq ? 0 : (hh < g.Hq + g.Hkv ? 1 : 2);
+      head = kind == 0 ? hh : (kind == 1 ? hh - g.Hq : hh - g.Hq - g.Hkv);
     } else {
       layer = hh / (2 * g.Hkv);
       const int j = hh % (2 * g.Hkv);
       kind = j < g.Hkv ? 1 : 2;
       head = j < g.Hkv ? j : j - g.Hkv;
-      pos = e.id->row_pos[tok];
-      slot = e.id->row_slot[tok];
-      row = e.id->row_dst[tok];
     }
-    float rs = 1.f;
-    if (e.ss_in) rs = rsqrtf(e.ss_in[tok] / (float)g.H + g.eps);
-    float x[4];
+    // loads first: gains, (cos, sin), destination row
+    float gn[PER];
+    float2 cs[PER];
+    const float* __restrict__ gsrc = (kind == 0) ? e.qn : (e.kind == EPI_QKV ? e.kn : e.kn + (long)layer * d);
+    const float2* __restrict__ csrc = e.rope_cs + (long)tok * half;
+    if (kind != 2) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if (q < per) x[q] = red[t * (kTileN + 1) + sh * d + lane * per + q] * rs;
+      for (int q = 0; q < PER; ++q) {
+        gn[q] = gsrc[dim0 + q];
+        cs[q] = csrc[(dim0 + q) % half];
+      }
+    }
+    const int dst = kind != 0 ? e.dest[tok] : 0;
+    const float rs = rsc[t];
+    float x[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) x[q] = red[t * (kTileN + 1) + sh * d + dim0 + q] * rs;
     if (kind != 2) {
       float ss = 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q < per) ss += x[q] * x[q];
+      for (int q = 0; q < PER; ++q) ss += x[q] * x[q];
       ss = warp_sum(ss);
       const float r = rsqrtf(ss / (float)d + g.eps);
-      const float* gn = (kind == 0) ? e.qn : (e.kind == EPI_QKV ? e.kn : e.kn + (long)layer * d);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q < per) x[q] = x[q] * r * gn[lane * per + q];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < per) {
-          const float partner = __shfl_xor_sync(0xffffffffu, x[q], 16);
-          const int dim = lane * per + q;
-          const int j = dim % (d / 2);
-          float sn, cs;
-          rope_sincos(pos, e.inv_freq, j, &sn, &cs);
-          x[q] = (lane < 16 ? (x[q] * cs - partner * sn) : (x[q] * cs + partner * sn)) * g.mscale;
-        } else {
-          (void)__shfl_xor_sync(0xffffffffu, 0.f, 16);
-        }
+      for (int q = 0; q < PER; ++q) {
+        const float y = x[q] * r * gn[q];
+        const float partner = __shfl_xor_sync(0xffffffffu, y, 16);   // dims j <-> j + d/2
+        x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
       }
     }
     if (kind == 0) {
-      const long base = ((long)tok * g.Hq + head) * d;
+      const long base = ((long)tok * g.Hq + head) * d + dim0;
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (q < per) put_kv(e.q_out, base + lane * per + q, x[q], g.kvtype);
+      for (int q = 0; q < PER; ++q) put_kv(e.q_out, base + q, x[q], g.kvtype);
     } else {
-      const int page = e.block_table[(long)slot * g.pages_per_seq + row / kPage];
-      const int off = row % kPage;
-      if (page < 0 || page >= g.max_pages) {
-        if (lane == 0) atomicExch(e.err, DERR_BAD_PAGE);
-        continue;
-      }
+      const int page = dst >> 6, off = dst & (kPage - 1);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (q < per) {
-          const int dim = lane * per + q;
-          if (kind == 1) put_kv(e.kpool, k_index(g, layer, page, head, off, dim), x[q], g.kvtype);
-          else put_kv(e.vpool, v_index(g, layer, page, head, off, dim), x[q], g.kvtype);
-        }
+      for (int q = 0; q < PER; ++q) {
+        if (kind == 1) put_kv(e.kpool, k_index(g, layer, page, head, off, dim0 + q), x[q], g.kvtype);
+        else put_kv(e.vpool, v_index(g, layer, page, head, off, dim0 + q), x[q], g.kvtype);
       }
     }
   }
 }
 
-// Reduce the partials of `tile` (contributors c_lo..c_hi, slot c+tile) and
-// run its epilogue.  Called by all kEpiThreads threads (et = 0..127) of the
-// CTA that arrived last.  red: shared scratch [kEpiTokChunk][129] floats.
-static __device__ void tile_epilogue(const EpiArgs& e, int tile, int c_lo, int c_hi, const float* part,
-                              float* red, int et) {
+static __device__ __forceinline__ void epi_heads(const EpiArgs& e, int tile, const float* red, const float* rsc,
+                                                 int tok0, int tc, int et) {
+  if (e.g.d == 128) epi_heads_t<4>(e, tile, red, rsc, tok0, tc, et);
+  else epi_heads_t<2>(e, tile, red, rsc, tok0, tc, et);
+}
+
+// Run the fused epilogue of `tile` from its accumulator (and clear it).
+// Called by all kEpiThreads threads (et = 0..127) of the CTA that arrived
+// last.  acc: the tile's accumulator [128][nt]; red: kRedFloats shared floats.
+static __device__ void tile_epilogue(const EpiArgs& e, int tile, float* acc, int nt, float* red, int et,
+                                     unsigned long long* tr = nullptr, int cta = 0, unsigned long long c0 = 0) {
   const Geo& g = e.g;
-  const long slot_elems = (long)g.Mt * kTileN;
+  float* rsc = red + kEpiTokChunk * (kTileN + 1);   // per-token input-norm scale
   const int f = et;                                 // feature within the tile
-  const int row = tile * kTileN + f;                // weight row
-  const float wsc = e.wscale ? e.wscale[row] : 1.f;
+  const float wsc = e.wscale ? e.wscale[tile * kTileN + f] : 1.f;
+  float* acc_f = acc + (long)f * nt;
   for (int tok0 = 0; tok0 < e.n_tok; tok0 += kEpiTokChunk) {
     const int tc = min(kEpiTokChunk, e.n_tok - tok0);
-    for (int t = 0; t < tc; ++t) {
-      float v = 0.f;
-      for (int c = c_lo; c <= c_hi; ++c)
-        v += __ldcg(part + (long)(c + tile) * slot_elems + (long)(tok0 + t) * kTileN + f);
-      red[t * (kTileN + 1) + f] = v * wsc;
+    // one batch of independent vector loads, then clear the accumulator
+    float4 v[kEpiTokChunk / 4];
+#pragma unroll
+    for (int q = 0; q < kEpiTokChunk / 4; ++q)
+      if (4 * q < tc) v[q] = __ldcg(reinterpret_cast<const float4*>(acc_f + tok0) + q);
+    if (et < tc) rsc[et] = e.ss_in ? rsqrtf(e.ss_in[e.tok_base + tok0 + et] / (float)g.H + g.eps) : 1.f;
+#pragma unroll
+    for (int q = 0; q < kEpiTokChunk / 4; ++q) {
+      if (4 * q < tc) {
+        __stcg(reinterpret_cast<float4*>(acc_f + tok0) + q, make_float4(0.f, 0.f, 0.f, 0.f));
+        red[(4 * q + 0) * (kTileN + 1) + f] = v[q].x * wsc;
+        red[(4 * q + 1) * (kTileN + 1) + f] = v[q].y * wsc;
+        red[(4 * q + 2) * (kTileN + 1) + f] = v[q].z * wsc;
+        red[(4 * q + 3) * (kTileN + 1) + f] = v[q].w * wsc;
+      }
     }
+    if (et == 0) trace_mark(tr, cta, 11, c0);   // 11: accumulator read
     epi_sync();
+    if (et == 0) trace_mark(tr, cta, 12, c0);   // 12: row scales ready
     if (e.kind == EPI_QKV || e.kind == EPI_KV) {
-      epi_heads(e, tile, red, tok0, tc, et);
+      epi_heads(e, tile, red, rsc, tok0, tc, et);
     } else if (e.kind == EPI_SWIGLU) {
       // tile rows [0,64) = gate rows, [64,128) = up rows of act columns [64*tile, 64*tile+64)
       const int j = et & 63;
       for (int t = et >> 6; t < tc; t += 2) {
         const int tok = e.tok_base + tok0 + t;
-        const float rs = e.ss_in ? rsqrtf(e.ss_in[tok] / (float)g.H + g.eps) : 1.f;
-        const float gv = red[t * (kTileN + 1) + j] * rs;
-        const float uv = red[t * (kTileN + 1) + 64 + j] * rs;
-        const float a = gv / (1.f + expf(-gv)) * uv;
+        const float gv = red[t * (kTileN + 1) + j] * rsc[t];
+        const float uv = red[t * (kTileN + 1) + 64 + j] * rsc[t];
+        const float a = gv / (1.f + __expf(-gv)) * uv;
         put_operand(e.op, (long)tok * e.op_ld + tile * 64 + j, e.op_plane, a, e.op_f32);
       }
     } else {  // EPI_FC, EPI_RESID
       const int col = tile * kTileN + f;
+      const float gn = e.gain ? e.gain[col] : 1.f;
+      if (e.kind == EPI_RESID) {
+        // all residual loads in flight at once, then the adds (red is a
+        // generic pointer the compiler cannot separate from e.h)
+        float hv[kEpiTokChunk];
+        const float* __restrict__ hcol = e.h + (long)(e.tok_base + tok0) * e.h_ld + col;
+#pragma unroll
+        for (int t = 0; t < kEpiTokChunk; ++t)
+          if (t < tc) hv[t] = __ldcg(hcol + (long)t * e.h_ld);
+#pragma unroll
+        for (int t = 0; t < kEpiTokChunk; ++t)
+          if (t < tc) red[t * (kTileN + 1) + f] += hv[t];
+      }
       for (int t = 0; t < tc; ++t) {
         const int tok = e.tok_base + tok0 + t;
-        float v = red[t * (kTileN + 1) + f];
-        if (e.kind == EPI_RESID) {
-          float* hp = e.h + (long)tok * e.h_ld + col;
-          v += *hp;
-          *hp = v;
-        }
-        red[t * (kTileN + 1) + f] = v;
-        if (e.op) put_operand(e.op, (long)tok * e.op_ld + col, e.op_plane, v * (e.gain ? e.gain[col] : 1.f), e.op_f32);
+        const float x = red[t * (kTileN + 1) + f];
+        if (e.kind == EPI_RESID) e.h[(long)tok * e.h_ld + col] = x;
+        if (e.op) put_operand(e.op, (long)tok * e.op_ld + col, e.op_plane, x * gn, e.op_f32);
       }
       epi_sync();
       if (e.ss_out) {
         const int warp = et >> 5, lane = et & 31;
         for (int t = warp; t < tc; t += kEpiThreads / 32) {
           float s = 0.f;
-#pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float v = red[t * (kTileN + 1) + lane + 32 * q];
-            s += v * v;
+            const float x = red[t * (kTileN + 1) + lane + 32 * q];
+            s += x * x;
           }
           s = warp_sum(s);
           if (lane == 0) atomicAdd(e.ss_out + e.tok_base + tok0 + t, s);
         }
       }
     }
+    if (et == 0) trace_mark(tr, cta, 13, c0);   // 13: fused step done
     epi_sync();
   }
 }

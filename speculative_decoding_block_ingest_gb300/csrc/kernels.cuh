@@ -1,28 +1,62 @@
 // kernels.cuh -- host-side launch interface of the drafter kernels.
 #pragma once
+#include <utility>
+
 #include "dflash_internal.cuh"
 
 namespace dfl {
 
-// One weight-streaming projection: Y[tok][N] = X[tok][K] * W[N][K]^T with the
-// fused epilogue e (swap-AB: W rows are tile rows, tokens are columns).
+// Where a projection's operand X[tok][K] comes from.
+enum XMode {
+  X_PLANES = 0,   // a prepared buffer: bf16 hi/lo planes (TMA), or f32 for f32 drafters
+  X_FROM_H = 1,   // the residual stream h [tok][K] f32 times a norm gain (pre-norm; the
+                  //   row scale is applied by whoever consumes the result)
+  X_SWIGLU = 2    // silu(g r) * (u r) from the gate/up accumulator [tok][2I] and row scale r
+};
+// Where a projection's result goes.
+enum OMode {
+  O_TILE = 0,     // stream-K ticket; the last arriver runs the tile epilogue EpiArgs::kind
+  O_RED = 1       // every contributor red.adds into a token-major destination [tok][ld]
+};
+
+// One weight-streaming projection: Y[tok][N] = X[tok][K] * W[N][K]^T
+// (swap-AB: W rows are tile rows, tokens are columns).
 struct GemmArgs {
   const void* W;      // [N][K] in Geo::wtype
   int N, K;
-  const void* X;      // operand [tok][K]: f32, or bf16 hi plane (+ lo plane at x_plane)
+  int xmode;
+  const void* X;      // X_PLANES: [tok][K] f32, or bf16 hi plane (+ lo plane at x_plane)
   int x_ld;
   long x_plane;
   int x_f32;
+  const float* xsrc;  // X_FROM_H: h; X_SWIGLU: gate/up accumulator (token-major)
+  int xsrc_ld;
+  const float* xgain; // X_FROM_H: gain [K]
+  const float* xrs;   // X_SWIGLU: per token row scale
+  int omode;
+  float* dst;         // O_RED: destination [tok][dst_ld]
+  int dst_ld;
+  // side duties spread over the CTAs (each may be null)
+  const float* rs_src;  // rows whose RMS scale rsqrt(mean(x^2)+eps) goes to rs_out[tok]
+  int rs_ld, rs_len;
+  float* rs_out;
+  float* zero_ptr;      // float4-aligned region cleared for a later call
+  long zero_n;          // floats, a multiple of 4
   Part p;
   int n_tiles;
-  float* part;        // partial slots [(grid + n_tiles)][Mt][128]
+  float* acc;         // O_TILE accumulators [n_tiles][128][nt], zero between calls
   int* counters;      // [n_tiles], zero between calls
+  unsigned long long* trace;   // optional per-CTA timestamps [grid][kTraceWords], or null
   EpiArgs e;
 };
 
 // Attention over the paged cache: per (seq, kv head, split) work item.
 struct AttnArgs {
-  const void* q;        // [Mt][Hq][d]  (kv dtype)
+  const float* qkv;     // QKV accumulator [Mt][(Hq+2Hkv)*d] f32 (pre-norm, unscaled)
+  const float* r_in;    // per token input-norm scale
+  const float* qn;      // q head-norm gain of this layer [d]
+  const float* kn;      // k head-norm gain of this layer [d]
+  const float2* rope_cs;  // per token [d/2] (cos, sin) x mscale
   const void* kpool;    // K pool base
   const void* vpool;    // V^T pool base
   int layer;
@@ -34,7 +68,8 @@ struct AttnArgs {
   int op_ld;
   long op_plane;
   int op_f32;
-  float scale;          // 1/sqrt(d)
+  float scale_log2;     // log2(e)/sqrt(d): scores and the saved max are in log2 units
+  unsigned long long* trace;   // optional per-CTA timestamps [items][kTraceWords], or null
   int* err;
   Geo g;
 };
@@ -42,10 +77,8 @@ struct AttnArgs {
 struct InitArgs {
   const float* src;     // noise [n_tok][H] (round) or taps [n_rows][n*H] (ingest)
   int n_rows, width;
-  float* h;             // round: residual stream [Mt][H]
-  float* ss0;           // round: ss of layer-0 input norm; ingest: null
-  const float* gain;    // round: layer-0 input_ln
-  void* op;             // operand output
+  float* h;             // round: residual stream [Mt][H] (then no operand is written)
+  void* op;             // ingest: operand output
   int op_ld;
   long op_plane;
   int op_f32;
@@ -54,15 +87,38 @@ struct InitArgs {
   void* desc_dst;       // device descriptor
   int desc_bytes;
   int* block_table;
+  const double* inv_freq;   // RoPE inverse frequencies [d/2] (f64)
+  float2* rope_cs;          // out: per row [d/2] (cos, sin) x mscale
+  int is_round;             // positions come from blob.round.pos (else blob.ingest.row_pos)
   Geo g;
 };
+
+// Launch with programmatic stream serialization: the kernel may become
+// resident while its predecessor drains; every kernel of the library calls
+// griddepcontrol.wait before touching data a predecessor writes or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 void launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 void launch_gemm_tc(const GemmArgs& a, const void* tmap_w, const void* tmap_x, cudaStream_t s);
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s);
+void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmk, const void* tmv, cudaStream_t s);
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s);
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s);
-void launch_final_norm(const float* h, const float* ss, const float* gain, float* out, int n_tok,
+void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, float* zero_ptr, long zero_n,
                        const Geo& g, cudaStream_t s);
 void launch_kv_read(const Geo& g, const void* kpool, const void* vpool, const int* block_table,
                     int slot, int layer, int row0, int nrows, float* k_out, float* v_out,

@@ -8,6 +8,7 @@
 //  * the per-call init kernels (descriptor upload, page-table update,
 //    residual stream / operand set-up), the final norm and KV read-back.
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace dfl {
 
@@ -21,28 +22,59 @@ __device__ __forceinline__ float load_w(const void* W, long idx, int wtype) {
 }
 
 __device__ __forceinline__ float load_x(const GemmArgs& a, int tok, int k) {
+  if (a.xmode == X_FROM_H) return a.xsrc[(long)tok * a.xsrc_ld + k] * a.xgain[k];
+  if (a.xmode == X_SWIGLU) {
+    const long base = (long)tok * a.xsrc_ld + (k / 64) * 128 + (k % 64);
+    const float rs = a.xrs[tok];
+    const float gs = a.xsrc[base] * rs, us = a.xsrc[base + 64] * rs;
+    return gs / (1.f + __expf(-gs)) * us;
+  }
   const long idx = (long)tok * a.x_ld + k;
   if (a.x_f32) return reinterpret_cast<const float*>(a.X)[idx];
   const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.X);
   return __bfloat162float(x[idx]) + __bfloat162float(x[idx + a.x_plane]);
 }
 
+// Side duties of a projection launch, spread over its CTAs: per-token RMS
+// scales of rs_src rows, and clearing a region for a later call.
+__device__ void gemm_duties(const GemmArgs& a, int cta, int grid, int tid, int nthreads) {
+  if (a.rs_out && tid < 32) {
+    for (int tok = cta; tok < a.e.n_tok; tok += grid) {
+      const float* src = a.rs_src + (long)(a.e.tok_base + tok) * a.rs_ld;
+      float ss = 0.f;
+      for (int k = tid; k < a.rs_len; k += 32) ss += src[k] * src[k];
+      ss = warp_sum(ss);
+      if (tid == 0) a.rs_out[a.e.tok_base + tok] = rsqrtf(ss / (float)a.rs_len + a.e.g.eps);
+    }
+  }
+  if (a.zero_ptr) {
+    const long n4 = a.zero_n / 4;
+    const long lo = n4 * cta / grid, hi = n4 * (cta + 1) / grid;
+    for (long k = lo + tid; k < hi; k += nthreads)
+      reinterpret_cast<float4*>(a.zero_ptr)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
 constexpr int kSimtTok = 16;
 
 __global__ void __launch_bounds__(128) gemm_simt_kernel(GemmArgs a) {
   __shared__ float smem[kTileN * (kTileK + 1) + kSimtTok * kTileK];
-  __shared__ int s_last, s_clo, s_chi;
+  __shared__ int s_last;
   float* Ws = smem;                          // [128][65]
   float* Xs = smem + kTileN * (kTileK + 1);  // [16][64]
+  pdl_wait();
+  pdl_launch_dependents();
   const int tid = threadIdx.x;
   const int c = blockIdx.x;
   const Part p = a.p;
   const int u1 = p.start(c + 1);
-  const long slot_elems = (long)a.e.g.Mt * kTileN;
+  const int nt = (a.e.n_tok + 15) / 16 * 16;
+  gemm_duties(a, c, p.grid, tid, 128);
   for (int u = p.start(c); u < u1;) {
     const int T = u / p.kb;
     const int seg_end = min(u1, (T + 1) * p.kb);
     const int kb0 = u - T * p.kb, kb1 = seg_end - T * p.kb;
+    float* acc_tile = a.acc + (long)T * kTileN * nt;
     for (int tok0 = 0; tok0 < a.e.n_tok; tok0 += kSimtTok) {
       float acc[kSimtTok];
 #pragma unroll
@@ -65,10 +97,19 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(GemmArgs a) {
           for (int t = 0; t < kSimtTok; ++t) acc[t] = fmaf(w, Xs[t * kTileK + k], acc[t]);
         }
       }
-      float* dst = a.part + (long)(c + T) * slot_elems;
+      if (a.omode == O_RED) {
+        float* dcol = a.dst + (long)(a.e.tok_base + tok0) * a.dst_ld + T * kTileN + tid;
+        const float wsc = a.e.wscale ? a.e.wscale[T * kTileN + tid] : 1.f;
 #pragma unroll
-      for (int t = 0; t < kSimtTok; ++t)
-        if (tok0 + t < a.e.n_tok) dst[(long)(tok0 + t) * kTileN + tid] = acc[t];
+        for (int t = 0; t < kSimtTok; ++t)
+          if (tok0 + t < a.e.n_tok) atomicAdd(dcol + (long)t * a.dst_ld, acc[t] * wsc);
+      } else {
+        acc_add16(acc_tile + (long)tid * nt, tok0, a.e.n_tok, acc);
+      }
+    }
+    if (a.omode == O_RED) {
+      u = seg_end;
+      continue;
     }
     __threadfence();
     __syncthreads();
@@ -76,13 +117,11 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(GemmArgs a) {
       const int c_lo = p.owner(T * p.kb), c_hi = p.owner((T + 1) * p.kb - 1);
       const int old = atomicAdd(a.counters + T, 1);
       s_last = (old == c_hi - c_lo);
-      s_clo = c_lo;
-      s_chi = c_hi;
     }
     __syncthreads();
     if (s_last) {
       __threadfence();
-      tile_epilogue(a.e, T, s_clo, s_chi, a.part, smem, tid);
+      tile_epilogue(a.e, T, acc_tile, nt, smem, tid);
       if (tid == 0) a.counters[T] = 0;
     }
     u = seg_end;
@@ -90,7 +129,7 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(GemmArgs a) {
 }
 
 void launch_gemm_simt(const GemmArgs& a, cudaStream_t s) {
-  gemm_simt_kernel<<<a.p.grid, 128, 0, s>>>(a);
+  launch_pdl(gemm_simt_kernel, dim3(a.p.grid), dim3(128), 0, s, a);
 }
 
 // ------------------------------------------------------------------ attention (CUDA cores)
@@ -99,85 +138,105 @@ __device__ __forceinline__ float load_kv(const void* base, long idx, int kvtype)
   return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
 }
 
-// Locate work item `item`: sequence s, kv head, split index and key range.
-__device__ __forceinline__ void attn_item(const RoundDesc* rd, int Hkv, int item, int* s_out, int* g_out,
-                                          int* k0, int* k1) {
-  int s = 0;
-  while (s + 1 < rd->n_seq && rd->item0[s + 1] <= item) ++s;
-  const int local = item - rd->item0[s];
-  const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / Hkv;
-  const int g = local / nsplit, sp = local % nsplit;
-  const int n_keys = rd->len[s] + kBlock;
-  *s_out = s;
-  *g_out = g;
-  *k0 = sp * rd->split_pages * kPage;
-  *k1 = min(n_keys, (sp + 1) * rd->split_pages * kPage);
+// Write lane's PER dims of a head row into an f32 shared row.
+template <int PER>
+__device__ __forceinline__ void put_row_f32(float* row, const float* x) {
+  const int dim0 = (threadIdx.x & 31) * PER;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) row[dim0 + q] = x[q];
 }
 
-__global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
-  extern __shared__ float sm[];
+template <int PER>
+__device__ void attn_simt_body(const AttnArgs& a, float* sm) {
   const Geo& g = a.g;
-  const int d = g.d, R = g.G * kBlock, dp = d + 1;
+  constexpr int d = 32 * PER;
+  const int R = g.G * kBlock, dp = d + 1;
   float* Qs = sm;                 // [R][d+1]
   float* Os = Qs + R * dp;        // [R][d+1]
   float* Ks = Os + R * dp;        // [64][d+1]
   float* Vs = Ks + kPage * dp;    // [d][65]
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int item = blockIdx.x;
   int s, kvh, k0, k1;
-  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1);
+  bool last;
+  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &last);
   const int slot = a.rd->seq_slot[s];
-  for (int idx = tid; idx < R * d; idx += 128) {
-    const int r = idx / d, dim = idx % d;
-    const int hl = r / kBlock, i = r % kBlock;
-    const long qi = ((long)(s * kBlock + i) * g.Hq + kvh * g.G + hl) * d + dim;
-    Qs[r * dp + dim] = load_kv(a.q, qi, g.kvtype);
-    Os[r * dp + dim] = 0.f;
+  const int n_pages = (k1 - k0 + kPage - 1) / kPage;
+  const int n_all = n_pages + (last ? 1 : 0);
+  // query rows r = token * G + local head: input-norm scale, head norm, RoPE
+  for (int r = warp; r < R; r += 4) {
+    const int i = r / g.G, hl = r % g.G, tok = s * kBlock + i;
+    float x[PER];
+    qkv_head_row<PER>(a.qkv, g.qkv_n, tok, (kvh * g.G + hl) * d, a.r_in[tok], a.qn, a.rope_cs + (long)tok * (d / 2),
+                      true, g.eps, x);
+    put_row_f32<PER>(Qs + r * dp, x);
   }
+  for (int idx = tid; idx < R * d; idx += 128) Os[(idx / d) * dp + idx % d] = 0.f;
   float m = -INFINITY, l = 0.f;
   const bool active = tid < R;
-  for (int kp = k0; kp < k1; kp += kPage) {
-    const int pidx = kp / kPage;
-    const int page = a.block_table[(long)slot * g.pages_per_seq + pidx];
-    const int kc = min(kPage, k1 - kp);
+  for (int j = 0; j < n_all; ++j) {
     __syncthreads();
-    if (page < 0 || page >= g.max_pages) {
-      if (tid == 0) atomicExch(a.err, DERR_BAD_PAGE);
-      break;
-    }
-    for (int idx = tid; idx < kPage * d; idx += 128) {
-      const int j = idx / d, dim = idx % d;
-      Ks[j * dp + dim] = j < kc ? load_kv(a.kpool, k_index(g, a.layer, page, kvh, j, dim), g.kvtype) : 0.f;
-      const int dv = idx / kPage, jv = idx % kPage;
-      Vs[dv * (kPage + 1) + jv] = jv < kc ? load_kv(a.vpool, v_index(g, a.layer, page, kvh, jv, dv), g.kvtype) : 0.f;
+    int kc;
+    if (j < n_pages) {
+      const int kp = k0 + j * kPage;
+      const int page = a.block_table[(long)slot * g.pages_per_seq + kp / kPage];
+      kc = min(kPage, k1 - kp);
+      if (page < 0 || page >= g.max_pages) {
+        if (tid == 0) atomicExch(a.err, DERR_BAD_PAGE);
+        break;
+      }
+      for (int idx = tid; idx < kPage * d; idx += 128) {
+        const int jj = idx / d, dim = idx % d;
+        Ks[jj * dp + dim] = jj < kc ? load_kv(a.kpool, k_index(g, a.layer, page, kvh, jj, dim), g.kvtype) : 0.f;
+        const int dv = idx / kPage, jv = idx % kPage;
+        Vs[dv * (kPage + 1) + jv] = jv < kc ? load_kv(a.vpool, v_index(g, a.layer, page, kvh, jv, dv), g.kvtype) : 0.f;
+      }
+    } else {
+      // the block rows' own K (normed, roped) and V, straight from the QKV
+      // accumulator; the unused key slots must hold zeros (0 x stale NaN = NaN)
+      kc = kBlock;
+      for (int idx = tid; idx < kPage * dp; idx += 128) Ks[idx] = 0.f;
+      for (int idx = tid; idx < d * (kPage + 1); idx += 128) Vs[idx] = 0.f;
+      __syncthreads();
+      for (int i = warp; i < kBlock; i += 4) {
+        const int tok = s * kBlock + i;
+        float x[PER];
+        qkv_head_row<PER>(a.qkv, g.qkv_n, tok, (g.Hq + kvh) * d, a.r_in[tok], a.kn, a.rope_cs + (long)tok * (d / 2),
+                          true, g.eps, x);
+        put_row_f32<PER>(Ks + i * dp, x);
+        qkv_head_row<PER>(a.qkv, g.qkv_n, tok, (g.Hq + g.Hkv + kvh) * d, a.r_in[tok], nullptr, nullptr, false, g.eps,
+                          x);
+#pragma unroll
+        for (int q = 0; q < PER; ++q) Vs[((tid & 31) * PER + q) * (kPage + 1) + i] = x[q];
+      }
     }
     __syncthreads();
     if (active) {
       float sc[kPage];
       float mx = m;
 #pragma unroll
-      for (int j = 0; j < kPage; ++j) {
+      for (int jj = 0; jj < kPage; ++jj) {
         float acc = 0.f;
-        if (j < kc) {
-          for (int dim = 0; dim < d; ++dim) acc = fmaf(Qs[tid * dp + dim], Ks[j * dp + dim], acc);
-          acc *= a.scale;
+        if (jj < kc) {
+          for (int dim = 0; dim < d; ++dim) acc = fmaf(Qs[tid * dp + dim], Ks[jj * dp + dim], acc);
+          acc *= a.scale_log2;
           mx = fmaxf(mx, acc);
         }
-        sc[j] = acc;
+        sc[jj] = acc;
       }
-      const float alpha = __expf(m - mx);
+      const float alpha = exp2f(m - mx);
       float lsum = 0.f;
 #pragma unroll
-      for (int j = 0; j < kPage; ++j) {
-        sc[j] = j < kc ? __expf(sc[j] - mx) : 0.f;
-        lsum += sc[j];
+      for (int jj = 0; jj < kPage; ++jj) {
+        sc[jj] = jj < kc ? exp2f(sc[jj] - mx) : 0.f;
+        lsum += sc[jj];
       }
       l = l * alpha + lsum;
       m = mx;
       for (int dim = 0; dim < d; ++dim) {
         float acc = Os[tid * dp + dim] * alpha;
 #pragma unroll
-        for (int j = 0; j < kPage; ++j) acc = fmaf(sc[j], Vs[dim * (kPage + 1) + j], acc);
+        for (int jj = 0; jj < kPage; ++jj) acc = fmaf(sc[jj], Vs[dim * (kPage + 1) + jj], acc);
         Os[tid * dp + dim] = acc;
       }
     }
@@ -194,21 +253,31 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   }
 }
 
+__global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
+  extern __shared__ float sm[];
+  pdl_wait();
+  pdl_launch_dependents();
+  if (a.g.d == 128) attn_simt_body<4>(a, sm);
+  else attn_simt_body<2>(a, sm);
+}
+
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s) {
   const int R = a.g.G * kBlock, dp = a.g.d + 1;
   const size_t smem = sizeof(float) * (2 * R * dp + kPage * dp + a.g.d * (kPage + 1));
   cudaFuncSetAttribute(attn_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_simt_kernel<<<n_items, 128, smem, s>>>(a);
+  launch_pdl(attn_simt_kernel, dim3(n_items), dim3(128), smem, s, a);
 }
 
 // Merge the split-KV partials of one (token, q head) row into the O-proj operand.
 __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
   const Geo& g = a.g;
   const int row = blockIdx.x;               // tok * Hq + h
   const int tok = row / g.Hq, h = row % g.Hq;
   const int s = tok / kBlock, i = tok % kBlock;
   const int kvh = h / g.G, hl = h % g.G;
-  const int R = g.G * kBlock, r = hl * kBlock + i;
+  const int R = g.G * kBlock, r = i * g.G + hl;
   const RoundDesc* rd = a.rd;
   const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / g.Hkv;
   const int it0 = rd->item0[s] + kvh * nsplit;
@@ -219,7 +288,7 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   float num = 0.f, den = 0.f;
   for (int sp = 0; sp < nsplit; ++sp) {
     const long pr = (long)(it0 + sp) * R + r;
-    const float w = __expf(a.part_ml[pr * 2] - M);
+    const float w = exp2f(a.part_ml[pr * 2] - M);
     den += w * a.part_ml[pr * 2 + 1];
     num += w * a.part_o[pr * g.d + dim];
   }
@@ -227,13 +296,15 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
 }
 
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s) {
-  attn_combine_kernel<<<n_tok * a.g.Hq, 128, 0, s>>>(a);
+  launch_pdl(attn_combine_kernel, dim3(n_tok * a.g.Hq), dim3(128), 0, s, a);
 }
 
 // ------------------------------------------------------------------ per-call init
 // CTA r < n_rows: stage row r (residual stream + operand); CTA n_rows: upload
 // the descriptor, apply page-table entries and clear accumulators.
 __global__ void __launch_bounds__(128) init_kernel(InitArgs a, InitBlob b) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int r = blockIdx.x, tid = threadIdx.x;
   if (r == a.n_rows) {
     const int* src = reinterpret_cast<const int*>(&b);
@@ -243,41 +314,57 @@ __global__ void __launch_bounds__(128) init_kernel(InitArgs a, InitBlob b) {
     for (int i = tid; i < a.zero_n; i += blockDim.x) a.zero_ptr[i] = 0.f;
     return;
   }
-  __shared__ float red[4];
-  float ss = 0.f;
+  // RoPE (cos, sin) of this row's position, mscale folded in
+  const int pos = a.is_round ? b.round.pos[r] : b.ingest.row_pos[r];
+  const int half = a.g.d / 2;
+  for (int j = tid; j < half; j += blockDim.x) {
+    float sn, cs;
+    rope_sincos(pos, a.inv_freq, j, &sn, &cs);
+    a.rope_cs[(long)r * half + j] = make_float2(cs * a.g.mscale, sn * a.g.mscale);
+  }
   for (int c = tid; c < a.width; c += blockDim.x) {
     const float v = a.src[(long)r * a.width + c];
     if (a.h) a.h[(long)r * a.width + c] = v;
-    ss += v * v;
-    put_operand(a.op, (long)r * a.op_ld + c, a.op_plane, v * (a.gain ? a.gain[c] : 1.f), a.op_f32);
-  }
-  if (a.ss0) {
-    ss = warp_sum(ss);
-    if ((tid & 31) == 0) red[tid >> 5] = ss;
-    __syncthreads();
-    if (tid == 0) a.ss0[r] = red[0] + red[1] + red[2] + red[3];
+    else put_operand(a.op, (long)r * a.op_ld + c, a.op_plane, v, a.op_f32);
   }
 }
 
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s) {
-  init_kernel<<<a.n_rows + 1, 128, 0, s>>>(a, blob);
+  launch_pdl(init_kernel, dim3(a.n_rows + 1), dim3(128), 0, s, a, blob);
 }
 
-__global__ void __launch_bounds__(128) final_norm_kernel(const float* h, const float* ss, const float* gain,
-                                                         float* out, int H, float eps) {
-  const int tok = blockIdx.x;
-  const float r = rsqrtf(ss[tok] / (float)H + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x)
-    out[(long)tok * H + c] = h[(long)tok * H + c] * gain[c] * r;
+__global__ void __launch_bounds__(128) final_norm_kernel(const float* h, const float* gain, float* out, int H,
+                                                         float eps, float* zero_ptr, long zero_n) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tok = blockIdx.x, tid = threadIdx.x;
+  __shared__ float red[4];
+  float ss = 0.f;
+  for (int c = tid; c < H; c += blockDim.x) {
+    const float v = h[(long)tok * H + c];
+    ss += v * v;
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  const float r = rsqrtf((red[0] + red[1] + red[2] + red[3]) / (float)H + eps);
+  for (int c = tid; c < H; c += blockDim.x) out[(long)tok * H + c] = h[(long)tok * H + c] * gain[c] * r;
+  if (zero_ptr) {
+    const long n4 = zero_n / 4;
+    const long lo = n4 * tok / gridDim.x, hi = n4 * (tok + 1) / gridDim.x;
+    for (long k = lo + tid; k < hi; k += blockDim.x)
+      reinterpret_cast<float4*>(zero_ptr)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
 }
 
-void launch_final_norm(const float* h, const float* ss, const float* gain, float* out, int n_tok,
+void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, float* zero_ptr, long zero_n,
                        const Geo& g, cudaStream_t s) {
-  final_norm_kernel<<<n_tok, 128, 0, s>>>(h, ss, gain, out, g.H, g.eps);
+  launch_pdl(final_norm_kernel, dim3(n_tok), dim3(128), 0, s, h, gain, out, g.H, g.eps, zero_ptr, zero_n);
 }
 
 __global__ void kv_read_kernel(Geo g, const void* kpool, const void* vpool, const int* block_table,
                                int slot, int layer, int row0, float* k_out, float* v_out) {
+  pdl_wait();
   const int rr = blockIdx.x, row = row0 + rr;
   const int page = block_table[(long)slot * g.pages_per_seq + row / kPage];
   const int off = row % kPage;

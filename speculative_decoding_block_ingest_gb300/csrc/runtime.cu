@@ -58,8 +58,8 @@ struct Layout {
   size_t s_fc, s_qkv, s_o, s_gu, s_down, s_kvall;       // fp8 row scales
   size_t hn, fn, in_ln, post_ln, qn, kn;                // norm gains
   size_t kpool, vpool, btab, inv_freq;
-  size_t h, op_h, op_taps, op_o, op_a, q, ss;
-  size_t part, counters, apart_o, apart_ml, rdesc, idesc, err;
+  size_t h, op_h, op_taps, op_o, qkv_acc, gu_acc, r_in, r_post, ss;
+  size_t gacc, rope_cs, counters, apart_o, apart_ml, rdesc, idesc, err;
   size_t total;
   int Mt, pps, max_tiles, grid_max, items_cap, n_sites;
 };
@@ -118,10 +118,13 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.op_h = take(Mt * H * 4);
   Lo.op_taps = take(Mt * nH * 4);
   Lo.op_o = take(Mt * Hq * d * 4);
-  Lo.op_a = take(Mt * I * 4);
-  Lo.q = take(Mt * Hq * d * 4);
-  Lo.ss = take((2 * L + 2) * Mt * 4);
-  Lo.part = take((size_t)(Lo.grid_max + Lo.max_tiles) * Mt * kTileN * 4);
+  Lo.qkv_acc = take(Mt * qkv_n * 4);
+  Lo.gu_acc = take(Mt * 2 * I * 4);
+  Lo.r_in = take(Mt * 4);
+  Lo.r_post = take(Mt * 4);
+  Lo.ss = take((2 * L + 2) * Mt * 4);   // [2L+1]: ingest feature sums of squares
+  Lo.gacc = take((size_t)Lo.max_tiles * kTileN * kPassTok * 4);
+  Lo.rope_cs = take(Mt * d / 2 * 8);
   Lo.counters = take((size_t)Lo.n_sites * Lo.max_tiles * 4);
   Lo.apart_o = take((size_t)Lo.items_cap * R * d * 4);
   Lo.apart_ml = take((size_t)Lo.items_cap * R * 2 * 4);
@@ -233,7 +236,8 @@ struct dflash_handle {
   int64_t launches = 0;
   // tensor maps of the tensor-core projections: weights per GEMM site, operands per buffer
   std::vector<CUtensorMap> wmap;
-  CUtensorMap xmap_taps, xmap_h, xmap_o, xmap_a;
+  CUtensorMap xmap_taps, xmap_h, xmap_o;
+  CUtensorMap kmap, vmap;                       // attention: K pool, V^T pool
   bool use_tc = false;
   bool prof_on = false;
   struct Rec {
@@ -243,6 +247,14 @@ struct dflash_handle {
   };
   std::vector<Rec> recs;
   std::vector<cudaEvent_t> event_pool;
+  // launch trace (per-CTA timestamps) into a caller buffer
+  unsigned long long* trace_buf = nullptr;
+  size_t trace_cap = 0, trace_used = 0;   // in u64 words
+  struct TraceRec {
+    int kind, grid;
+    int64_t offset;
+  };
+  std::vector<TraceRec> trace_recs;
   template <class T>
   T* at(size_t off) { return reinterpret_cast<T*>(ws + off); }
 };
@@ -280,6 +292,17 @@ struct Launch {
   }
 };
 
+// Next free trace region for a launch of `grid` CTAs (null when tracing is off or full).
+unsigned long long* trace_slot(dflash_t* h, int kind, int grid) {
+  if (!h->trace_buf) return nullptr;
+  const size_t words = (size_t)grid * kTraceWords;
+  if (h->trace_used + words > h->trace_cap) return nullptr;
+  unsigned long long* p = h->trace_buf + h->trace_used;
+  h->trace_recs.push_back({kind, grid, (int64_t)h->trace_used});
+  h->trace_used += words;
+  return p;
+}
+
 // Reserve pages so that slot covers `rows` rows; records block-table entries.
 bool ensure_pages(dflash_t* h, int slot, int64_t rows, InitBlob& blob, std::vector<int>& taken) {
   const int need = (int)((rows + kPage - 1) / kPage);
@@ -310,55 +333,90 @@ void rollback_pages(dflash_t* h, const InitBlob& blob, const std::vector<int>& t
 EpiArgs base_epi(dflash_t* h) {
   EpiArgs e{};
   e.g = h->g;
-  e.inv_freq = h->at<double>(h->lo.inv_freq);
-  e.block_table = h->at<int>(h->lo.btab);
+  e.rope_cs = h->at<float2>(h->lo.rope_cs);
   e.kpool = h->at<void>(h->lo.kpool);
   e.vpool = h->at<void>(h->lo.vpool);
-  e.rd = h->at<RoundDesc>(h->lo.rdesc);
-  e.id = h->at<IngestDesc>(h->lo.idesc);
   e.err = h->at<int>(h->lo.err);
   e.op_f32 = h->cfg.weight_dtype == DFLASH_F32;
   return e;
 }
 
-// One projection: passes of <= 256 token columns; tensor cores for bf16
-// weights, CUDA cores for f32 weights (and, for now, fp8 weights).
-void run_gemm(dflash_t* h, int site, const void* W, const float* wscale, int N, int K, const void* X,
-              const CUtensorMap* xmap, EpiArgs e, cudaStream_t s) {
+// One projection call: where its operand comes from, where its result goes,
+// and its side duties.
+struct GemmSpec {
+  int site;                     // counter block of O_TILE calls
+  const void* W;
+  const float* wscale;
+  int N, K;
+  int xmode = X_PLANES;
+  const void* X = nullptr;      // X_PLANES
+  const CUtensorMap* xmap = nullptr;
+  const float* xsrc = nullptr;  // X_FROM_H / X_SWIGLU
+  int xsrc_ld = 0;
+  const float* xgain = nullptr;
+  const float* xrs = nullptr;
+  int omode = O_TILE;
+  float* dst = nullptr;         // O_RED
+  int dst_ld = 0;
+  const float* rs_src = nullptr;
+  int rs_ld = 0, rs_len = 0;
+  float* rs_out = nullptr;
+  float* zero_ptr = nullptr;
+  long zero_n = 0;
+  EpiArgs e;
+};
+
+// Passes of <= 256 token columns; tensor cores for bf16 weights, CUDA cores
+// for f32 weights (and, for now, fp8 weights).
+void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
   const Geo& g = h->g;
-  const int n_all = e.n_tok;
-  for (int base = 0; base < n_all; base += 256) {
+  const int n_all = sp.e.n_tok;
+  for (int base = 0; base < n_all; base += kPassTok) {
     GemmArgs a{};
-    a.W = W;
-    a.N = N;
-    a.K = K;
-    a.X = X;
-    a.x_ld = K;
-    a.x_plane = (long)h->lo.Mt * K;
+    a.W = sp.W;
+    a.N = sp.N;
+    a.K = sp.K;
+    a.xmode = sp.xmode;
+    a.X = sp.X;
+    a.x_ld = sp.K;
+    a.x_plane = (long)h->lo.Mt * sp.K;
     a.x_f32 = h->cfg.weight_dtype == DFLASH_F32;
-    a.n_tiles = N / kTileN;
-    a.p.kb = K / kTileK;
+    a.xsrc = sp.xsrc;
+    a.xsrc_ld = sp.xsrc_ld;
+    a.xgain = sp.xgain;
+    a.xrs = sp.xrs;
+    a.omode = sp.omode;
+    a.dst = sp.dst;
+    a.dst_ld = sp.dst_ld;
+    a.rs_src = sp.rs_src;
+    a.rs_ld = sp.rs_ld;
+    a.rs_len = sp.rs_len;
+    a.rs_out = sp.rs_out;
+    a.zero_ptr = base == 0 ? sp.zero_ptr : nullptr;
+    a.zero_n = sp.zero_n;
+    a.n_tiles = sp.N / kTileN;
+    a.p.kb = sp.K / kTileK;
     a.p.units = a.n_tiles * a.p.kb;
     a.p.grid = std::min(a.p.units, h->use_tc ? h->n_sm : h->lo.grid_max);
-    a.part = h->at<float>(h->lo.part);
-    a.counters = h->at<int>(h->lo.counters) + (size_t)site * h->lo.max_tiles;
-    e.wscale = wscale;
-    e.tok_base = base;
-    e.n_tok = std::min(256, n_all - base);
-    a.e = e;
-    const double nt = e.n_tok;
-    double out_b = 0;
-    switch (e.kind) {
-      case EPI_FC: out_b = nt * N * 4; break;
-      case EPI_KV: out_b = nt * N * (g.kvtype == KV_F32 ? 4 : 2); break;
-      case EPI_QKV: out_b = nt * N * (g.kvtype == KV_F32 ? 4 : 2); break;
-      case EPI_RESID: out_b = nt * N * 12; break;
-      default: out_b = nt * N / 2 * 4; break;
-    }
-    const double bytes =
-        (double)N * K * esize_w(g.wtype) + (g.wtype == W_FP8 ? N * 4.0 : 0.0) + nt * K * 4 + out_b;
+    a.acc = h->at<float>(h->lo.gacc);
+    a.counters = h->at<int>(h->lo.counters) + (size_t)sp.site * h->lo.max_tiles;
+    a.e = sp.e;
+    a.e.wscale = sp.wscale;
+    a.e.tok_base = base;
+    a.e.n_tok = std::min(kPassTok, n_all - base);
+    const double nt = a.e.n_tok;
+    // algorithmic bytes: weights (+ scales), the operand once, the result once
+    double x_b = nt * sp.K * (sp.xmode == X_SWIGLU ? 8 : 4);
+    double out_b;
+    if (sp.omode == O_RED) out_b = nt * sp.N * 4;
+    else if (sp.e.kind == EPI_RESID) out_b = nt * sp.N * 12;
+    else if (sp.e.kind == EPI_SWIGLU) out_b = nt * sp.N / 2 * 4;
+    else if (sp.e.kind == EPI_FC) out_b = nt * sp.N * 4;
+    else out_b = nt * sp.N * (g.kvtype == KV_F32 ? 4 : 2);
+    const double bytes = (double)sp.N * sp.K * esize_w(g.wtype) + (g.wtype == W_FP8 ? sp.N * 4.0 : 0.0) + x_b + out_b;
     Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
-    if (h->use_tc) launch_gemm_tc(a, &h->wmap[site], xmap, s);
+    a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_GEMM, a.p.grid) : nullptr;
+    if (h->use_tc) launch_gemm_tc(a, &h->wmap[sp.site], sp.xmap, s);
     else launch_gemm_simt(a, s);
   }
   ck(cudaGetLastError(), "gemm launch");
@@ -375,6 +433,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   ia.src = taps;
   ia.n_rows = n_rows;
   ia.width = width;
+  ia.h = nullptr;
   ia.op = h->at<void>(h->lo.op_taps);
   ia.op_ld = width;
   ia.op_plane = (long)h->lo.Mt * width;
@@ -385,6 +444,9 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   ia.desc_dst = h->at<void>(h->lo.idesc);
   ia.desc_bytes = sizeof(IngestDesc);
   ia.block_table = h->at<int>(h->lo.btab);
+  ia.inv_freq = h->at<double>(h->lo.inv_freq);
+  ia.rope_cs = h->at<float2>(h->lo.rope_cs);
+  ia.is_round = 0;
   ia.g = g;
   {
     Launch L(h, DFLASH_KERNEL_INIT, (double)n_rows * width * 8, s);
@@ -393,88 +455,122 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   ck(cudaGetLastError(), "ingest init launch");
 
   // fc over the taps; epilogue: feats operand (c * hidden_norm) + sum c^2
-  EpiArgs e = base_epi(h);
-  e.kind = EPI_FC;
-  e.n_tok = n_rows;
-  e.ss_out = ss_feat;
-  e.gain = h->at<float>(h->lo.hn);
-  e.op = h->at<void>(h->lo.op_h);
-  e.op_ld = g.H;
-  e.op_plane = (long)h->lo.Mt * g.H;
   const bool fp8 = h->cfg.weight_dtype == DFLASH_FP8_E4M3;
-  run_gemm(h, 0, h->at<void>(h->lo.fc), fp8 ? h->at<float>(h->lo.s_fc) : nullptr, g.H, width,
-           h->at<void>(h->lo.op_taps), &h->xmap_taps, e, s);
+  GemmSpec fc;
+  fc.site = 0;
+  fc.W = h->at<void>(h->lo.fc);
+  fc.wscale = fp8 ? h->at<float>(h->lo.s_fc) : nullptr;
+  fc.N = g.H;
+  fc.K = width;
+  fc.X = h->at<void>(h->lo.op_taps);
+  fc.xmap = &h->xmap_taps;
+  fc.e = base_epi(h);
+  fc.e.kind = EPI_FC;
+  fc.e.n_tok = n_rows;
+  fc.e.ss_out = ss_feat;
+  fc.e.gain = h->at<float>(h->lo.hn);
+  fc.e.op = h->at<void>(h->lo.op_h);
+  fc.e.op_ld = g.H;
+  fc.e.op_plane = (long)h->lo.Mt * g.H;
+  run_gemm(h, fc, s);
 
   // K/V of every layer in one projection; epilogue: hidden_norm scale,
   // k head-norm + RoPE, paged write.
-  EpiArgs k = base_epi(h);
-  k.kind = EPI_KV;
-  k.n_tok = n_rows;
-  k.ss_in = ss_feat;
-  k.kn = h->at<float>(h->lo.kn);
-  run_gemm(h, 1, h->at<void>(h->lo.kvall), fp8 ? h->at<float>(h->lo.s_kvall) : nullptr, g.L * g.kv_n, g.H,
-           h->at<void>(h->lo.op_h), &h->xmap_h, k, s);
+  GemmSpec kv;
+  kv.site = 1;
+  kv.W = h->at<void>(h->lo.kvall);
+  kv.wscale = fp8 ? h->at<float>(h->lo.s_kvall) : nullptr;
+  kv.N = g.L * g.kv_n;
+  kv.K = g.H;
+  kv.X = h->at<void>(h->lo.op_h);
+  kv.xmap = &h->xmap_h;
+  kv.e = base_epi(h);
+  kv.e.kind = EPI_KV;
+  kv.e.n_tok = n_rows;
+  kv.e.ss_in = ss_feat;
+  kv.e.kn = h->at<float>(h->lo.kn);
+  kv.e.dest = h->at<IngestDesc>(h->lo.idesc)->row_dest;
+  run_gemm(h, kv, s);
 }
 
 int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens) {
   long units = 0;
-  for (auto L : lens) units += (long)h->g.Hkv * ((L + kBlock + kPage - 1) / kPage);
-  const long target = 2L * h->n_sm;
+  for (auto L : lens) units += (long)h->g.Hkv * std::max<int64_t>(1, (L + kPage - 1) / kPage);
+  const long target = h->use_tc ? (long)h->n_sm : 2L * h->n_sm;
   return (int)std::max<long>(1, (units + target - 1) / target);
 }
 
+// The round: per layer QKV -> attention -> combine -> O -> gate/up -> down.
+// Projections add straight into token-major accumulators (QKV, gate/up) or
+// into the residual stream h (O, down); their consumers apply the norms and
+// SwiGLU while building their own operands, so no projection ends in a
+// serial epilogue.  Row scales rsqrt(mean(h^2)+eps) are computed by the
+// projection that reads h; spent accumulators are cleared by a later kernel.
 void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, cudaStream_t s) {
   const Geo& g = h->g;
   RoundDesc& rd = blob.round;
   const int n_tok = rd.n_tok;
   const size_t Mt = h->lo.Mt;
-  float* ss = h->at<float>(h->lo.ss);
-  auto ss_in = [&](int l) { return ss + (size_t)l * Mt; };
-  auto ss_post = [&](int l) { return ss + (size_t)(g.L + l) * Mt; };
-  float* ss_fin = ss + (size_t)(2 * g.L) * Mt;
   const bool fp8 = h->cfg.weight_dtype == DFLASH_FP8_E4M3;
   const size_t ew = wbytes(h);
+  float* hres = h->at<float>(h->lo.h);
+  float* qkv_acc = h->at<float>(h->lo.qkv_acc);
+  float* gu_acc = h->at<float>(h->lo.gu_acc);
+  float* r_in = h->at<float>(h->lo.r_in);
+  float* r_post = h->at<float>(h->lo.r_post);
+  const long qkv_acc_n = (long)n_tok * g.qkv_n, gu_acc_n = (long)n_tok * 2 * g.I;
 
   InitArgs ia{};
   ia.src = noise;
   ia.n_rows = n_tok;
   ia.width = g.H;
-  ia.h = h->at<float>(h->lo.h);
-  ia.ss0 = ss_in(0);
-  ia.gain = h->at<float>(h->lo.in_ln);
-  ia.op = h->at<void>(h->lo.op_h);
-  ia.op_ld = g.H;
-  ia.op_plane = (long)Mt * g.H;
-  ia.op_f32 = h->cfg.weight_dtype == DFLASH_F32;
-  ia.zero_ptr = ss + Mt;                    // every per-token accumulator after ss_in(0)
-  ia.zero_n = (int)((2 * g.L + 1 - 1) * Mt);
+  ia.h = hres;
   ia.desc_dst = h->at<void>(h->lo.rdesc);
   ia.desc_bytes = sizeof(RoundDesc);
   ia.block_table = h->at<int>(h->lo.btab);
+  ia.inv_freq = h->at<double>(h->lo.inv_freq);
+  ia.rope_cs = h->at<float2>(h->lo.rope_cs);
+  ia.is_round = 1;
   ia.g = g;
   {
-    Launch L(h, DFLASH_KERNEL_INIT, (double)n_tok * g.H * 12, s);
+    Launch L(h, DFLASH_KERNEL_INIT, (double)n_tok * g.H * 8, s);
     launch_init(ia, blob, s);
   }
   ck(cudaGetLastError(), "round init launch");
 
   for (int l = 0; l < g.L; ++l) {
-    // QKV: epilogue = input-norm scale, q/k head-norm + RoPE, block K/V into the pages
-    EpiArgs e = base_epi(h);
-    e.kind = EPI_QKV;
-    e.layer = l;
-    e.n_tok = n_tok;
-    e.ss_in = ss_in(l);
-    e.qn = h->at<float>(h->lo.qn) + (size_t)l * g.d;
-    e.kn = h->at<float>(h->lo.kn) + (size_t)l * g.d;
-    e.q_out = h->at<void>(h->lo.q);
-    run_gemm(h, 2 + 4 * l, h->at<char>(h->lo.qkv) + (size_t)l * g.qkv_n * g.H * ew,
-             fp8 ? h->at<float>(h->lo.s_qkv) + (size_t)l * g.qkv_n : nullptr, g.qkv_n, g.H,
-             h->at<void>(h->lo.op_h), &h->xmap_h, e, s);
+    // QKV of RMSNorm(h; input_ln) -> QKV accumulator; r_in from h; clears the
+    // previous layer's gate/up accumulator
+    GemmSpec q;
+    q.site = 2 + 4 * l;
+    q.W = h->at<char>(h->lo.qkv) + (size_t)l * g.qkv_n * g.H * ew;
+    q.wscale = fp8 ? h->at<float>(h->lo.s_qkv) + (size_t)l * g.qkv_n : nullptr;
+    q.N = g.qkv_n;
+    q.K = g.H;
+    q.xmode = X_FROM_H;
+    q.xsrc = hres;
+    q.xsrc_ld = g.H;
+    q.xgain = h->at<float>(h->lo.in_ln) + (size_t)l * g.H;
+    q.omode = O_RED;
+    q.dst = qkv_acc;
+    q.dst_ld = g.qkv_n;
+    q.rs_src = hres;
+    q.rs_ld = g.H;
+    q.rs_len = g.H;
+    q.rs_out = r_in;
+    q.zero_ptr = l > 0 ? gu_acc : nullptr;
+    q.zero_n = gu_acc_n;
+    q.e = base_epi(h);
+    q.e.n_tok = n_tok;
+    run_gemm(h, q, s);
 
     // attention over [cached ctx ; block] K/V, split over keys, then merge
     AttnArgs a{};
-    a.q = h->at<void>(h->lo.q);
+    a.qkv = qkv_acc;
+    a.r_in = r_in;
+    a.qn = h->at<float>(h->lo.qn) + (size_t)l * g.d;
+    a.kn = h->at<float>(h->lo.kn) + (size_t)l * g.d;
+    a.rope_cs = h->at<float2>(h->lo.rope_cs);
     a.kpool = h->at<void>(h->lo.kpool);
     a.vpool = h->at<void>(h->lo.vpool);
     a.layer = l;
@@ -486,16 +582,18 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     a.op_ld = g.Hq * g.d;
     a.op_plane = (long)Mt * g.Hq * g.d;
     a.op_f32 = h->cfg.weight_dtype == DFLASH_F32;
-    a.scale = 1.f / std::sqrt((float)g.d);
+    a.scale_log2 = 1.4426950408889634f / std::sqrt((float)g.d);
     a.err = h->at<int>(h->lo.err);
     a.g = g;
     const double ekv = g.kvtype == KV_F32 ? 4 : 2;
     const double part_b = (double)rd.n_items * g.G * kBlock * (g.d + 2) * 4;
     {
       double kv_b = 0;
-      for (int i = 0; i < rd.n_seq; ++i) kv_b += (double)(rd.len[i] + kBlock) * g.Hkv * g.d * 2 * ekv;
-      Launch L(h, DFLASH_KERNEL_ATTENTION, kv_b + (double)n_tok * g.Hq * g.d * ekv + part_b, s);
-      launch_attention_simt(a, rd.n_items, s);
+      for (int i = 0; i < rd.n_seq; ++i) kv_b += (double)rd.len[i] * g.Hkv * g.d * 2 * ekv;
+      Launch L(h, DFLASH_KERNEL_ATTENTION, kv_b + (double)n_tok * g.qkv_n * 4 + part_b, s);
+      a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_ATTENTION, rd.n_items) : nullptr;
+      if (h->use_tc) launch_attention_tc(a, rd.n_items, &h->kmap, &h->vmap, s);
+      else launch_attention_simt(a, rd.n_items, s);
     }
     ck(cudaGetLastError(), "attention launch");
     {
@@ -504,52 +602,67 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     }
     ck(cudaGetLastError(), "attention combine launch");
 
-    // O projection + residual; operand for the MLP = h * post_ln
-    EpiArgs o = base_epi(h);
-    o.kind = EPI_RESID;
-    o.n_tok = n_tok;
-    o.h = h->at<float>(h->lo.h);
-    o.h_ld = g.H;
-    o.gain = h->at<float>(h->lo.post_ln) + (size_t)l * g.H;
-    o.ss_out = ss_post(l);
-    o.op = h->at<void>(h->lo.op_h);
-    o.op_ld = g.H;
-    o.op_plane = (long)Mt * g.H;
-    run_gemm(h, 3 + 4 * l, h->at<char>(h->lo.o) + (size_t)l * g.H * g.Hq * g.d * ew,
-             fp8 ? h->at<float>(h->lo.s_o) + (size_t)l * g.H : nullptr, g.H, g.Hq * g.d,
-             h->at<void>(h->lo.op_o), &h->xmap_o, o, s);
+    // O projection added into h; clears the QKV accumulator
+    GemmSpec o;
+    o.site = 3 + 4 * l;
+    o.W = h->at<char>(h->lo.o) + (size_t)l * g.H * g.Hq * g.d * ew;
+    o.wscale = fp8 ? h->at<float>(h->lo.s_o) + (size_t)l * g.H : nullptr;
+    o.N = g.H;
+    o.K = g.Hq * g.d;
+    o.X = h->at<void>(h->lo.op_o);
+    o.xmap = &h->xmap_o;
+    o.omode = O_RED;
+    o.dst = hres;
+    o.dst_ld = g.H;
+    o.zero_ptr = qkv_acc;
+    o.zero_n = qkv_acc_n;
+    o.e = base_epi(h);
+    o.e.n_tok = n_tok;
+    run_gemm(h, o, s);
 
-    // gate/up (interleaved per 64 rows) + SwiGLU
-    EpiArgs gu = base_epi(h);
-    gu.kind = EPI_SWIGLU;
-    gu.n_tok = n_tok;
-    gu.ss_in = ss_post(l);
-    gu.op = h->at<void>(h->lo.op_a);
-    gu.op_ld = g.I;
-    gu.op_plane = (long)Mt * g.I;
-    run_gemm(h, 4 + 4 * l, h->at<char>(h->lo.gu) + (size_t)l * 2 * g.I * g.H * ew,
-             fp8 ? h->at<float>(h->lo.s_gu) + (size_t)l * 2 * g.I : nullptr, 2 * g.I, g.H,
-             h->at<void>(h->lo.op_h), &h->xmap_h, gu, s);
+    // gate/up of RMSNorm(h; post_ln) -> gate/up accumulator; r_post from h
+    GemmSpec gu;
+    gu.site = 4 + 4 * l;
+    gu.W = h->at<char>(h->lo.gu) + (size_t)l * 2 * g.I * g.H * ew;
+    gu.wscale = fp8 ? h->at<float>(h->lo.s_gu) + (size_t)l * 2 * g.I : nullptr;
+    gu.N = 2 * g.I;
+    gu.K = g.H;
+    gu.xmode = X_FROM_H;
+    gu.xsrc = hres;
+    gu.xsrc_ld = g.H;
+    gu.xgain = h->at<float>(h->lo.post_ln) + (size_t)l * g.H;
+    gu.omode = O_RED;
+    gu.dst = gu_acc;
+    gu.dst_ld = 2 * g.I;
+    gu.rs_src = hres;
+    gu.rs_ld = g.H;
+    gu.rs_len = g.H;
+    gu.rs_out = r_post;
+    gu.e = base_epi(h);
+    gu.e.n_tok = n_tok;
+    run_gemm(h, gu, s);
 
-    // down + residual; operand for the next layer = h * input_ln[l+1]
-    EpiArgs dn = base_epi(h);
-    dn.kind = EPI_RESID;
-    dn.n_tok = n_tok;
-    dn.h = h->at<float>(h->lo.h);
-    dn.h_ld = g.H;
-    const bool last = l + 1 == g.L;
-    dn.gain = last ? nullptr : h->at<float>(h->lo.in_ln) + (size_t)(l + 1) * g.H;
-    dn.ss_out = last ? ss_fin : ss_in(l + 1);
-    dn.op = last ? nullptr : h->at<void>(h->lo.op_h);
-    dn.op_ld = g.H;
-    dn.op_plane = (long)Mt * g.H;
-    run_gemm(h, 5 + 4 * l, h->at<char>(h->lo.down) + (size_t)l * g.H * g.I * ew,
-             fp8 ? h->at<float>(h->lo.s_down) + (size_t)l * g.H : nullptr, g.H, g.I,
-             h->at<void>(h->lo.op_a), &h->xmap_a, dn, s);
+    // down of SwiGLU(gate/up) added into h
+    GemmSpec dn;
+    dn.site = 5 + 4 * l;
+    dn.W = h->at<char>(h->lo.down) + (size_t)l * g.H * g.I * ew;
+    dn.wscale = fp8 ? h->at<float>(h->lo.s_down) + (size_t)l * g.H : nullptr;
+    dn.N = g.H;
+    dn.K = g.I;
+    dn.xmode = X_SWIGLU;
+    dn.xsrc = gu_acc;
+    dn.xsrc_ld = 2 * g.I;
+    dn.xrs = r_post;
+    dn.omode = O_RED;
+    dn.dst = hres;
+    dn.dst_ld = g.H;
+    dn.e = base_epi(h);
+    dn.e.n_tok = n_tok;
+    run_gemm(h, dn, s);
   }
   {
     Launch L(h, DFLASH_KERNEL_NORM, (double)n_tok * g.H * 8, s);
-    launch_final_norm(h->at<float>(h->lo.h), ss_fin, h->at<float>(h->lo.fn), out, n_tok, g, s);
+    launch_final_norm(hres, h->at<float>(h->lo.fn), out, n_tok, gu_acc, gu_acc_n, g, s);
   }
   ck(cudaGetLastError(), "final norm launch");
 }
@@ -560,8 +673,8 @@ void plan_attention(dflash_t* h, RoundDesc& rd, const std::vector<int64_t>& lens
   int items = 0;
   for (int s = 0; s < rd.n_seq; ++s) {
     rd.item0[s] = items;
-    const int pages = (int)((lens[s] + kBlock + kPage - 1) / kPage);
-    items += h->g.Hkv * ((pages + rd.split_pages - 1) / rd.split_pages);
+    const int pages = (int)((lens[s] + kPage - 1) / kPage);   // cached-context pages
+    items += h->g.Hkv * std::max(1, (pages + rd.split_pages - 1) / rd.split_pages);
   }
   rd.item0[rd.n_seq] = items;
   rd.n_items = items;
@@ -618,8 +731,8 @@ int ingest_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* t_
       return fail(DFLASH_ERR_CAPACITY, "out of KV pages");
     }
     for (int j = 0; j < t_per_seq[i]; ++j, ++r) {
-      id.row_slot[r] = slot;
-      id.row_dst[r] = (int)h->len[slot] + j;
+      const int64_t row = h->len[slot] + j;
+      id.row_dest[r] = h->pages[slot][row / kPage] * kPage + (int)(row % kPage);
       id.row_pos[r] = pos_new[r];
     }
   }
@@ -654,11 +767,6 @@ int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos
     rd.seq_slot[i] = slot;
     rd.len[i] = (int)lens[i];
     for (int j = 0; j < kBlock; ++j) rd.pos[i * kBlock + j] = pos_block[i * kBlock + j];
-    if (!ensure_pages(h, slot, lens[i] + kBlock, *blob, taken)) {
-      rollback_pages(h, *blob, taken);
-      delete blob;
-      return fail(DFLASH_ERR_CAPACITY, "out of KV pages for the block rows");
-    }
   }
   plan_attention(h, rd, lens);
   if (rd.n_items > h->lo.items_cap) {
@@ -807,10 +915,19 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       h->xmap_taps = make_map_bf16(h->ws + lo.op_taps, Mt2, (uint64_t)g.n * H, 16);
       h->xmap_h = make_map_bf16(h->ws + lo.op_h, Mt2, H, 16);
       h->xmap_o = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, 16);
-      h->xmap_a = make_map_bf16(h->ws + lo.op_a, Mt2, I, 16);
+
+      const uint64_t pool_rows = (uint64_t)L * cfg->max_pages * Hkv;
+      h->kmap = make_map_bf16(h->ws + lo.kpool, pool_rows * kPage, d, kPage);
+      h->vmap = make_map_bf16(h->ws + lo.vpool, pool_rows * d, kPage, d);
     }
+    // stale pool rows are read (and masked) by the attention MMA: keep them finite
+    ck(cudaMemsetAsync(h->ws + lo.kpool, 0, lo.vpool - lo.kpool, s), "K pool clear");
+    ck(cudaMemsetAsync(h->ws + lo.vpool, 0, lo.btab - lo.vpool, s), "V pool clear");
     ck(cudaMemsetAsync(h->ws + lo.btab, 0xff, (size_t)(cfg->max_seqs + 1) * lo.pps * 4, s), "block table");
     ck(cudaMemsetAsync(h->ws + lo.counters, 0, (size_t)lo.n_sites * lo.max_tiles * 4, s), "counters");
+    ck(cudaMemsetAsync(h->ws + lo.gacc, 0, (size_t)lo.max_tiles * kTileN * kPassTok * 4, s), "tile accumulators");
+    ck(cudaMemsetAsync(h->ws + lo.qkv_acc, 0, (size_t)lo.Mt * g.qkv_n * 4, s), "QKV accumulator");
+    ck(cudaMemsetAsync(h->ws + lo.gu_acc, 0, (size_t)lo.Mt * 2 * I * 4, s), "gate/up accumulator");
     ck(cudaMemsetAsync(h->ws + lo.err, 0, 256, s), "error word");
     ck(cudaStreamSynchronize(s), "create sync");
     return DFLASH_OK;
@@ -954,6 +1071,32 @@ int dflash_profile_read(dflash_t* h, int32_t kind, int64_t* launches, double* ms
     }
     return DFLASH_OK;
   });
+}
+
+int dflash_trace_begin(dflash_t* h, void* device_buffer, size_t bytes) {
+  g_last_error.clear();
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
+  if (device_buffer && reinterpret_cast<uintptr_t>(device_buffer) % 8)
+    return fail(DFLASH_ERR_INVALID_ARG, "trace buffer must be 8-byte aligned");
+  h->trace_buf = static_cast<unsigned long long*>(device_buffer);
+  h->trace_cap = device_buffer ? bytes / 8 : 0;
+  h->trace_used = 0;
+  h->trace_recs.clear();
+  return DFLASH_OK;
+}
+
+int dflash_trace_launches(dflash_t* h, int32_t max_launches, int32_t* kinds, int32_t* grids, int64_t* offsets,
+                          int32_t* n_launches) {
+  g_last_error.clear();
+  if (!h || !n_launches) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  const int n = (int)h->trace_recs.size();
+  *n_launches = n;
+  for (int i = 0; i < n && i < max_launches; ++i) {
+    if (kinds) kinds[i] = h->trace_recs[i].kind;
+    if (grids) grids[i] = h->trace_recs[i].grid;
+    if (offsets) offsets[i] = h->trace_recs[i].offset;
+  }
+  return DFLASH_OK;
 }
 
 int dflash_launch_count(dflash_t* h, int64_t* launches) {

@@ -26,7 +26,8 @@ _DT = {"f32": F32, "bf16": BF16, "fp8": FP8}
 EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dflash_forward_round",
            "dflash_forward_full", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
            "dflash_device_status", "dflash_destroy", "dflash_last_error", "dflash_profile_enable",
-           "dflash_profile_read", "dflash_launch_count")
+           "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches")
+TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
 KERNEL_KINDS = ("gemm", "attention", "combine", "init", "norm")
 
 
@@ -81,6 +82,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_profile_read.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_double)]
     lib.dflash_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
+    lib.dflash_trace_begin.argtypes = [vp, vp, ctypes.c_size_t]
+    lib.dflash_trace_launches.argtypes = [vp, i32, p32, p32, ctypes.POINTER(ctypes.c_int64), p32]
     lib.dflash_destroy.argtypes = [vp]
     lib.dflash_destroy.restype = None
     lib.dflash_last_error.restype = ctypes.c_char_p
@@ -238,6 +241,26 @@ class Drafter:
             n, ms, b = ctypes.c_int64(0), ctypes.c_double(0), ctypes.c_double(0)
             _check(self.lib.dflash_profile_read(self.handle, i, ctypes.byref(n), ctypes.byref(ms), ctypes.byref(b)))
             out[name] = (n.value, ms.value, b.value)
+        return out
+
+    def trace_begin(self, words: int):
+        """Start tracing into a fresh device buffer of `words` u64 words."""
+        self._trace = torch.zeros(words, dtype=torch.int64, device=self.device)
+        _check(self.lib.dflash_trace_begin(self.handle, ctypes.c_void_p(self._trace.data_ptr()), words * 8))
+
+    def trace_end(self):
+        """Stop tracing; returns [(kind, grid, tensor[grid, 8])] per traced launch."""
+        n = ctypes.c_int32(0)
+        _check(self.lib.dflash_trace_launches(self.handle, 0, None, None, None, ctypes.byref(n)))
+        k = (ctypes.c_int32 * max(1, n.value))()
+        g = (ctypes.c_int32 * max(1, n.value))()
+        o = (ctypes.c_int64 * max(1, n.value))()
+        _check(self.lib.dflash_trace_launches(self.handle, n.value, k, g, o, ctypes.byref(n)))
+        _check(self.lib.dflash_trace_begin(self.handle, None, 0))
+        torch.cuda.synchronize(self.device)
+        buf = self._trace.cpu()
+        out = [(k[i], g[i], buf[o[i]:o[i] + TRACE_WORDS * g[i]].view(g[i], TRACE_WORDS)) for i in range(n.value)]
+        self._trace = None
         return out
 
     def launch_count(self) -> int:
