@@ -176,7 +176,9 @@ enum dflash_kernel_kind {
   DFLASH_KERNEL_COMBINE = 2,    /* merge of the split-KV partial softmaxes                        */
   DFLASH_KERNEL_INIT = 3,       /* per-call descriptor upload and residual / operand set-up       */
   DFLASH_KERNEL_NORM = 4,       /* final RMSNorm                                                  */
-  DFLASH_KERNEL_KINDS = 5
+  DFLASH_KERNEL_FINISH = 5,     /* element-wise steps between projections (norm operands, q/k
+                                   head-norm + RoPE and block K/V rows, SwiGLU)                   */
+  DFLASH_KERNEL_KINDS = 6
 };
 
 /* Measurement (not needed to draft).  While enabled, every kernel launch

@@ -1,27 +1,21 @@
 // attn_tc.cu -- non-causal block attention over the paged KV cache on the
 // 5th-generation tensor cores.
 //
-// One CTA per work item (sequence, kv head, split of the cached keys).  The
-// G q-heads x 16 block rows that share a kv head form one M = 128 query tile
-// (rows padded with zeros when G*16 < 128), so each K/V page is read once per
-// item:
-//   warp 0 (one lane)  TMA: the split's K pages [64 x d] and V^T pages
-//                      [d x 64] through a ring of stages;
+// One CTA per work item (sequence, kv head, split of the keys [cached context
+// ; 16 block rows]).  The G q-heads x 16 block rows that share a kv head form
+// one M = 128 query tile (rows padded with zeros when G*16 < 128), so each
+// K/V page is read once per item:
+//   warp 0 (one lane)  TMA: the query tile, then the split's K pages [64 x d]
+//                      and V^T pages [d x 64] through a ring of stages;
 //   warp 1 (one lane)  tcgen05.mma: S = Q K^T into one of two TMEM buffers,
 //                      then O += P V^T into the TMEM output accumulator;
-//   warps 2..5         first build the query tile from the QKV accumulator
-//                      (input-norm scale, q head RMSNorm, RoPE, bf16) and, in
-//                      a sequence's last split, the 16 block rows' K and V^T
-//                      as one more "page" in shared memory (the block's K/V are
-//                      transient: they never go to HBM); then the softmax, one
-//                      thread per query row: scores from TMEM, exp2 with a
-//                      running max, P (bf16) into shared memory in the
-//                      128-byte swizzle the MMA reads.  O is rescaled only when
-//                      a row's max grows by more than 2^8 (exact: the final
-//                      division uses the same max).
-// The query tile is built while the first K/V pages stream in.  Each item
-// writes its unnormalised O with (max, sum); the combine kernel merges the
-// splits (all in log2 units).
+//   warps 2..5         softmax, one thread per query row: scores from TMEM,
+//                      exp2 with a running max, P (bf16) into shared memory in
+//                      the 128-byte swizzle the MMA reads.  O is rescaled only
+//                      when a row's max grows by more than 2^8 (exact: the
+//                      final division uses the same max).
+// Each item writes its unnormalised O with (max, sum); the combine kernel
+// merges the splits (all in log2 units).
 #include <algorithm>
 #include <cmath>
 
@@ -44,124 +38,24 @@ constexpr int kQAtomBytes = 128 * 128;   // 128 rows x 128 B
 constexpr int kKAtomBytes = 64 * 128;    // 64 keys x 128 B
 constexpr float kRescaleLog2 = 8.f;
 
-// Byte offset of element (row, col) (col in bf16 units, < 64) in a K-major
-// 128-byte-swizzled atom.
-__device__ __forceinline__ int sw128_off(int row, int col) {
-  return (row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ (row & 7))) << 4) + (col & 7) * 2;
-}
-
-// Write lane's PER dims of one row into a K-major tile of atoms atom_bytes apart.
-template <int PER>
-__device__ __forceinline__ void put_row_bf16(uint8_t* tile, int atom_bytes, int row, const float* x) {
-  const int lane = threadIdx.x & 31;
-  const int dim0 = lane * PER;
-  uint8_t* at = tile + (dim0 >> 6) * atom_bytes + sw128_off(row, dim0 & 63);
-  if (PER == 4) {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(x[2], x[3]);
-    *reinterpret_cast<uint2*>(at) =
-        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-  } else {
-    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]);
-    *reinterpret_cast<uint32_t*>(at) = *reinterpret_cast<const uint32_t*>(&a);
-  }
-}
-
-// Rows of the QKV accumulator for the query tile (block == false: rows
-// r = token * G + local head) or the block page (block == true: the 16 block
-// rows' K, normed and roped, and V^T).  Each builder warp handles 4 rows per
-// step and issues all of their loads before any arithmetic.
-template <int PER>
-__device__ __forceinline__ void build_tiles(const AttnArgs& a, int s, int kvh, bool block, uint8_t* sQ, uint8_t* sBK,
-                                            uint8_t* sBV) {
-  const Geo& g = a.g;
-  constexpr int d = 32 * PER, half = d / 2;
-  const int warp = (threadIdx.x >> 5) - 2, lane = threadIdx.x & 31;
-  const int dim0 = lane * PER;
-  const int ld = g.qkv_n;
-  const int rows = block ? kBlock : g.G * kBlock;
-  const float* gsrc = block ? a.kn : a.qn;
-  float gn[PER];
-#pragma unroll
-  for (int q = 0; q < PER; ++q) gn[q] = gsrc[dim0 + q];
-  for (int r0 = warp * 4; r0 < rows; r0 += 16) {
-    float x[4][PER], v[4][PER], rs[4];
-    float2 cs[4][PER];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int r = r0 + u;
-      if (r >= rows) continue;
-      const int i = block ? r : r / g.G;
-      const int tok = s * kBlock + i;
-      const int col0 = block ? (g.Hq + kvh) * d : (kvh * g.G + r % g.G) * d;
-      const float* src = a.qkv + (long)tok * ld + col0 + dim0;
-      if (PER == 4) {
-        const float4 t4 = __ldcg(reinterpret_cast<const float4*>(src));
-        x[u][0] = t4.x; x[u][1] = t4.y; x[u][2] = t4.z; x[u][3] = t4.w;
-      } else {
-        const float2 t2 = __ldcg(reinterpret_cast<const float2*>(src));
-        x[u][0] = t2.x; x[u][1] = t2.y;
-      }
-      if (block) {
-        const float* vsrc = a.qkv + (long)tok * ld + (g.Hq + g.Hkv + kvh) * d + dim0;
-#pragma unroll
-        for (int q = 0; q < PER; ++q) v[u][q] = __ldcg(vsrc + q);
-      }
-      rs[u] = a.r_in[tok];
-#pragma unroll
-      for (int q = 0; q < PER; ++q) cs[u][q] = a.rope_cs[(long)tok * half + (dim0 + q) % half];
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int r = r0 + u;
-      if (r >= rows) continue;
-      float ss = 0.f;
-#pragma unroll
-      for (int q = 0; q < PER; ++q) {
-        x[u][q] *= rs[u];
-        ss += x[u][q] * x[u][q];
-      }
-      ss = warp_sum(ss);
-      const float rn = rsqrtf(ss / (float)d + g.eps);
-#pragma unroll
-      for (int q = 0; q < PER; ++q) {
-        const float y = x[u][q] * rn * gn[q];
-        const float partner = __shfl_xor_sync(0xffffffffu, y, 16);   // dims j <-> j + d/2
-        x[u][q] = lane < 16 ? (y * cs[u][q].x - partner * cs[u][q].y) : (y * cs[u][q].x + partner * cs[u][q].y);
-      }
-      if (!block) {
-        put_row_bf16<PER>(sQ, kQAtomBytes, r, x[u]);
-      } else {
-        put_row_bf16<PER>(sBK, kKAtomBytes, r, x[u]);
-#pragma unroll
-        for (int q = 0; q < PER; ++q)
-          *reinterpret_cast<__nv_bfloat16*>(sBV + sw128_off(dim0 + q, r)) = __float2bfloat16_rn(v[u][q] * rs[u]);
-      }
-    }
-  }
-}
-
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnArgs a,
-                   AttnTcCfg t) {
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, AttnArgs a, AttnTcCfg t) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Geo& g = a.g;
   uint8_t* sQ = smem;                                   // datoms x 16 KB
   uint8_t* sP = sQ + t.datoms * kQAtomBytes;            // 16 KB
-  uint8_t* sB = sP + kQAtomBytes;                       // block "page": K then V^T (stage_bytes)
-  uint8_t* sKV = sB + t.stage_bytes;                    // stages x stage_bytes
+  uint8_t* sKV = sP + kQAtomBytes;                      // stages x stage_bytes
   uint8_t* ctl = sKV + t.stages * t.stage_bytes;
   uint64_t* kvfull = reinterpret_cast<uint64_t*>(ctl);
   uint64_t* kvempty = kvfull + t.stages;
   uint64_t* sfull = kvempty + t.stages;                 // [2]
   uint64_t* qfull = sfull + 2;
-  uint64_t* bfull = qfull + 1;
-  uint64_t* pfull = bfull + 1;
+  uint64_t* pfull = qfull + 1;
   uint64_t* pvdone = pfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pvdone + 1);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);   // abort
-  uint8_t* sBV = sB + t.datoms * kKAtomBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned long long c0 = 0;
@@ -173,14 +67,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     c0 = c0_shared;
   }
   const int R = g.G * kBlock;
-  // zero the query tile's padding rows and the whole block page (its unused
-  // key rows / columns must read as zeros)
+  // zero the query tile's padding rows (the MMA reads all 128 rows)
   for (int idx = threadIdx.x; idx < t.datoms * (128 - R) * 32; idx += kAttnThreads) {
     const int atom = idx / ((128 - R) * 32), rem = idx % ((128 - R) * 32);
     reinterpret_cast<uint32_t*>(sQ + atom * kQAtomBytes + R * 128)[rem] = 0u;
   }
-  for (int idx = threadIdx.x; idx < t.stage_bytes / 16; idx += kAttnThreads)
-    reinterpret_cast<uint4*>(sB)[idx] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   if (threadIdx.x == 0) {
     for (int s = 0; s < t.stages; ++s) {
       mbar_init(&kvfull[s], 1);
@@ -188,12 +80,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     mbar_init(&sfull[0], 1);
     mbar_init(&sfull[1], 1);
-    mbar_init(qfull, kEpiThreads);
-    mbar_init(bfull, kEpiThreads);
+    mbar_init(qfull, 1);
     mbar_init(pfull, kEpiThreads);
     mbar_init(pvdone, 1);
     flags[0] = 0;
     fence_barrier_init();
+    tma_prefetch_map(&tmQ);
     tma_prefetch_map(&tmK);
     tma_prefetch_map(&tmV);
   }
@@ -203,32 +95,30 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  pdl_launch_dependents();
-  pdl_wait();
-  if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 1, c0);  // 1: set-up and launch wait done
+  if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 1, c0);  // 1: set-up done
 
+  // The descriptor, the page table and the cached-context pages were written
+  // by kernels that completed before the predecessor passed its own launch
+  // wait (which is when this kernel may start), so they are read before this
+  // kernel's wait; only the pages holding this round's block rows and the
+  // query tile (both written by the predecessor) wait for it.
   const int item = blockIdx.x;
   int s, kvh, k0, k1;
-  bool last;
-  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &last);
-  const int n_pages = (k1 - k0 + kPage - 1) / kPage;     // cached-key pages
-  const int n_all = n_pages + (last ? 1 : 0);            // plus the block page
+  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1);
+  const int n_pages = (k1 - k0 + kPage - 1) / kPage;
+  const int n_all = n_pages;
   const int slot = a.rd->seq_slot[s];
+  const int len = a.rd->len[s];
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
-      for (int j = 0; j < n_pages; ++j) {
+      auto load_page = [&](int j) -> bool {
         const int st = j % t.stages;
-        if (j >= t.stages && !mbar_wait(&kvempty[st], ((j / t.stages) & 1) ^ 1, &flags[0])) {
-          flags[0] = 1;
-          break;
-        }
         const int page = a.block_table[(long)slot * g.pages_per_seq + k0 / kPage + j];
         if (page < 0 || page >= g.max_pages) {
           atomicExch(a.err, DERR_BAD_PAGE);
-          flags[0] = 1;
-          break;
+          return false;
         }
         const long base = ((long)a.layer * g.max_pages + page) * g.Hkv + kvh;
         uint8_t* st_k = sKV + st * t.stage_bytes;
@@ -237,7 +127,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int at = 0; at < t.datoms; ++at)
           tma_load_2d(st_k + at * kKAtomBytes, &tmK, &kvfull[st], at * 64, (int)(base * kPage));
         tma_load_2d(st_v, &tmV, &kvfull[st], 0, (int)(base * g.d));
+        return true;
+      };
+      bool ok = true;
+      int j = 0;
+      // context-only pages that fit the ring, before the launch wait
+      for (; ok && j < n_pages && j < t.stages && k0 + (j + 1) * kPage <= len; ++j) ok = load_page(j);
+      pdl_wait();
+      pdl_launch_dependents();
+      mbar_arrive_expect_tx(qfull, (uint32_t)(t.datoms * R * 128));
+      for (int at = 0; at < t.datoms; ++at)
+        tma_load_3d(sQ + at * kQAtomBytes, &tmQ, qfull, at * 64, kvh * g.G, s * kBlock);
+      for (; ok && j < n_pages; ++j) {
+        const int st = j % t.stages;
+        if (j >= t.stages && !mbar_wait(&kvempty[st], ((j / t.stages) & 1) ^ 1, &flags[0])) {
+          ok = false;
+          break;
+        }
+        ok = load_page(j);
       }
+      if (!ok) flags[0] = 1;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -246,15 +155,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       trace_mark(a.trace, blockIdx.x, 2, c0);                   // 2: query tile ready
       const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
-      auto kv_addr = [&](int j) -> uint32_t {
-        return j < n_pages ? smem_u32(sKV + (j % t.stages) * t.stage_bytes) : smem_u32(sB);
-      };
+      auto kv_addr = [&](int j) -> uint32_t { return smem_u32(sKV + (j % t.stages) * t.stage_bytes); };
       auto issue_s = [&](int j) -> bool {
-        if (j < n_pages) {
-          if (!mbar_wait(&kvfull[j % t.stages], (j / t.stages) & 1, &flags[0])) return false;
-        } else {
-          if (!mbar_wait(bfull, 0, &flags[0])) return false;
-        }
+        if (!mbar_wait(&kvfull[j % t.stages], (j / t.stages) & 1, &flags[0])) return false;
         tc_fence_after();
         const uint32_t k_addr = kv_addr(j);
         const uint32_t d_s = tmem + 128u + (uint32_t)((j & 1) * 64);
@@ -282,24 +185,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
           mma_bf16(tmem, desc_sw128(p_addr) + adv, desc_sw128(v_addr) + adv, t.idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(pvdone);
-        if (j < n_pages) mma_commit(&kvempty[j % t.stages]);
+        mma_commit(&kvempty[j % t.stages]);
         if (j + 2 < n_all) ok = issue_s(j + 2);
       }
       if (!ok) flags[0] = 1;
       trace_mark(a.trace, blockIdx.x, 3, c0);                   // 3: last MMA issued
     }
   } else {
-    // ------------------------------------------------------------------ tile builders, then softmax
-    if (g.d == 128) build_tiles<4>(a, s, kvh, false, sQ, sB, sBV);
-    else build_tiles<2>(a, s, kvh, false, sQ, sB, sBV);
-    fence_proxy_async_smem();
-    mbar_arrive(qfull);
-    if (last) {
-      if (g.d == 128) build_tiles<4>(a, s, kvh, true, sQ, sB, sBV);
-      else build_tiles<2>(a, s, kvh, true, sQ, sB, sBV);
-      fence_proxy_async_smem();
-      mbar_arrive(bfull);
-    }
+    // ------------------------------------------------------------------ softmax warps
+    pdl_wait();
     const int q = warp & 3;
     const int r = 32 * q + lane;                 // query row of this thread
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
@@ -315,7 +209,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float sc[kPage];
       tmem_ld32(tmem + lane_base + 128u + (uint32_t)((j & 1) * 64), sc);
       tmem_ld32(tmem + lane_base + 128u + (uint32_t)((j & 1) * 64) + 32u, sc + 32);
-      const int kc = j < n_pages ? min(kPage, k1 - (k0 + j * kPage)) : kBlock;
+      const int kc = min(kPage, k1 - (k0 + j * kPage));
       float mj = -INFINITY;
 #pragma unroll
       for (int i = 0; i < kPage; ++i) {
@@ -399,10 +293,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 size_t attn_tc_smem_bytes(int d, int stages) {
   const int datoms = d / 64;
   const int stage_bytes = datoms * kKAtomBytes + d * 128;
-  return (size_t)datoms * kQAtomBytes + kQAtomBytes + (size_t)(stages + 1) * stage_bytes + 256 + 1024;
+  return (size_t)datoms * kQAtomBytes + kQAtomBytes + (size_t)stages * stage_bytes + 256 + 1024;
 }
 
-void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmk, const void* tmv, cudaStream_t s) {
+void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
+                         cudaStream_t s) {
   AttnTcCfg t{};
   const int d = a.g.d;
   t.datoms = d / 64;
@@ -418,8 +313,8 @@ void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmk, const 
       return;
     attr_bytes = smem;
   }
-  launch_pdl(attn_tc_kernel, dim3(n_items), dim3(kAttnThreads), smem, s, *static_cast<const CUtensorMap*>(tmk),
-             *static_cast<const CUtensorMap*>(tmv), a, t);
+  launch_pdl(attn_tc_kernel, dim3(n_items), dim3(kAttnThreads), smem, s, *static_cast<const CUtensorMap*>(tmq),
+             *static_cast<const CUtensorMap*>(tmk), *static_cast<const CUtensorMap*>(tmv), a, t);
 }
 
 }  // namespace dfl

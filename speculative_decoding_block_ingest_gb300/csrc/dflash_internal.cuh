@@ -76,6 +76,7 @@ struct RoundDesc {
   int len[kMaxBatch];
   int item0[kMaxBatch + 1];        // attention work items of seq s: [item0[s], item0[s+1])
   int pos[kMaxBatch * kBlock];     // absolute position of each block row
+  int dest[kMaxBatch * kBlock];    // page*64 + offset of the row's transient K/V
 };
 
 // Per-call descriptor of an ingest (rows in call order).
@@ -194,71 +195,20 @@ __device__ __forceinline__ void rope_sincos(int pos, const double* inv_freq, int
   sincosf((float)th, s, c);
 }
 
-// Locate attention work item `item`: sequence s, kv head, its range of
-// cached context keys [k0, k1), and whether it is the sequence's last split
-// (which also attends the 16 block rows).
+// Locate attention work item `item`: sequence s, kv head, and its key range
+// [k0, k1) within [cached context ; 16 block rows].
 __device__ __forceinline__ void attn_item(const RoundDesc* rd, int Hkv, int item, int* s_out, int* g_out,
-                                          int* k0, int* k1, bool* last) {
+                                          int* k0, int* k1) {
   int s = 0;
   while (s + 1 < rd->n_seq && rd->item0[s + 1] <= item) ++s;
   const int local = item - rd->item0[s];
   const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / Hkv;
   const int g = local / nsplit, sp = local % nsplit;
-  const int len = rd->len[s];
+  const int n_keys = rd->len[s] + kBlock;
   *s_out = s;
   *g_out = g;
-  *k0 = min(len, sp * rd->split_pages * kPage);
-  *k1 = min(len, (sp + 1) * rd->split_pages * kPage);
-  *last = sp == nsplit - 1;
-}
-
-// One head row for the attention, read from the QKV accumulator (token-major
-// [tok][(Hq+2Hkv)*d], pre-norm and unscaled): x = acc[tok][col0 .. col0+d) *
-// rs; for q and k (norm_rope) a head RMSNorm with `gain` and the NeoX
-// rotation by (cos, sin) of the token's position (mscale folded in).  Called
-// by a whole warp; lane l returns dims l*PER .. l*PER+PER-1 (lanes 0..15 the
-// first half, so the partner of dim j is dim j + d/2 in lane l + 16).
-template <int PER>
-__device__ __forceinline__ void qkv_head_row(const float* __restrict__ acc, int ld, int tok, int col0, float rs,
-                                             const float* __restrict__ gain, const float2* __restrict__ cs_row,
-                                             bool norm_rope, float eps, float* x) {
-  constexpr int d = 32 * PER, half = d / 2;
-  const int lane = threadIdx.x & 31;
-  const int dim0 = lane * PER;
-  const float* src = acc + (long)tok * ld + col0 + dim0;
-  if (PER == 4) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-  } else {
-    const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-    x[0] = v.x; x[1] = v.y;
-  }
-  if (!norm_rope) {
-#pragma unroll
-    for (int q = 0; q < PER; ++q) x[q] *= rs;
-    return;
-  }
-  float gn[PER];
-  float2 cs[PER];
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    gn[q] = gain[dim0 + q];
-    cs[q] = cs_row[(dim0 + q) % half];
-  }
-  float ss = 0.f;
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    x[q] *= rs;
-    ss += x[q] * x[q];
-  }
-  ss = warp_sum(ss);
-  const float r = rsqrtf(ss / (float)d + eps);
-#pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    const float y = x[q] * r * gn[q];
-    const float partner = __shfl_xor_sync(0xffffffffu, y, 16);
-    x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
-  }
+  *k0 = sp * rd->split_pages * kPage;
+  *k1 = min(n_keys, (sp + 1) * rd->split_pages * kPage);
 }
 
 // ------------------------------------------------------------------ stream-K reduction

@@ -1,0 +1,151 @@
+// finish.cu -- the small element-wise steps between the round's projections.
+//
+// They run as short, wide kernels between the weight-streaming ones (chained
+// by programmatic dependent launch) so that no latency-bound step sits inside
+// a kernel that streams HBM at full rate:
+//   prep_norm    RMSNorm operand of the next projection: per token row,
+//                x = h * gain * rsqrt(mean(h^2) + eps) as hi/lo bf16 planes
+//                (or f32 for f32 drafters);
+//   qk_finish    per (token, head) row of the QKV accumulator: q and k head
+//                RMSNorm + NeoX RoPE (mscale folded into the table); q to the
+//                attention's query buffer, the block rows' K and V into the
+//                KV pages (rows len .. len+15, transient); the row is cleared;
+//   swiglu       act = silu(g) * u from the gate/up accumulator as hi/lo
+//                planes; the entries are cleared.
+#include <algorithm>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace dfl {
+
+__global__ void __launch_bounds__(128) prep_norm_kernel(FinishArgs f) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tok = blockIdx.x, tid = threadIdx.x;
+  const Geo& g = f.g;
+  const float* row = f.h + (long)tok * g.H;
+  __shared__ float red[4];
+  float ss = 0.f;
+  for (int c = tid * 4; c < g.H; c += 512) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  const float r = rsqrtf((red[0] + red[1] + red[2] + red[3]) / (float)g.H + g.eps);
+  for (int c = tid * 4; c < g.H; c += 512) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
+    const float4 w = __ldg(reinterpret_cast<const float4*>(f.gain + c));
+    const long idx = (long)tok * g.H + c;
+    put_operand(f.op, idx + 0, f.op_plane, v.x * w.x * r, f.op_f32);
+    put_operand(f.op, idx + 1, f.op_plane, v.y * w.y * r, f.op_f32);
+    put_operand(f.op, idx + 2, f.op_plane, v.z * w.z * r, f.op_f32);
+    put_operand(f.op, idx + 3, f.op_plane, v.w * w.w * r, f.op_f32);
+  }
+}
+
+// One warp per (token, head) row of the QKV accumulator.
+template <int PER>
+__device__ void qk_finish_row(const FinishArgs& f, int tok, int hh) {
+  const Geo& g = f.g;
+  constexpr int d = 32 * PER, half = d / 2;
+  const int lane = threadIdx.x & 31, dim0 = lane * PER;
+  const int kind = hh < g.Hq ? 0 : (hh < g.Hq + g.Hkv ? 1 : 2);
+  const int head = kind == 0 ? hh : (kind == 1 ? hh - g.Hq : hh - g.Hq - g.Hkv);
+  float* src = f.acc + (long)tok * g.qkv_n + hh * d + dim0;
+  float x[PER], gn[PER];
+  float2 cs[PER];
+  if (PER == 4) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  } else {
+    const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+    x[0] = v.x; x[1] = v.y;
+  }
+  const float* gsrc = kind == 0 ? f.qn : f.kn;
+#pragma unroll
+  for (int q = 0; q < PER; ++q) {
+    gn[q] = kind != 2 ? gsrc[dim0 + q] : 1.f;
+    cs[q] = kind != 2 ? f.rope_cs[(long)tok * half + (dim0 + q) % half] : make_float2(1.f, 0.f);
+  }
+  const int dst = kind != 0 ? f.dest[tok] : 0;
+  // clear the accumulator row for the next layer
+  if (PER == 4) *reinterpret_cast<float4*>(src) = make_float4(0.f, 0.f, 0.f, 0.f);
+  else *reinterpret_cast<float2*>(src) = make_float2(0.f, 0.f);
+  if (kind != 2) {
+    float ss = 0.f;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) ss += x[q] * x[q];
+    ss = warp_sum(ss);
+    const float rn = rsqrtf(ss / (float)d + g.eps);
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const float y = x[q] * rn * gn[q];
+      const float partner = __shfl_xor_sync(0xffffffffu, y, 16);   // dims j <-> j + d/2
+      x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
+    }
+  }
+  if (kind == 0) {
+    const long base = ((long)tok * g.Hq + head) * d + dim0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) put_kv(f.q_out, base + q, x[q], g.kvtype);
+  } else {
+    const int page = dst >> 6, off = dst & (kPage - 1);
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      if (kind == 1) put_kv(f.kpool, k_index(g, f.layer, page, head, off, dim0 + q), x[q], g.kvtype);
+      else put_kv(f.vpool, v_index(g, f.layer, page, head, off, dim0 + q), x[q], g.kvtype);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(128) qk_finish_kernel(FinishArgs f) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const Geo& g = f.g;
+  const int heads = g.Hq + 2 * g.Hkv;
+  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (row >= f.n_tok * heads) return;
+  const int tok = row / heads, hh = row % heads;
+  if (g.d == 128) qk_finish_row<4>(f, tok, hh);
+  else qk_finish_row<2>(f, tok, hh);
+}
+
+__global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const Geo& g = f.g;
+  const long n4 = (long)f.n_tok * g.I / 4;
+  for (long k = (long)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (long)gridDim.x * blockDim.x) {
+    const long e = k * 4;
+    const int tok = (int)(e / g.I), j = (int)(e % g.I);
+    float* gp = f.acc + (long)tok * 2 * g.I + (j / 64) * 128 + (j % 64);
+    const float4 gv = __ldcg(reinterpret_cast<const float4*>(gp));
+    const float4 uv = __ldcg(reinterpret_cast<const float4*>(gp + 64));
+    *reinterpret_cast<float4*>(gp) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(gp + 64) = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float gg[4] = {gv.x, gv.y, gv.z, gv.w}, uu[4] = {uv.x, uv.y, uv.z, uv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      put_operand(f.op, (long)tok * g.I + j + q, f.op_plane, gg[q] / (1.f + __expf(-gg[q])) * uu[q], f.op_f32);
+  }
+}
+
+void launch_prep_norm(const FinishArgs& f, cudaStream_t s) {
+  launch_pdl(prep_norm_kernel, dim3(f.n_tok), dim3(128), 0, s, f);
+}
+
+void launch_qk_finish(const FinishArgs& f, cudaStream_t s) {
+  const int rows = f.n_tok * (f.g.Hq + 2 * f.g.Hkv);
+  launch_pdl(qk_finish_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, f);
+}
+
+void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s) {
+  const long n4 = (long)f.n_tok * f.g.I / 4;
+  const int grid = (int)std::min<long>((n4 + 127) / 128, 4L * n_sm);
+  launch_pdl(swiglu_kernel, dim3(grid), dim3(128), 0, s, f);
+}
+
+}  // namespace dfl

@@ -6,13 +6,6 @@
 
 namespace dfl {
 
-// Where a projection's operand X[tok][K] comes from.
-enum XMode {
-  X_PLANES = 0,   // a prepared buffer: bf16 hi/lo planes (TMA), or f32 for f32 drafters
-  X_FROM_H = 1,   // the residual stream h [tok][K] f32 times a norm gain (pre-norm; the
-                  //   row scale is applied by whoever consumes the result)
-  X_SWIGLU = 2    // silu(g r) * (u r) from the gate/up accumulator [tok][2I] and row scale r
-};
 // Where a projection's result goes.
 enum OMode {
   O_TILE = 0,     // stream-K ticket; the last arriver runs the tile epilogue EpiArgs::kind
@@ -24,24 +17,13 @@ enum OMode {
 struct GemmArgs {
   const void* W;      // [N][K] in Geo::wtype
   int N, K;
-  int xmode;
-  const void* X;      // X_PLANES: [tok][K] f32, or bf16 hi plane (+ lo plane at x_plane)
+  const void* X;      // operand [tok][K]: f32, or bf16 hi plane (+ lo plane at x_plane)
   int x_ld;
   long x_plane;
   int x_f32;
-  const float* xsrc;  // X_FROM_H: h; X_SWIGLU: gate/up accumulator (token-major)
-  int xsrc_ld;
-  const float* xgain; // X_FROM_H: gain [K]
-  const float* xrs;   // X_SWIGLU: per token row scale
   int omode;
   float* dst;         // O_RED: destination [tok][dst_ld]
   int dst_ld;
-  // side duties spread over the CTAs (each may be null)
-  const float* rs_src;  // rows whose RMS scale rsqrt(mean(x^2)+eps) goes to rs_out[tok]
-  int rs_ld, rs_len;
-  float* rs_out;
-  float* zero_ptr;      // float4-aligned region cleared for a later call
-  long zero_n;          // floats, a multiple of 4
   Part p;
   int n_tiles;
   float* acc;         // O_TILE accumulators [n_tiles][128][nt], zero between calls
@@ -50,13 +32,29 @@ struct GemmArgs {
   EpiArgs e;
 };
 
+// The small element-wise steps between the round's projections.
+struct FinishArgs {
+  int n_tok;
+  int layer;
+  const float* h;         // prep_norm: residual stream [Mt][H]
+  const float* gain;      // prep_norm: RMSNorm gain [H]
+  float* acc;             // qk_finish: QKV accumulator [Mt][qkv_n]; swiglu: gate/up [Mt][2I]
+  void* op;               // prep_norm / swiglu: operand planes
+  long op_plane;
+  int op_f32;
+  const float* qn;        // qk_finish: head-norm gains of this layer
+  const float* kn;
+  const float2* rope_cs;  // per token [d/2] (cos, sin) x mscale
+  const int* dest;        // per token page*64 + offset of its (transient) K/V row
+  void* q_out;            // [Mt][Hq][d]
+  void* kpool;
+  void* vpool;
+  Geo g;
+};
+
 // Attention over the paged cache: per (seq, kv head, split) work item.
 struct AttnArgs {
-  const float* qkv;     // QKV accumulator [Mt][(Hq+2Hkv)*d] f32 (pre-norm, unscaled)
-  const float* r_in;    // per token input-norm scale
-  const float* qn;      // q head-norm gain of this layer [d]
-  const float* kn;      // k head-norm gain of this layer [d]
-  const float2* rope_cs;  // per token [d/2] (cos, sin) x mscale
+  const void* q;        // [Mt][Hq][d]  (kv dtype): normed, roped queries
   const void* kpool;    // K pool base
   const void* vpool;    // V^T pool base
   int layer;
@@ -115,11 +113,14 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 void launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 void launch_gemm_tc(const GemmArgs& a, const void* tmap_w, const void* tmap_x, cudaStream_t s);
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s);
-void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmk, const void* tmv, cudaStream_t s);
+void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
+                         cudaStream_t s);
+void launch_prep_norm(const FinishArgs& f, cudaStream_t s);
+void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
+void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s);
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s);
-void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, float* zero_ptr, long zero_n,
-                       const Geo& g, cudaStream_t s);
+void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s);
 void launch_kv_read(const Geo& g, const void* kpool, const void* vpool, const int* block_table,
                     int slot, int layer, int row0, int nrows, float* k_out, float* v_out,
                     cudaStream_t s);

@@ -22,37 +22,10 @@ __device__ __forceinline__ float load_w(const void* W, long idx, int wtype) {
 }
 
 __device__ __forceinline__ float load_x(const GemmArgs& a, int tok, int k) {
-  if (a.xmode == X_FROM_H) return a.xsrc[(long)tok * a.xsrc_ld + k] * a.xgain[k];
-  if (a.xmode == X_SWIGLU) {
-    const long base = (long)tok * a.xsrc_ld + (k / 64) * 128 + (k % 64);
-    const float rs = a.xrs[tok];
-    const float gs = a.xsrc[base] * rs, us = a.xsrc[base + 64] * rs;
-    return gs / (1.f + __expf(-gs)) * us;
-  }
   const long idx = (long)tok * a.x_ld + k;
   if (a.x_f32) return reinterpret_cast<const float*>(a.X)[idx];
   const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(a.X);
   return __bfloat162float(x[idx]) + __bfloat162float(x[idx + a.x_plane]);
-}
-
-// Side duties of a projection launch, spread over its CTAs: per-token RMS
-// scales of rs_src rows, and clearing a region for a later call.
-__device__ void gemm_duties(const GemmArgs& a, int cta, int grid, int tid, int nthreads) {
-  if (a.rs_out && tid < 32) {
-    for (int tok = cta; tok < a.e.n_tok; tok += grid) {
-      const float* src = a.rs_src + (long)(a.e.tok_base + tok) * a.rs_ld;
-      float ss = 0.f;
-      for (int k = tid; k < a.rs_len; k += 32) ss += src[k] * src[k];
-      ss = warp_sum(ss);
-      if (tid == 0) a.rs_out[a.e.tok_base + tok] = rsqrtf(ss / (float)a.rs_len + a.e.g.eps);
-    }
-  }
-  if (a.zero_ptr) {
-    const long n4 = a.zero_n / 4;
-    const long lo = n4 * cta / grid, hi = n4 * (cta + 1) / grid;
-    for (long k = lo + tid; k < hi; k += nthreads)
-      reinterpret_cast<float4*>(a.zero_ptr)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
 }
 
 constexpr int kSimtTok = 16;
@@ -69,7 +42,6 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(GemmArgs a) {
   const Part p = a.p;
   const int u1 = p.start(c + 1);
   const int nt = (a.e.n_tok + 15) / 16 * 16;
-  gemm_duties(a, c, p.grid, tid, 128);
   for (int u = p.start(c); u < u1;) {
     const int T = u / p.kb;
     const int seg_end = min(u1, (T + 1) * p.kb);
@@ -138,105 +110,72 @@ __device__ __forceinline__ float load_kv(const void* base, long idx, int kvtype)
   return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[idx]);
 }
 
-// Write lane's PER dims of a head row into an f32 shared row.
-template <int PER>
-__device__ __forceinline__ void put_row_f32(float* row, const float* x) {
-  const int dim0 = (threadIdx.x & 31) * PER;
-#pragma unroll
-  for (int q = 0; q < PER; ++q) row[dim0 + q] = x[q];
-}
-
-template <int PER>
-__device__ void attn_simt_body(const AttnArgs& a, float* sm) {
+__global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
+  extern __shared__ float sm[];
+  pdl_wait();
+  pdl_launch_dependents();
   const Geo& g = a.g;
-  constexpr int d = 32 * PER;
-  const int R = g.G * kBlock, dp = d + 1;
+  const int d = g.d, R = g.G * kBlock, dp = d + 1;
   float* Qs = sm;                 // [R][d+1]
   float* Os = Qs + R * dp;        // [R][d+1]
   float* Ks = Os + R * dp;        // [64][d+1]
   float* Vs = Ks + kPage * dp;    // [d][65]
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x;
   const int item = blockIdx.x;
   int s, kvh, k0, k1;
-  bool last;
-  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &last);
+  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1);
   const int slot = a.rd->seq_slot[s];
-  const int n_pages = (k1 - k0 + kPage - 1) / kPage;
-  const int n_all = n_pages + (last ? 1 : 0);
-  // query rows r = token * G + local head: input-norm scale, head norm, RoPE
-  for (int r = warp; r < R; r += 4) {
-    const int i = r / g.G, hl = r % g.G, tok = s * kBlock + i;
-    float x[PER];
-    qkv_head_row<PER>(a.qkv, g.qkv_n, tok, (kvh * g.G + hl) * d, a.r_in[tok], a.qn, a.rope_cs + (long)tok * (d / 2),
-                      true, g.eps, x);
-    put_row_f32<PER>(Qs + r * dp, x);
+  for (int idx = tid; idx < R * d; idx += 128) {
+    const int r = idx / d, dim = idx % d;
+    const int i = r / g.G, hl = r % g.G;      // row = token * G + local head
+    const long qi = ((long)(s * kBlock + i) * g.Hq + kvh * g.G + hl) * d + dim;
+    Qs[r * dp + dim] = load_kv(a.q, qi, g.kvtype);
+    Os[r * dp + dim] = 0.f;
   }
-  for (int idx = tid; idx < R * d; idx += 128) Os[(idx / d) * dp + idx % d] = 0.f;
   float m = -INFINITY, l = 0.f;
   const bool active = tid < R;
-  for (int j = 0; j < n_all; ++j) {
+  for (int kp = k0; kp < k1; kp += kPage) {
+    const int pidx = kp / kPage;
+    const int page = a.block_table[(long)slot * g.pages_per_seq + pidx];
+    const int kc = min(kPage, k1 - kp);
     __syncthreads();
-    int kc;
-    if (j < n_pages) {
-      const int kp = k0 + j * kPage;
-      const int page = a.block_table[(long)slot * g.pages_per_seq + kp / kPage];
-      kc = min(kPage, k1 - kp);
-      if (page < 0 || page >= g.max_pages) {
-        if (tid == 0) atomicExch(a.err, DERR_BAD_PAGE);
-        break;
-      }
-      for (int idx = tid; idx < kPage * d; idx += 128) {
-        const int jj = idx / d, dim = idx % d;
-        Ks[jj * dp + dim] = jj < kc ? load_kv(a.kpool, k_index(g, a.layer, page, kvh, jj, dim), g.kvtype) : 0.f;
-        const int dv = idx / kPage, jv = idx % kPage;
-        Vs[dv * (kPage + 1) + jv] = jv < kc ? load_kv(a.vpool, v_index(g, a.layer, page, kvh, jv, dv), g.kvtype) : 0.f;
-      }
-    } else {
-      // the block rows' own K (normed, roped) and V, straight from the QKV
-      // accumulator; the unused key slots must hold zeros (0 x stale NaN = NaN)
-      kc = kBlock;
-      for (int idx = tid; idx < kPage * dp; idx += 128) Ks[idx] = 0.f;
-      for (int idx = tid; idx < d * (kPage + 1); idx += 128) Vs[idx] = 0.f;
-      __syncthreads();
-      for (int i = warp; i < kBlock; i += 4) {
-        const int tok = s * kBlock + i;
-        float x[PER];
-        qkv_head_row<PER>(a.qkv, g.qkv_n, tok, (g.Hq + kvh) * d, a.r_in[tok], a.kn, a.rope_cs + (long)tok * (d / 2),
-                          true, g.eps, x);
-        put_row_f32<PER>(Ks + i * dp, x);
-        qkv_head_row<PER>(a.qkv, g.qkv_n, tok, (g.Hq + g.Hkv + kvh) * d, a.r_in[tok], nullptr, nullptr, false, g.eps,
-                          x);
-#pragma unroll
-        for (int q = 0; q < PER; ++q) Vs[((tid & 31) * PER + q) * (kPage + 1) + i] = x[q];
-      }
+    if (page < 0 || page >= g.max_pages) {
+      if (tid == 0) atomicExch(a.err, DERR_BAD_PAGE);
+      break;
+    }
+    for (int idx = tid; idx < kPage * d; idx += 128) {
+      const int j = idx / d, dim = idx % d;
+      Ks[j * dp + dim] = j < kc ? load_kv(a.kpool, k_index(g, a.layer, page, kvh, j, dim), g.kvtype) : 0.f;
+      const int dv = idx / kPage, jv = idx % kPage;
+      Vs[dv * (kPage + 1) + jv] = jv < kc ? load_kv(a.vpool, v_index(g, a.layer, page, kvh, jv, dv), g.kvtype) : 0.f;
     }
     __syncthreads();
     if (active) {
       float sc[kPage];
       float mx = m;
 #pragma unroll
-      for (int jj = 0; jj < kPage; ++jj) {
+      for (int j = 0; j < kPage; ++j) {
         float acc = 0.f;
-        if (jj < kc) {
-          for (int dim = 0; dim < d; ++dim) acc = fmaf(Qs[tid * dp + dim], Ks[jj * dp + dim], acc);
+        if (j < kc) {
+          for (int dim = 0; dim < d; ++dim) acc = fmaf(Qs[tid * dp + dim], Ks[j * dp + dim], acc);
           acc *= a.scale_log2;
           mx = fmaxf(mx, acc);
         }
-        sc[jj] = acc;
+        sc[j] = acc;
       }
       const float alpha = exp2f(m - mx);
       float lsum = 0.f;
 #pragma unroll
-      for (int jj = 0; jj < kPage; ++jj) {
-        sc[jj] = jj < kc ? exp2f(sc[jj] - mx) : 0.f;
-        lsum += sc[jj];
+      for (int j = 0; j < kPage; ++j) {
+        sc[j] = j < kc ? exp2f(sc[j] - mx) : 0.f;
+        lsum += sc[j];
       }
       l = l * alpha + lsum;
       m = mx;
       for (int dim = 0; dim < d; ++dim) {
         float acc = Os[tid * dp + dim] * alpha;
 #pragma unroll
-        for (int jj = 0; jj < kPage; ++jj) acc = fmaf(sc[jj], Vs[dim * (kPage + 1) + jj], acc);
+        for (int j = 0; j < kPage; ++j) acc = fmaf(sc[j], Vs[dim * (kPage + 1) + j], acc);
         Os[tid * dp + dim] = acc;
       }
     }
@@ -251,14 +190,6 @@ __device__ void attn_simt_body(const AttnArgs& a, float* sm) {
     a.part_ml[(ob + tid) * 2 + 0] = m;
     a.part_ml[(ob + tid) * 2 + 1] = l;
   }
-}
-
-__global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
-  extern __shared__ float sm[];
-  pdl_wait();
-  pdl_launch_dependents();
-  if (a.g.d == 128) attn_simt_body<4>(a, sm);
-  else attn_simt_body<2>(a, sm);
 }
 
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s) {
@@ -334,7 +265,7 @@ void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s) {
 }
 
 __global__ void __launch_bounds__(128) final_norm_kernel(const float* h, const float* gain, float* out, int H,
-                                                         float eps, float* zero_ptr, long zero_n) {
+                                                         float eps) {
   pdl_wait();
   pdl_launch_dependents();
   const int tok = blockIdx.x, tid = threadIdx.x;
@@ -349,17 +280,10 @@ __global__ void __launch_bounds__(128) final_norm_kernel(const float* h, const f
   __syncthreads();
   const float r = rsqrtf((red[0] + red[1] + red[2] + red[3]) / (float)H + eps);
   for (int c = tid; c < H; c += blockDim.x) out[(long)tok * H + c] = h[(long)tok * H + c] * gain[c] * r;
-  if (zero_ptr) {
-    const long n4 = zero_n / 4;
-    const long lo = n4 * tok / gridDim.x, hi = n4 * (tok + 1) / gridDim.x;
-    for (long k = lo + tid; k < hi; k += blockDim.x)
-      reinterpret_cast<float4*>(zero_ptr)[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
 }
 
-void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, float* zero_ptr, long zero_n,
-                       const Geo& g, cudaStream_t s) {
-  launch_pdl(final_norm_kernel, dim3(n_tok), dim3(128), 0, s, h, gain, out, g.H, g.eps, zero_ptr, zero_n);
+void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s) {
+  launch_pdl(final_norm_kernel, dim3(n_tok), dim3(128), 0, s, h, gain, out, g.H, g.eps);
 }
 
 __global__ void kv_read_kernel(Geo g, const void* kpool, const void* vpool, const int* block_table,

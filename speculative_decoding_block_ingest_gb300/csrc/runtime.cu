@@ -58,7 +58,7 @@ struct Layout {
   size_t s_fc, s_qkv, s_o, s_gu, s_down, s_kvall;       // fp8 row scales
   size_t hn, fn, in_ln, post_ln, qn, kn;                // norm gains
   size_t kpool, vpool, btab, inv_freq;
-  size_t h, op_h, op_taps, op_o, qkv_acc, gu_acc, r_in, r_post, ss;
+  size_t h, op_h, op_taps, op_o, op_a, q, qkv_acc, gu_acc, ss;
   size_t gacc, rope_cs, counters, apart_o, apart_ml, rdesc, idesc, err;
   size_t total;
   int Mt, pps, max_tiles, grid_max, items_cap, n_sites;
@@ -118,10 +118,10 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.op_h = take(Mt * H * 4);
   Lo.op_taps = take(Mt * nH * 4);
   Lo.op_o = take(Mt * Hq * d * 4);
+  Lo.op_a = take(Mt * I * 4);
+  Lo.q = take(Mt * Hq * d * 4);
   Lo.qkv_acc = take(Mt * qkv_n * 4);
   Lo.gu_acc = take(Mt * 2 * I * 4);
-  Lo.r_in = take(Mt * 4);
-  Lo.r_post = take(Mt * 4);
   Lo.ss = take((2 * L + 2) * Mt * 4);   // [2L+1]: ingest feature sums of squares
   Lo.gacc = take((size_t)Lo.max_tiles * kTileN * kPassTok * 4);
   Lo.rope_cs = take(Mt * d / 2 * 8);
@@ -220,6 +220,20 @@ CUtensorMap make_map_bf16(const void* base, uint64_t rows, uint64_t cols, uint32
   return m;
 }
 
+// 3-D bf16 map over [d2][d1][d0] (d0 innermost), box {64, b1, b2}, 128-byte swizzle.
+CUtensorMap make_map_bf16_3d(const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, uint32_t b2) {
+  CUtensorMap m;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  cuuint32_t box[3] = {64, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = tensor_map_encoder()(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) throw CudaError{"cuTensorMapEncodeTiled (3-D) failed (" + std::to_string((int)r) + ")"};
+  return m;
+}
+
 }  // namespace
 
 struct dflash_handle {
@@ -236,8 +250,8 @@ struct dflash_handle {
   int64_t launches = 0;
   // tensor maps of the tensor-core projections: weights per GEMM site, operands per buffer
   std::vector<CUtensorMap> wmap;
-  CUtensorMap xmap_taps, xmap_h, xmap_o;
-  CUtensorMap kmap, vmap;                       // attention: K pool, V^T pool
+  CUtensorMap xmap_taps, xmap_h, xmap_o, xmap_a;
+  CUtensorMap qmap, kmap, vmap;                 // attention: q buffer (3-D), K pool, V^T pool
   bool use_tc = false;
   bool prof_on = false;
   struct Rec {
@@ -341,28 +355,18 @@ EpiArgs base_epi(dflash_t* h) {
   return e;
 }
 
-// One projection call: where its operand comes from, where its result goes,
-// and its side duties.
+// One projection call: its operand, where its result goes, and (for the
+// ingest's projections) the tile epilogue.
 struct GemmSpec {
-  int site;                     // counter block of O_TILE calls
+  int site;                     // weight map and counter block
   const void* W;
   const float* wscale;
   int N, K;
-  int xmode = X_PLANES;
-  const void* X = nullptr;      // X_PLANES
+  const void* X = nullptr;      // operand planes (bf16 hi/lo, or f32)
   const CUtensorMap* xmap = nullptr;
-  const float* xsrc = nullptr;  // X_FROM_H / X_SWIGLU
-  int xsrc_ld = 0;
-  const float* xgain = nullptr;
-  const float* xrs = nullptr;
   int omode = O_TILE;
-  float* dst = nullptr;         // O_RED
+  float* dst = nullptr;         // O_RED destination [tok][dst_ld]
   int dst_ld = 0;
-  const float* rs_src = nullptr;
-  int rs_ld = 0, rs_len = 0;
-  float* rs_out = nullptr;
-  float* zero_ptr = nullptr;
-  long zero_n = 0;
   EpiArgs e;
 };
 
@@ -376,24 +380,13 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     a.W = sp.W;
     a.N = sp.N;
     a.K = sp.K;
-    a.xmode = sp.xmode;
     a.X = sp.X;
     a.x_ld = sp.K;
     a.x_plane = (long)h->lo.Mt * sp.K;
     a.x_f32 = h->cfg.weight_dtype == DFLASH_F32;
-    a.xsrc = sp.xsrc;
-    a.xsrc_ld = sp.xsrc_ld;
-    a.xgain = sp.xgain;
-    a.xrs = sp.xrs;
     a.omode = sp.omode;
     a.dst = sp.dst;
     a.dst_ld = sp.dst_ld;
-    a.rs_src = sp.rs_src;
-    a.rs_ld = sp.rs_ld;
-    a.rs_len = sp.rs_len;
-    a.rs_out = sp.rs_out;
-    a.zero_ptr = base == 0 ? sp.zero_ptr : nullptr;
-    a.zero_n = sp.zero_n;
     a.n_tiles = sp.N / kTileN;
     a.p.kb = sp.K / kTileK;
     a.p.units = a.n_tiles * a.p.kb;
@@ -406,7 +399,7 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     a.e.n_tok = std::min(kPassTok, n_all - base);
     const double nt = a.e.n_tok;
     // algorithmic bytes: weights (+ scales), the operand once, the result once
-    double x_b = nt * sp.K * (sp.xmode == X_SWIGLU ? 8 : 4);
+    double x_b = nt * sp.K * 4;
     double out_b;
     if (sp.omode == O_RED) out_b = nt * sp.N * 4;
     else if (sp.e.kind == EPI_RESID) out_b = nt * sp.N * 12;
@@ -495,30 +488,30 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
 
 int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens) {
   long units = 0;
-  for (auto L : lens) units += (long)h->g.Hkv * std::max<int64_t>(1, (L + kPage - 1) / kPage);
+  for (auto L : lens) units += (long)h->g.Hkv * ((L + kBlock + kPage - 1) / kPage);
   const long target = h->use_tc ? (long)h->n_sm : 2L * h->n_sm;
   return (int)std::max<long>(1, (units + target - 1) / target);
 }
 
-// The round: per layer QKV -> attention -> combine -> O -> gate/up -> down.
-// Projections add straight into token-major accumulators (QKV, gate/up) or
-// into the residual stream h (O, down); their consumers apply the norms and
-// SwiGLU while building their own operands, so no projection ends in a
-// serial epilogue.  Row scales rsqrt(mean(h^2)+eps) are computed by the
-// projection that reads h; spent accumulators are cleared by a later kernel.
+// The round: per layer
+//   prep_norm(input_ln) -> QKV -> qk_finish -> attention -> combine -> O ->
+//   prep_norm(post_ln) -> gate/up -> swiglu -> down.
+// The projections only stream weights: their operands are prepared planes
+// read by TMA, and their results are red.added into token-major
+// accumulators (QKV, gate/up) or into the residual stream h (O, down).  The
+// small element-wise steps run as wide kernels in between (finish.cu), all
+// chained by programmatic dependent launch.
 void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, cudaStream_t s) {
   const Geo& g = h->g;
   RoundDesc& rd = blob.round;
   const int n_tok = rd.n_tok;
   const size_t Mt = h->lo.Mt;
   const bool fp8 = h->cfg.weight_dtype == DFLASH_FP8_E4M3;
+  const bool f32 = h->cfg.weight_dtype == DFLASH_F32;
   const size_t ew = wbytes(h);
   float* hres = h->at<float>(h->lo.h);
   float* qkv_acc = h->at<float>(h->lo.qkv_acc);
   float* gu_acc = h->at<float>(h->lo.gu_acc);
-  float* r_in = h->at<float>(h->lo.r_in);
-  float* r_post = h->at<float>(h->lo.r_post);
-  const long qkv_acc_n = (long)n_tok * g.qkv_n, gu_acc_n = (long)n_tok * 2 * g.I;
 
   InitArgs ia{};
   ia.src = noise;
@@ -538,39 +531,58 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   }
   ck(cudaGetLastError(), "round init launch");
 
+  FinishArgs fb{};
+  fb.n_tok = n_tok;
+  fb.h = hres;
+  fb.op_f32 = f32;
+  fb.rope_cs = h->at<float2>(h->lo.rope_cs);
+  fb.dest = h->at<RoundDesc>(h->lo.rdesc)->dest;
+  fb.q_out = h->at<void>(h->lo.q);
+  fb.kpool = h->at<void>(h->lo.kpool);
+  fb.vpool = h->at<void>(h->lo.vpool);
+  fb.g = g;
+  auto prep_norm = [&](const float* gain) {
+    FinishArgs f = fb;
+    f.gain = gain;
+    f.op = h->at<void>(h->lo.op_h);
+    f.op_plane = (long)Mt * g.H;
+    Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * 8, s);
+    launch_prep_norm(f, s);
+  };
+
   for (int l = 0; l < g.L; ++l) {
-    // QKV of RMSNorm(h; input_ln) -> QKV accumulator; r_in from h; clears the
-    // previous layer's gate/up accumulator
+    prep_norm(h->at<float>(h->lo.in_ln) + (size_t)l * g.H);
+    ck(cudaGetLastError(), "input norm launch");
+
     GemmSpec q;
     q.site = 2 + 4 * l;
     q.W = h->at<char>(h->lo.qkv) + (size_t)l * g.qkv_n * g.H * ew;
     q.wscale = fp8 ? h->at<float>(h->lo.s_qkv) + (size_t)l * g.qkv_n : nullptr;
     q.N = g.qkv_n;
     q.K = g.H;
-    q.xmode = X_FROM_H;
-    q.xsrc = hres;
-    q.xsrc_ld = g.H;
-    q.xgain = h->at<float>(h->lo.in_ln) + (size_t)l * g.H;
+    q.X = h->at<void>(h->lo.op_h);
+    q.xmap = &h->xmap_h;
     q.omode = O_RED;
     q.dst = qkv_acc;
     q.dst_ld = g.qkv_n;
-    q.rs_src = hres;
-    q.rs_ld = g.H;
-    q.rs_len = g.H;
-    q.rs_out = r_in;
-    q.zero_ptr = l > 0 ? gu_acc : nullptr;
-    q.zero_n = gu_acc_n;
     q.e = base_epi(h);
     q.e.n_tok = n_tok;
     run_gemm(h, q, s);
 
+    {
+      FinishArgs f = fb;
+      f.layer = l;
+      f.acc = qkv_acc;
+      f.qn = h->at<float>(h->lo.qn) + (size_t)l * g.d;
+      f.kn = h->at<float>(h->lo.kn) + (size_t)l * g.d;
+      Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.qkv_n * 6, s);
+      launch_qk_finish(f, s);
+    }
+    ck(cudaGetLastError(), "qk finish launch");
+
     // attention over [cached ctx ; block] K/V, split over keys, then merge
     AttnArgs a{};
-    a.qkv = qkv_acc;
-    a.r_in = r_in;
-    a.qn = h->at<float>(h->lo.qn) + (size_t)l * g.d;
-    a.kn = h->at<float>(h->lo.kn) + (size_t)l * g.d;
-    a.rope_cs = h->at<float2>(h->lo.rope_cs);
+    a.q = h->at<void>(h->lo.q);
     a.kpool = h->at<void>(h->lo.kpool);
     a.vpool = h->at<void>(h->lo.vpool);
     a.layer = l;
@@ -581,7 +593,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     a.op = h->at<void>(h->lo.op_o);
     a.op_ld = g.Hq * g.d;
     a.op_plane = (long)Mt * g.Hq * g.d;
-    a.op_f32 = h->cfg.weight_dtype == DFLASH_F32;
+    a.op_f32 = f32;
     a.scale_log2 = 1.4426950408889634f / std::sqrt((float)g.d);
     a.err = h->at<int>(h->lo.err);
     a.g = g;
@@ -589,10 +601,10 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     const double part_b = (double)rd.n_items * g.G * kBlock * (g.d + 2) * 4;
     {
       double kv_b = 0;
-      for (int i = 0; i < rd.n_seq; ++i) kv_b += (double)rd.len[i] * g.Hkv * g.d * 2 * ekv;
-      Launch L(h, DFLASH_KERNEL_ATTENTION, kv_b + (double)n_tok * g.qkv_n * 4 + part_b, s);
+      for (int i = 0; i < rd.n_seq; ++i) kv_b += (double)(rd.len[i] + kBlock) * g.Hkv * g.d * 2 * ekv;
+      Launch L(h, DFLASH_KERNEL_ATTENTION, kv_b + (double)n_tok * g.Hq * g.d * ekv + part_b, s);
       a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_ATTENTION, rd.n_items) : nullptr;
-      if (h->use_tc) launch_attention_tc(a, rd.n_items, &h->kmap, &h->vmap, s);
+      if (h->use_tc) launch_attention_tc(a, rd.n_items, &h->qmap, &h->kmap, &h->vmap, s);
       else launch_attention_simt(a, rd.n_items, s);
     }
     ck(cudaGetLastError(), "attention launch");
@@ -602,7 +614,6 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     }
     ck(cudaGetLastError(), "attention combine launch");
 
-    // O projection added into h; clears the QKV accumulator
     GemmSpec o;
     o.site = 3 + 4 * l;
     o.W = h->at<char>(h->lo.o) + (size_t)l * g.H * g.Hq * g.d * ew;
@@ -614,45 +625,46 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     o.omode = O_RED;
     o.dst = hres;
     o.dst_ld = g.H;
-    o.zero_ptr = qkv_acc;
-    o.zero_n = qkv_acc_n;
     o.e = base_epi(h);
     o.e.n_tok = n_tok;
     run_gemm(h, o, s);
 
-    // gate/up of RMSNorm(h; post_ln) -> gate/up accumulator; r_post from h
+    prep_norm(h->at<float>(h->lo.post_ln) + (size_t)l * g.H);
+    ck(cudaGetLastError(), "post norm launch");
+
     GemmSpec gu;
     gu.site = 4 + 4 * l;
     gu.W = h->at<char>(h->lo.gu) + (size_t)l * 2 * g.I * g.H * ew;
     gu.wscale = fp8 ? h->at<float>(h->lo.s_gu) + (size_t)l * 2 * g.I : nullptr;
     gu.N = 2 * g.I;
     gu.K = g.H;
-    gu.xmode = X_FROM_H;
-    gu.xsrc = hres;
-    gu.xsrc_ld = g.H;
-    gu.xgain = h->at<float>(h->lo.post_ln) + (size_t)l * g.H;
+    gu.X = h->at<void>(h->lo.op_h);
+    gu.xmap = &h->xmap_h;
     gu.omode = O_RED;
     gu.dst = gu_acc;
     gu.dst_ld = 2 * g.I;
-    gu.rs_src = hres;
-    gu.rs_ld = g.H;
-    gu.rs_len = g.H;
-    gu.rs_out = r_post;
     gu.e = base_epi(h);
     gu.e.n_tok = n_tok;
     run_gemm(h, gu, s);
 
-    // down of SwiGLU(gate/up) added into h
+    {
+      FinishArgs f = fb;
+      f.acc = gu_acc;
+      f.op = h->at<void>(h->lo.op_a);
+      f.op_plane = (long)Mt * g.I;
+      Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.I * 16, s);
+      launch_swiglu(f, h->n_sm, s);
+    }
+    ck(cudaGetLastError(), "swiglu launch");
+
     GemmSpec dn;
     dn.site = 5 + 4 * l;
     dn.W = h->at<char>(h->lo.down) + (size_t)l * g.H * g.I * ew;
     dn.wscale = fp8 ? h->at<float>(h->lo.s_down) + (size_t)l * g.H : nullptr;
     dn.N = g.H;
     dn.K = g.I;
-    dn.xmode = X_SWIGLU;
-    dn.xsrc = gu_acc;
-    dn.xsrc_ld = 2 * g.I;
-    dn.xrs = r_post;
+    dn.X = h->at<void>(h->lo.op_a);
+    dn.xmap = &h->xmap_a;
     dn.omode = O_RED;
     dn.dst = hres;
     dn.dst_ld = g.H;
@@ -662,7 +674,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   }
   {
     Launch L(h, DFLASH_KERNEL_NORM, (double)n_tok * g.H * 8, s);
-    launch_final_norm(hres, h->at<float>(h->lo.fn), out, n_tok, gu_acc, gu_acc_n, g, s);
+    launch_final_norm(hres, h->at<float>(h->lo.fn), out, n_tok, g, s);
   }
   ck(cudaGetLastError(), "final norm launch");
 }
@@ -673,8 +685,8 @@ void plan_attention(dflash_t* h, RoundDesc& rd, const std::vector<int64_t>& lens
   int items = 0;
   for (int s = 0; s < rd.n_seq; ++s) {
     rd.item0[s] = items;
-    const int pages = (int)((lens[s] + kPage - 1) / kPage);   // cached-context pages
-    items += h->g.Hkv * std::max(1, (pages + rd.split_pages - 1) / rd.split_pages);
+    const int pages = (int)((lens[s] + kBlock + kPage - 1) / kPage);   // context + block rows
+    items += h->g.Hkv * ((pages + rd.split_pages - 1) / rd.split_pages);
   }
   rd.item0[rd.n_seq] = items;
   rd.n_items = items;
@@ -767,6 +779,15 @@ int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos
     rd.seq_slot[i] = slot;
     rd.len[i] = (int)lens[i];
     for (int j = 0; j < kBlock; ++j) rd.pos[i * kBlock + j] = pos_block[i * kBlock + j];
+    if (!ensure_pages(h, slot, lens[i] + kBlock, *blob, taken)) {
+      rollback_pages(h, *blob, taken);
+      delete blob;
+      return fail(DFLASH_ERR_CAPACITY, "out of KV pages for the block rows");
+    }
+    for (int j = 0; j < kBlock; ++j) {
+      const int64_t row = lens[i] + j;
+      rd.dest[i * kBlock + j] = h->pages[slot][row / kPage] * kPage + (int)(row % kPage);
+    }
   }
   plan_attention(h, rd, lens);
   if (rd.n_items > h->lo.items_cap) {
@@ -915,6 +936,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       h->xmap_taps = make_map_bf16(h->ws + lo.op_taps, Mt2, (uint64_t)g.n * H, 16);
       h->xmap_h = make_map_bf16(h->ws + lo.op_h, Mt2, H, 16);
       h->xmap_o = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, 16);
+      h->xmap_a = make_map_bf16(h->ws + lo.op_a, Mt2, I, 16);
+      h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
 
       const uint64_t pool_rows = (uint64_t)L * cfg->max_pages * Hkv;
       h->kmap = make_map_bf16(h->ws + lo.kpool, pool_rows * kPage, d, kPage);
