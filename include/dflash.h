@@ -25,6 +25,9 @@
  *  - Calls are asynchronous on the given stream (a cudaStream_t passed as
  *    void*, NULL = the legacy default stream).  Calls on one handle must be
  *    issued on one stream, or ordered by the caller.
+ *  - Device f32 row buffers (taps, noise_emb, out) start on a 16-byte
+ *    boundary (rows are moved as float4); a misaligned one is rejected with
+ *    DFLASH_ERR_INVALID_ARG.
  *  - The library never allocates device memory: the caller allocates the
  *    workspace (dflash_workspace_bytes) and owns every buffer.
  *  - Every call validates all of its arguments before it launches anything.
@@ -63,7 +66,7 @@ enum dflash_rope { DFLASH_ROPE_PLAIN = 0, DFLASH_ROPE_YARN = 1 };
 /* Drafter shape and capacity (the pages' DflashCfg plus storage sizes). */
 typedef struct dflash_config {
   int32_t n_layers;      /* L                                              */
-  int32_t hidden;        /* H, a multiple of 128                           */
+  int32_t hidden;        /* H, a multiple of 128, at most 8192             */
   int32_t n_heads;       /* Hq query heads                                 */
   int32_t n_kv_heads;    /* Hkv, divides Hq, Hq/Hkv <= 8                   */
   int32_t head_dim;      /* d: 64 or 128                                   */

@@ -10,8 +10,9 @@
 //   warp 1 (one lane)  tcgen05.mma: S = Q K^T into one of two TMEM buffers,
 //                      then O += P V^T into the TMEM output accumulator;
 //   warps 2..5         softmax, one thread per query row: scores from TMEM,
-//                      exp2 with a running max, P (bf16) into shared memory in
-//                      the 128-byte swizzle the MMA reads.  O is rescaled only
+//                      exp2 with a running max, P (bf16) into one of two
+//                      shared-memory buffers in the 128-byte swizzle the MMA
+//                      reads, so page j+1's softmax overlaps page j's P V^T.  O is rescaled only
 //                      when a row's max grows by more than 2^8 (exact: the
 //                      final division uses the same max).
 // Each item writes its unnormalised O with (max, sum); the combine kernel
@@ -45,16 +46,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Geo& g = a.g;
   uint8_t* sQ = smem;                                   // datoms x 16 KB
-  uint8_t* sP = sQ + t.datoms * kQAtomBytes;            // 16 KB
-  uint8_t* sKV = sP + kQAtomBytes;                      // stages x stage_bytes
+  uint8_t* sP = sQ + t.datoms * kQAtomBytes;            // 2 x 16 KB (P of pages j, j+1)
+  uint8_t* sKV = sP + 2 * kQAtomBytes;                  // stages x stage_bytes
   uint8_t* ctl = sKV + t.stages * t.stage_bytes;
   uint64_t* kvfull = reinterpret_cast<uint64_t*>(ctl);
   uint64_t* kvempty = kvfull + t.stages;
   uint64_t* sfull = kvempty + t.stages;                 // [2]
   uint64_t* qfull = sfull + 2;
-  uint64_t* pfull = qfull + 1;
-  uint64_t* pvdone = pfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pvdone + 1);
+  uint64_t* pfull = qfull + 1;                          // [2]
+  uint64_t* pvdone = pfull + 2;                         // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pvdone + 2);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);   // abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,8 +82,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(&sfull[0], 1);
     mbar_init(&sfull[1], 1);
     mbar_init(qfull, 1);
-    mbar_init(pfull, kEpiThreads);
-    mbar_init(pvdone, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pfull[b], kEpiThreads);
+      mbar_init(&pvdone[b], 1);
+    }
     flags[0] = 0;
     fence_barrier_init();
     tma_prefetch_map(&tmQ);
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = mbar_wait(qfull, 0, &flags[0]);
       tc_fence_after();
       trace_mark(a.trace, blockIdx.x, 2, c0);                   // 2: query tile ready
-      const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP);
+      const uint32_t q_addr = smem_u32(sQ);
       auto kv_addr = [&](int j) -> uint32_t { return smem_u32(sKV + (j % t.stages) * t.stage_bytes); };
       auto issue_s = [&](int j) -> bool {
         if (!mbar_wait(&kvfull[j % t.stages], (j / t.stages) & 1, &flags[0])) return false;
@@ -173,18 +176,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       if (ok && n_all > 0) ok = issue_s(0);
       if (ok && n_all > 1) ok = issue_s(1);
       for (int j = 0; j < n_all && ok; ++j) {
-        if (!mbar_wait(pfull, j & 1, &flags[0])) {
+        if (!mbar_wait(&pfull[j & 1], (j >> 1) & 1, &flags[0])) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t p_addr = smem_u32(sP + (j & 1) * kQAtomBytes);
         const uint32_t v_addr = kv_addr(j) + (uint32_t)(t.datoms * kKAtomBytes);
 #pragma unroll
         for (int kk = 0; kk < kPage / 16; ++kk) {
           const uint64_t adv = (uint64_t)(kk * 32) >> 4;
           mma_bf16(tmem, desc_sw128(p_addr) + adv, desc_sw128(v_addr) + adv, t.idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(pvdone);
+        mma_commit(&pvdone[j & 1]);
         mma_commit(&kvempty[j % t.stages]);
         if (j + 2 < n_all) ok = issue_s(j + 2);
       }
@@ -217,15 +221,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mj = fmaxf(mj, sc[i]);
       }
       const bool need = mj > m_run + kRescaleLog2;
-      if (j > 0) {
-        if (!__all_sync(0xffffffffu, mbar_wait(pvdone, (j - 1) & 1, &flags[0]))) {
+      // P buffer j&1 is free once O += P V^T of page j-2 has completed
+      if (j >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[j & 1], ((j - 2) >> 1) & 1, &flags[0]))) {
           ok = false;
           break;
         }
         __syncwarp();
         tc_fence_after();
       }
-      if (__any_sync(0xffffffffu, need && j > 0)) {
+      const bool resc = __any_sync(0xffffffffu, need && j > 0);
+      // rescaling O needs every product issued so far (through page j-1) done
+      if (resc) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1, &flags[0]))) {
+          ok = false;
+          break;
+        }
+        __syncwarp();
+        tc_fence_after();
+      }
+      if (resc) {
         const float alpha = need ? exp2f(m_run - mj) : 1.f;
         for (int c = 0; c < g.d / 32; ++c) {
           float o[32];
@@ -238,7 +253,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (need) m_run = mj;
       float lsum = 0.f;
-      uint8_t* prow = sP + (r >> 3) * 1024 + (r & 7) * 128;
+      uint8_t* prow = sP + (j & 1) * kQAtomBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
@@ -255,9 +270,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       l_run += lsum;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(pfull);
+      mbar_arrive(&pfull[j & 1]);
     }
-    if (ok && n_all > 0 && __all_sync(0xffffffffu, mbar_wait(pvdone, (n_all - 1) & 1, &flags[0]))) {
+    if (ok && n_all > 0 &&
+        __all_sync(0xffffffffu, mbar_wait(&pvdone[(n_all - 1) & 1], ((n_all - 1) >> 1) & 1, &flags[0]))) {
       __syncwarp();
       tc_fence_after();
       const long prow = (long)item * R + r;
@@ -282,6 +298,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncwarp();   // role lanes rejoin their warp before the CTA barrier
   __syncthreads();
   if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 5, c0);     // 5: exit
+  if (threadIdx.x == 64) trace_mark(a.trace, blockIdx.x, 7, c0);
   if (flags[0] && threadIdx.x == 0) atomicExch(a.err, DERR_TIMEOUT);
   if (warp == 1) {
     __syncwarp();
@@ -293,7 +310,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 size_t attn_tc_smem_bytes(int d, int stages) {
   const int datoms = d / 64;
   const int stage_bytes = datoms * kKAtomBytes + d * 128;
-  return (size_t)datoms * kQAtomBytes + kQAtomBytes + (size_t)stages * stage_bytes + 256 + 1024;
+  return (size_t)datoms * kQAtomBytes + 2 * kQAtomBytes + (size_t)stages * stage_bytes + 256 + 1024;
 }
 
 void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,

@@ -30,6 +30,7 @@ constexpr int kTileK = 64;        // K columns per unit
 constexpr int kPassTok = 256;     // token columns per GEMM pass (one MMA N)
 constexpr int kMaxBatch = 64;
 constexpr int kMaxIngestRows = 512;
+constexpr int kMaxHidden = 8192;  // widest residual row the row kernels hold in registers
 constexpr int kMaxPtUpdates = 160;
 constexpr int kEpiThreads = 128;  // threads running a tile epilogue
 constexpr int kEpiTokChunk = 32;  // tokens per epilogue pass

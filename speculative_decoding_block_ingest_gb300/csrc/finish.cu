@@ -3,6 +3,7 @@
 // They run as short, wide kernels between the weight-streaming ones (chained
 // by programmatic dependent launch) so that no latency-bound step sits inside
 // a kernel that streams HBM at full rate:
+//   final_norm   the round's closing RMSNorm into the f32 output rows;
 //   prep_norm    RMSNorm operand of the next projection: per token row,
 //                x = h * gain * rsqrt(mean(h^2) + eps) as hi/lo bf16 planes
 //                (or f32 for f32 drafters);
@@ -19,30 +20,82 @@
 
 namespace dfl {
 
-__global__ void __launch_bounds__(128) prep_norm_kernel(FinishArgs f) {
+// Row kernels: one CTA of kRowThreads per token row, every load of the row
+// (and of the gain) issued before the first use, so a row costs one L2 round
+// trip plus a block reduction.
+constexpr int kRowThreads = 256;
+constexpr int kRowVec = kMaxHidden / (4 * kRowThreads);   // float4 per thread
+
+__device__ __forceinline__ float block_sum_rows(float v) {
+  __shared__ float red[kRowThreads / 32];
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kRowThreads / 32; ++w) t += red[w];
+  return t;
+}
+
+// x = row * gain * rsqrt(mean(row^2) + eps) for the row's float4 slots this
+// thread owns (slot tid + k * kRowThreads); returns false for unused slots.
+struct RowNorm {
+  float4 v[kRowVec], w[kRowVec];
+  float r;
+  __device__ void load(const float* row, const float* gain, int H, float eps) {
+    const int n4 = H / 4;
+    const float4* r4 = reinterpret_cast<const float4*>(row);
+    const float4* g4 = reinterpret_cast<const float4*>(gain);
+#pragma unroll
+    for (int k = 0; k < kRowVec; ++k) {
+      const int i = threadIdx.x + k * kRowThreads;
+      v[k] = i < n4 ? __ldcg(r4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+      w[k] = i < n4 ? __ldg(g4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < kRowVec; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    r = rsqrtf(block_sum_rows(ss) / (float)H + eps);
+  }
+  __device__ float4 out(int k) const {
+    return make_float4(v[k].x * w[k].x * r, v[k].y * w[k].y * r, v[k].z * w[k].z * r, v[k].w * w[k].w * r);
+  }
+};
+
+__global__ void __launch_bounds__(kRowThreads) prep_norm_kernel(FinishArgs f) {
   pdl_wait();
   pdl_launch_dependents();
-  const int tok = blockIdx.x, tid = threadIdx.x;
+  const int tok = blockIdx.x;
   const Geo& g = f.g;
-  const float* row = f.h + (long)tok * g.H;
-  __shared__ float red[4];
-  float ss = 0.f;
-  for (int c = tid * 4; c < g.H; c += 512) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  RowNorm rn;
+  rn.load(f.h + (long)tok * g.H, f.gain, g.H, g.eps);
+#pragma unroll
+  for (int k = 0; k < kRowVec; ++k) {
+    const int i = threadIdx.x + k * kRowThreads;
+    if (4 * i < g.H) {
+      const float4 x = rn.out(k);
+      const long idx = (long)tok * g.H + 4 * i;
+      put_operand(f.op, idx + 0, f.op_plane, x.x, f.op_f32);
+      put_operand(f.op, idx + 1, f.op_plane, x.y, f.op_f32);
+      put_operand(f.op, idx + 2, f.op_plane, x.z, f.op_f32);
+      put_operand(f.op, idx + 3, f.op_plane, x.w, f.op_f32);
+    }
   }
-  ss = warp_sum(ss);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
-  __syncthreads();
-  const float r = rsqrtf((red[0] + red[1] + red[2] + red[3]) / (float)g.H + g.eps);
-  for (int c = tid * 4; c < g.H; c += 512) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
-    const float4 w = __ldg(reinterpret_cast<const float4*>(f.gain + c));
-    const long idx = (long)tok * g.H + c;
-    put_operand(f.op, idx + 0, f.op_plane, v.x * w.x * r, f.op_f32);
-    put_operand(f.op, idx + 1, f.op_plane, v.y * w.y * r, f.op_f32);
-    put_operand(f.op, idx + 2, f.op_plane, v.z * w.z * r, f.op_f32);
-    put_operand(f.op, idx + 3, f.op_plane, v.w * w.w * r, f.op_f32);
+}
+
+// Final RMSNorm of the residual stream into the f32 output rows.
+__global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* h, const float* gain, float* out, int H,
+                                                               float eps) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int tok = blockIdx.x;
+  RowNorm rn;
+  rn.load(h + (long)tok * H, gain, H, eps);
+  float4* o4 = reinterpret_cast<float4*>(out + (long)tok * H);
+#pragma unroll
+  for (int k = 0; k < kRowVec; ++k) {
+    const int i = threadIdx.x + k * kRowThreads;
+    if (4 * i < H) o4[i] = rn.out(k);
   }
 }
 
@@ -134,7 +187,11 @@ __global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
 }
 
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s) {
-  launch_pdl(prep_norm_kernel, dim3(f.n_tok), dim3(128), 0, s, f);
+  launch_pdl(prep_norm_kernel, dim3(f.n_tok), dim3(kRowThreads), 0, s, f);
+}
+
+void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s) {
+  launch_pdl(final_norm_kernel, dim3(n_tok), dim3(kRowThreads), 0, s, h, gain, out, g.H, g.eps);
 }
 
 void launch_qk_finish(const FinishArgs& f, cudaStream_t s) {

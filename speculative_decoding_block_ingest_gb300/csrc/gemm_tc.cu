@@ -237,6 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncwarp();   // role lanes rejoin their warp before the CTA barrier
   __syncthreads();
   if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 5, c0);  // 5: all roles done
+  if (threadIdx.x == 64) trace_mark(a.trace, blockIdx.x, 7, c0);
   if (flags[0] && threadIdx.x == 0) atomicExch(const_cast<int*>(err), DERR_TIMEOUT);
   if (warp == 1) {
     __syncwarp();

@@ -199,10 +199,31 @@ void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s) {
   launch_pdl(attn_simt_kernel, dim3(n_items), dim3(128), smem, s, a);
 }
 
-// Merge the split-KV partials of one (token, q head) row into the O-proj operand.
-__global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
+// Merge the split-KV partials of one (token, q head) row into the O-proj
+// operand.  All loads of a pass are issued before their use: the (m, l) pairs
+// one split per thread, then the partial rows (d/4 lanes per split, a warp
+// covering 32/(d/4) splits, eight warps, four splits deep per thread).
+constexpr int kCombThreads = 256;
+__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float u = __shfl_xor_sync(0xffffffffu, v, o);
+    v = is_max ? fmaxf(v, u) : v + u;
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = red[0];
+#pragma unroll
+  for (int w = 1; w < kCombThreads / 32; ++w) t = is_max ? fmaxf(t, red[w]) : t + red[w];
+  __syncthreads();
+  return t;
+}
+
+__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) {
   pdl_wait();
   pdl_launch_dependents();
+  __shared__ float red[kCombThreads / 32];
+  __shared__ float4 part[kCombThreads];
   const Geo& g = a.g;
   const int row = blockIdx.x;               // tok * Hq + h
   const int tok = row / g.Hq, h = row % g.Hq;
@@ -212,78 +233,116 @@ __global__ void __launch_bounds__(128) attn_combine_kernel(AttnArgs a) {
   const RoundDesc* rd = a.rd;
   const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / g.Hkv;
   const int it0 = rd->item0[s] + kvh * nsplit;
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
   float M = -INFINITY;
-  for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, a.part_ml[((long)(it0 + sp) * R + r) * 2]);
-  const int dim = threadIdx.x;
-  if (dim >= g.d) return;
-  float num = 0.f, den = 0.f;
-  for (int sp = 0; sp < nsplit; ++sp) {
-    const long pr = (long)(it0 + sp) * R + r;
-    const float w = exp2f(a.part_ml[pr * 2] - M);
-    den += w * a.part_ml[pr * 2 + 1];
-    num += w * a.part_o[pr * g.d + dim];
+  for (int sp = threadIdx.x; sp < nsplit; sp += kCombThreads) M = fmaxf(M, __ldcg(ml + (long)(it0 + sp) * R + r).x);
+  M = block_reduce(M, true, red);
+
+  const int lpp = g.d / 4, spw = 32 / lpp, step = (kCombThreads / 32) * spw;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int sub = lane / lpp, d4 = lane % lpp;
+  const float4* po = reinterpret_cast<const float4*>(a.part_o);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+  for (int base = warp * spw + sub; base < nsplit; base += 4 * step) {
+    float4 o[4];
+    float2 m[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int sp = base + k * step;
+      const long pr = (long)(it0 + sp) * R + r;
+      o[k] = sp < nsplit ? __ldcg(po + pr * lpp + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      m[k] = sp < nsplit ? __ldcg(ml + pr) : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float w = exp2f(m[k].x - M);
+      acc.x += w * o[k].x;
+      acc.y += w * o[k].y;
+      acc.z += w * o[k].z;
+      acc.w += w * o[k].w;
+      if (d4 == 0) den += w * m[k].y;
+    }
   }
-  put_operand(a.op, (long)tok * a.op_ld + h * g.d + dim, a.op_plane, num / den, a.op_f32);
+  den = block_reduce(den, false, red);
+  part[threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.x < lpp) {
+    float4 t = part[threadIdx.x];
+    for (int j = 1; j < step; ++j) {
+      const float4 u = part[j * lpp + threadIdx.x];
+      t.x += u.x;
+      t.y += u.y;
+      t.z += u.z;
+      t.w += u.w;
+    }
+    const float inv = 1.f / den;
+    const long idx = (long)tok * a.op_ld + h * g.d + 4 * threadIdx.x;
+    put_operand(a.op, idx + 0, a.op_plane, t.x * inv, a.op_f32);
+    put_operand(a.op, idx + 1, a.op_plane, t.y * inv, a.op_f32);
+    put_operand(a.op, idx + 2, a.op_plane, t.z * inv, a.op_f32);
+    put_operand(a.op, idx + 3, a.op_plane, t.w * inv, a.op_f32);
+  }
 }
 
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s) {
-  launch_pdl(attn_combine_kernel, dim3(n_tok * a.g.Hq), dim3(128), 0, s, a);
+  launch_pdl(attn_combine_kernel, dim3(n_tok * a.g.Hq), dim3(kCombThreads), 0, s, a);
 }
 
 // ------------------------------------------------------------------ per-call init
 // CTA r < n_rows: stage row r (residual stream + operand); CTA n_rows: upload
-// the descriptor, apply page-table entries and clear accumulators.
-__global__ void __launch_bounds__(128) init_kernel(InitArgs a, InitBlob b) {
+// the used words of the descriptor, apply page-table entries and clear
+// accumulators.  Row copies issue four float4 loads per thread before storing.
+constexpr int kInitThreads = 256;
+__global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __grid_constant__ InitBlob b) {
   pdl_wait();
   pdl_launch_dependents();
   const int r = blockIdx.x, tid = threadIdx.x;
   if (r == a.n_rows) {
     const int* src = reinterpret_cast<const int*>(&b);
     int* dst = reinterpret_cast<int*>(a.desc_dst);
-    for (int i = tid; i < a.desc_bytes / 4; i += blockDim.x) dst[i] = src[i];
-    for (int i = tid; i < b.n_pt; i += blockDim.x) a.block_table[b.pt_idx[i]] = b.pt_page[i];
-    for (int i = tid; i < a.zero_n; i += blockDim.x) a.zero_ptr[i] = 0.f;
+    for (int q = 0; q < 3; ++q)
+      for (int i = tid; i < a.cp_len[q]; i += kInitThreads) dst[a.cp_off[q] + i] = src[a.cp_off[q] + i];
+    for (int i = tid; i < b.n_pt; i += kInitThreads) a.block_table[b.pt_idx[i]] = b.pt_page[i];
+    for (int i = tid; i < a.zero_n; i += kInitThreads) a.zero_ptr[i] = 0.f;
     return;
   }
   // RoPE (cos, sin) of this row's position, mscale folded in
   const int pos = a.is_round ? b.round.pos[r] : b.ingest.row_pos[r];
   const int half = a.g.d / 2;
-  for (int j = tid; j < half; j += blockDim.x) {
+  for (int j = tid; j < half; j += kInitThreads) {
     float sn, cs;
     rope_sincos(pos, a.inv_freq, j, &sn, &cs);
     a.rope_cs[(long)r * half + j] = make_float2(cs * a.g.mscale, sn * a.g.mscale);
   }
-  for (int c = tid; c < a.width; c += blockDim.x) {
-    const float v = a.src[(long)r * a.width + c];
-    if (a.h) a.h[(long)r * a.width + c] = v;
-    else put_operand(a.op, (long)r * a.op_ld + c, a.op_plane, v, a.op_f32);
+  const int n4 = a.width / 4;
+  const float4* src4 = reinterpret_cast<const float4*>(a.src + (long)r * a.width);
+  for (int c0 = tid; c0 < n4; c0 += 4 * kInitThreads) {
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = c0 + k * kInitThreads;
+      v[k] = c < n4 ? __ldg(src4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = c0 + k * kInitThreads;
+      if (c >= n4) break;
+      if (a.h) {
+        reinterpret_cast<float4*>(a.h + (long)r * a.width)[c] = v[k];
+      } else {
+        const long idx = (long)r * a.op_ld + 4 * c;
+        put_operand(a.op, idx + 0, a.op_plane, v[k].x, a.op_f32);
+        put_operand(a.op, idx + 1, a.op_plane, v[k].y, a.op_f32);
+        put_operand(a.op, idx + 2, a.op_plane, v[k].z, a.op_f32);
+        put_operand(a.op, idx + 3, a.op_plane, v[k].w, a.op_f32);
+      }
+    }
   }
 }
 
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s) {
-  launch_pdl(init_kernel, dim3(a.n_rows + 1), dim3(128), 0, s, a, blob);
-}
-
-__global__ void __launch_bounds__(128) final_norm_kernel(const float* h, const float* gain, float* out, int H,
-                                                         float eps) {
-  pdl_wait();
-  pdl_launch_dependents();
-  const int tok = blockIdx.x, tid = threadIdx.x;
-  __shared__ float red[4];
-  float ss = 0.f;
-  for (int c = tid; c < H; c += blockDim.x) {
-    const float v = h[(long)tok * H + c];
-    ss += v * v;
-  }
-  ss = warp_sum(ss);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
-  __syncthreads();
-  const float r = rsqrtf((red[0] + red[1] + red[2] + red[3]) / (float)H + eps);
-  for (int c = tid; c < H; c += blockDim.x) out[(long)tok * H + c] = h[(long)tok * H + c] * gain[c] * r;
-}
-
-void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s) {
-  launch_pdl(final_norm_kernel, dim3(n_tok), dim3(128), 0, s, h, gain, out, g.H, g.eps);
+  launch_pdl(init_kernel, dim3(a.n_rows + 1), dim3(kInitThreads), 0, s, a, blob);
 }
 
 __global__ void kv_read_kernel(Geo g, const void* kpool, const void* vpool, const int* block_table,

@@ -140,6 +140,7 @@ int validate_config(const dflash_config* c) {
   if (c->n_layers < 1 || c->hidden < 128 || c->n_heads < 1 || c->n_kv_heads < 1 || c->intermediate < 64 ||
       c->n_taps < 1)
     return fail(DFLASH_ERR_INVALID_ARG, "non-positive dimension in config");
+  if (c->hidden > kMaxHidden) return fail(DFLASH_ERR_UNSUPPORTED, "hidden must be at most %d", kMaxHidden);
   if (c->block != kBlock) return fail(DFLASH_ERR_UNSUPPORTED, "block must be 16 (got %d)", c->block);
   if (c->page_size != kPage) return fail(DFLASH_ERR_UNSUPPORTED, "page_size must be 64 (got %d)", c->page_size);
   if (c->head_dim != 64 && c->head_dim != 128) return fail(DFLASH_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
@@ -435,7 +436,12 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   ia.zero_ptr = ss_feat;
   ia.zero_n = n_rows;
   ia.desc_dst = h->at<void>(h->lo.idesc);
-  ia.desc_bytes = sizeof(IngestDesc);
+  ia.cp_off[0] = 0;
+  ia.cp_len[0] = (int)(offsetof(IngestDesc, row_pos) / 4);
+  ia.cp_off[1] = (int)(offsetof(IngestDesc, row_pos) / 4);
+  ia.cp_len[1] = n_rows;
+  ia.cp_off[2] = (int)(offsetof(IngestDesc, row_dest) / 4);
+  ia.cp_len[2] = n_rows;
   ia.block_table = h->at<int>(h->lo.btab);
   ia.inv_freq = h->at<double>(h->lo.inv_freq);
   ia.rope_cs = h->at<float2>(h->lo.rope_cs);
@@ -519,7 +525,12 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   ia.width = g.H;
   ia.h = hres;
   ia.desc_dst = h->at<void>(h->lo.rdesc);
-  ia.desc_bytes = sizeof(RoundDesc);
+  ia.cp_off[0] = 0;
+  ia.cp_len[0] = (int)(offsetof(RoundDesc, pos) / 4);
+  ia.cp_off[1] = (int)(offsetof(RoundDesc, pos) / 4);
+  ia.cp_len[1] = n_tok;
+  ia.cp_off[2] = (int)(offsetof(RoundDesc, dest) / 4);
+  ia.cp_len[2] = n_tok;
   ia.block_table = h->at<int>(h->lo.btab);
   ia.inv_freq = h->at<double>(h->lo.inv_freq);
   ia.rope_cs = h->at<float2>(h->lo.rope_cs);
@@ -692,6 +703,8 @@ void plan_attention(dflash_t* h, RoundDesc& rd, const std::vector<int64_t>& lens
   rd.n_items = items;
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 template <class F>
 int guarded(F&& f) {
   try {
@@ -726,6 +739,7 @@ int ingest_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* t_
   if (total > h->cfg.max_ingest_rows)
     return fail(DFLASH_ERR_CAPACITY, "ingest of %ld rows exceeds max_ingest_rows %d", total, h->cfg.max_ingest_rows);
   if (!taps || !pos_new) return fail(DFLASH_ERR_INVALID_ARG, "taps / pos_new is null");
+  if (!aligned16(taps)) return fail(DFLASH_ERR_INVALID_ARG, "taps must start on a 16-byte boundary");
   for (int i = 0; i < n_seq; ++i)
     if (h->len[slots[i]] + t_per_seq[i] + kBlock > h->cfg.max_seq_len)
       return fail(DFLASH_ERR_CAPACITY, "sequence %d would exceed max_seq_len %d", slots[i], h->cfg.max_seq_len);
@@ -766,6 +780,8 @@ int ingest_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* t_
 int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos_block, const float* noise,
                 float* out, cudaStream_t s) {
   if (!pos_block || !noise || !out) return fail(DFLASH_ERR_INVALID_ARG, "pos_block / noise_emb / out is null");
+  if (!aligned16(noise) || !aligned16(out))
+    return fail(DFLASH_ERR_INVALID_ARG, "noise_emb / out must start on a 16-byte boundary");
   InitBlob* blob = new InitBlob();
   std::vector<int> taken;
   blob->n_pt = 0;
@@ -994,6 +1010,8 @@ int dflash_forward_full(dflash_t* h, int32_t ctx, const float* taps, const float
   if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
   if (ctx < 0) return fail(DFLASH_ERR_INVALID_ARG, "negative ctx");
   if (!pos || !noise_emb || !out || (ctx > 0 && !taps)) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  if (!aligned16(noise_emb) || !aligned16(out) || (ctx > 0 && !aligned16(taps)))
+    return fail(DFLASH_ERR_INVALID_ARG, "taps / noise_emb / out must start on a 16-byte boundary");
   if (ctx + kBlock > h->cfg.max_seq_len) return fail(DFLASH_ERR_CAPACITY, "ctx exceeds max_seq_len");
   const int need = (ctx + kBlock + kPage - 1) / kPage;
   if ((int)h->free_pages.size() < need) return fail(DFLASH_ERR_CAPACITY, "out of KV pages");
