@@ -27,7 +27,8 @@
  *    issued on one stream, or ordered by the caller.
  *  - Device f32 row buffers (taps, noise_emb, out) start on a 16-byte
  *    boundary (rows are moved as float4); a misaligned one is rejected with
- *    DFLASH_ERR_INVALID_ARG.
+ *    DFLASH_ERR_INVALID_ARG.  So do bf16 weight matrices (re-blocked at
+ *    dflash_create with 16-byte moves).
  *  - The library never allocates device memory: the caller allocates the
  *    workspace (dflash_workspace_bytes) and owns every buffer.
  *  - Every call validates all of its arguments before it launches anything.

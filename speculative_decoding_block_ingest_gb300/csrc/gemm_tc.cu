@@ -5,10 +5,12 @@
 // weight dimension fills the tensor core while the few drafted rows ride
 // along.  Stream-K over units of 64 K-columns spreads every projection over
 // all SMs.  One CTA of six warps per SM (two fit):
-//   warp 0 (one lane)  TMA producer: weight tiles [128 x 64] and the operand's
-//                      hi/lo bf16 planes [N x 64] into a ring of stages (the
-//                      first stages' weights before the programmatic-launch
-//                      wait, so they stream during the previous kernel's tail);
+//   warp 0 (one lane)  producer: weight blocks [128 x 64] (one contiguous
+//                      16 KB bulk copy each, stored pre-swizzled) and the
+//                      operand's hi/lo bf16 planes [N x 64] (TMA) into a ring
+//                      of stages (the first stages' weights before the
+//                      programmatic-launch wait, so they stream during the
+//                      previous kernel's tail);
 //   warp 1 (one lane)  MMA issuer: per unit, 4 K-steps x (hi, lo) tcgen05.mma
 //                      into a TMEM accumulator (two buffers);
 //   warps 2..5         drain: move finished accumulators out of TMEM and
@@ -29,6 +31,7 @@ struct TcCfg {
   int stages;
   int stage_bytes;
   int tmem_cols;
+  int aw;            // accumulator columns: 2*nt when hi and lo ride in one MMA, else nt
   int x_row_lo;      // row of the lo plane in the operand map (= Mt)
   uint32_t idesc;
 };
@@ -40,9 +43,9 @@ constexpr int kXBox = 16;                           // operand rows per TMA box
 // One CTA per SM with a deep ring: every stage it can hold is filled with
 // weights before the programmatic-launch wait, so HBM keeps streaming while
 // the small kernel before it finishes.
+template <bool kFused>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, GemmArgs a,
-                   TcCfg t) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, GemmArgs a, TcCfg t) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ctl = smem + t.stages * t.stage_bytes;
@@ -74,7 +77,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     flags[0] = flags[1] = 0;
     fence_barrier_init();
-    tma_prefetch_map(&tmW);
     tma_prefetch_map(&tmX);
   }
   if (warp == 1) tmem_alloc(tmem_slot, t.tmem_cols);
@@ -92,49 +94,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t x_plane_bytes = (uint32_t)t.nt * 128;
   const int* err = a.e.err;
 
+  // The two single-thread loops below are latency-bound on their own scalar
+  // work, so they keep it minimal: stage index and phase are stepped, not
+  // divided out, and the descriptors are the base descriptor plus offsets.
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
       const uint64_t pol = policy_evict_first();
+      const uint8_t* wsrc = static_cast<const uint8_t*>(a.W) + (size_t)u0 * kWTileBytes;
       const uint32_t bytes = kWTileBytes + 2 * x_plane_bytes;
-      auto load_x = [&](int i, int u) {
-        uint8_t* st = smem + (i % t.stages) * t.stage_bytes;
-        const int kx = (u % p.kb) * kTileK;
-        for (int r = 0; r < t.nt; r += kXBox) {
-          tma_load_2d(st + kWTileBytes + r * 128, &tmX, &full[i % t.stages], kx, a.e.tok_base + r);
-          tma_load_2d(st + kWTileBytes + x_plane_bytes + r * 128, &tmX, &full[i % t.stages], kx,
-                      t.x_row_lo + a.e.tok_base + r);
-        }
-      };
       const int pre = min(n_units, t.stages);
       for (int i = 0; i < pre; ++i) {
-        const int u = u0 + i;
         mbar_arrive_expect_tx(&full[i], bytes);
-        tma_load_2d_hint(smem + i * t.stage_bytes, &tmW, &full[i], (u % p.kb) * kTileK, (u / p.kb) * kTileN, pol);
+        bulk_load_hint(smem + i * t.stage_bytes, wsrc + (size_t)i * kWTileBytes, kWTileBytes, &full[i], pol);
       }
       pdl_wait();
       // dependents may launch only once this kernel is past its own wait, so
       // at most two kernels overlap and everything older has completed
       pdl_launch_dependents();
       trace_mark(a.trace, blockIdx.x, 2, c0);               // 2: producer past the launch wait
-      for (int i = 0; i < pre; ++i) load_x(i, u0 + i);
+      const int kmax = p.kb * kTileK;
+      const int y_hi = a.e.tok_base, y_lo = t.x_row_lo + a.e.tok_base;
+      int kx = (u0 % p.kb) * kTileK;                        // operand column of the next unit
+      auto load_x = [&](uint8_t* st, uint64_t* bar) {
+        for (int r = 0; r < t.nt; r += kXBox) {
+          tma_load_2d(st + kWTileBytes + r * 128, &tmX, bar, kx, y_hi + r);
+          tma_load_2d(st + kWTileBytes + x_plane_bytes + r * 128, &tmX, bar, kx, y_lo + r);
+        }
+        kx += kTileK;
+        if (kx == kmax) kx = 0;
+      };
+      for (int i = 0; i < pre; ++i) load_x(smem + i * t.stage_bytes, &full[i]);
+      int st = 0;
+      uint32_t ph = 0;   // parity of the empty phase the next refill waits for
       for (int i = pre; i < n_units; ++i) {
-        const int s = i % t.stages;
-        if (!mbar_wait(&empty[s], ((i / t.stages) & 1) ^ 1, &flags[0])) {
+        if (!mbar_wait(&empty[st], ph, &flags[0])) {
           flags[0] = 1;
           break;
         }
-        const int u = u0 + i;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        tma_load_2d_hint(smem + s * t.stage_bytes, &tmW, &full[s], (u % p.kb) * kTileK, (u / p.kb) * kTileN, pol);
-        load_x(i, u);
+        uint8_t* sp = smem + st * t.stage_bytes;
+        mbar_arrive_expect_tx(&full[st], bytes);
+        bulk_load_hint(sp, wsrc + (size_t)i * kWTileBytes, kWTileBytes, &full[st], pol);
+        load_x(sp, &full[st]);
+        if (++st == t.stages) {
+          st = 0;
+          ph ^= 1;
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      int i = 0, seg = 0;
+      // descriptor start fields are address >> 4 (14 bits, shared memory
+      // < 256 KB), so stage and K-step offsets add without carries
+      const uint64_t d0 = desc_sw128(smem_u32(smem));
+      const uint32_t dstage = (uint32_t)t.stage_bytes >> 4;
+      constexpr uint32_t xo = kWTileBytes >> 4;
+      const uint32_t lo = (kWTileBytes + x_plane_bytes) >> 4;
+      const uint32_t idesc = t.idesc;
+      int seg = 0, st = 0;
+      uint32_t ph = 0;
       bool ok = true;
+      unsigned long long wait_cyc = 0, issue_cyc = 0, first_full = 0;
       for (int u = u0; u < u1 && ok; ++seg) {
         const int T = u / p.kb;
         const int seg_end = min(u1, (T + 1) * p.kb);
@@ -144,30 +165,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(b * t.nt);
-        for (const int seg_start = u; u < seg_end; ++u, ++i) {
-          const int s = i % t.stages;
-          if (!mbar_wait(&full[s], (i / t.stages) & 1, &flags[0])) {
+        const uint32_t d_tmem = tmem + (uint32_t)(b * t.aw);
+        for (int k = 0; u < seg_end; ++u, ++k) {
+          const unsigned long long w0 = a.trace ? trace_clock() : 0;
+          if (!mbar_wait(&full[st], ph, &flags[0])) {
             flags[0] = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + s * t.stage_bytes);
-          const uint64_t dw = desc_sw128(sa);
-          const uint64_t dh = desc_sw128(sa + kWTileBytes);
-          const uint64_t dl = desc_sw128(sa + kWTileBytes + x_plane_bytes);
+          const unsigned long long w1 = a.trace ? trace_clock() : 0;
+          const uint64_t dw = d0 + (uint64_t)(st * dstage);
+          // 4 K-steps of 16 (32 bytes = 2 descriptor units each)
+          mma_bf16(d_tmem, dw, dw + xo, idesc, k > 0 ? 1u : 0u);
+          if (!kFused) mma_bf16(d_tmem, dw, dw + lo, idesc, 1u);
 #pragma unroll
-          for (int kk = 0; kk < kTileK / 16; ++kk) {
-            const uint64_t adv = (uint64_t)(kk * 32) >> 4;   // 16 bf16 = 32 bytes per K-step
-            mma_bf16(d_tmem, dw + adv, dh + adv, t.idesc, (u > seg_start || kk > 0) ? 1u : 0u);
-            mma_bf16(d_tmem, dw + adv, dl + adv, t.idesc, 1u);
+          for (uint32_t kk = 2; kk < 8; kk += 2) {
+            mma_bf16(d_tmem, dw + kk, dw + xo + kk, idesc, 1u);
+            if (!kFused) mma_bf16(d_tmem, dw + kk, dw + lo + kk, idesc, 1u);
           }
-          mma_commit(&empty[s]);
+          mma_commit(&empty[st]);
+          if (a.trace) {
+            wait_cyc += w1 - w0;
+            issue_cyc += trace_clock() - w1;
+            if (u == u0) first_full = w1 - c0;
+          }
+          if (++st == t.stages) {
+            st = 0;
+            ph ^= 1;
+          }
         }
         if (ok) mma_commit(&accfull[b]);
       }
       trace_mark(a.trace, blockIdx.x, 3, c0);                   // 3: last MMA issued
+      if (a.trace) {   // 8, 9, 10: issuer cycles waiting for stages, issuing; first stage ready
+        a.trace[(long)blockIdx.x * kTraceWords + 9] = wait_cyc;
+        a.trace[(long)blockIdx.x * kTraceWords + 10] = issue_cyc;
+        a.trace[(long)blockIdx.x * kTraceWords + 11] = first_full;
+      }
     }
   } else {
     // ------------------------------------------------------------------ drain
@@ -175,6 +210,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int et = threadIdx.x - 64;
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
     const int row = 32 * q + lane;          // tile row (output feature) of this thread
+    // the thread's row of accumulator buffer b, token columns j0..j0+15
+    // (hi + lo halves when fused)
+    auto acc_ld16 = [&](int b, int j0, float* v) {
+      const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * t.aw + j0);
+      tmem_ld16(base, v);
+      if (kFused) {
+        float w[16];
+        tmem_ld16(base + (uint32_t)t.nt, w);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] += w[j];
+      }
+    };
     int seg = 0;
     for (int u = u0; u < u1; ++seg) {
       const int T = u / p.kb;
@@ -194,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const float wsc = a.e.wscale ? a.e.wscale[T * kTileN + row] : 1.f;
           for (int j0 = 0; j0 < a.e.n_tok; j0 += 16) {
             float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * t.nt + j0), v);
+            acc_ld16(b, j0, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (j0 + j < a.e.n_tok)
@@ -209,7 +256,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (got) {
           for (int j0 = 0; j0 < a.e.n_tok; j0 += 16) {
             float v[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * t.nt + j0), v);
+            acc_ld16(b, j0, v);
             acc_add16(acc_tile + (long)row * t.nt, j0, a.e.n_tok, v);
           }
         }
@@ -258,26 +305,31 @@ size_t gemm_tc_smem_bytes(int nt, int stages) {
   return (size_t)stages * stage_bytes + 512 + kRedFloats * 4 + 1024;
 }
 
-void launch_gemm_tc(const GemmArgs& a, const void* tmap_w, const void* tmap_x, cudaStream_t s) {
+void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s) {
   TcCfg t{};
   t.nt = (a.e.n_tok + 15) / 16 * 16;
   t.stage_bytes = kWTileBytes + 2 * t.nt * 128;
   // as many stages as the SM's shared memory holds (weights prefetched before
   // the launch wait)
   t.stages = std::max(2, std::min(12, (225 * 1024 - 512 - kRedFloats * 4) / t.stage_bytes));
-  t.tmem_cols = pow2_at_least(2 * t.nt);
+  // the lo plane follows the hi plane in the stage, so for nt <= 128 one MMA
+  // with N = 2*nt multiplies both (half the tcgen05.mma issues; the drain adds
+  // the two column halves)
+  const bool fused = 2 * t.nt <= 256;
+  t.aw = fused ? 2 * t.nt : t.nt;
+  t.tmem_cols = pow2_at_least(2 * t.aw);
   t.x_row_lo = a.e.g.Mt;
-  t.idesc = idesc_bf16(kTileN, t.nt);
+  t.idesc = idesc_bf16(kTileN, t.aw);
   const size_t smem = gemm_tc_smem_bytes(t.nt, t.stages);
-  static size_t attr_bytes = 0;
-  if (smem > attr_bytes) {
-    if (cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+  static size_t attr_bytes[2] = {0, 0};
+  auto kern = fused ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
+  if (smem > attr_bytes[fused]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return;   // the launch below is skipped; the caller's cudaGetLastError reports it
-    attr_bytes = smem;
+    attr_bytes[fused] = smem;
   }
-  const CUtensorMap* mw = static_cast<const CUtensorMap*>(tmap_w);
   const CUtensorMap* mx = static_cast<const CUtensorMap*>(tmap_x);
-  launch_pdl(gemm_tc_kernel, dim3(a.p.grid), dim3(kTcThreads), smem, s, *mw, *mx, a, t);
+  launch_pdl(kern, dim3(a.p.grid), dim3(kTcThreads), smem, s, *mx, a, t);
 }
 
 }  // namespace dfl

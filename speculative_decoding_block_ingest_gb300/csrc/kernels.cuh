@@ -15,7 +15,7 @@ enum OMode {
 // One weight-streaming projection: Y[tok][N] = X[tok][K] * W[N][K]^T
 // (swap-AB: W rows are tile rows, tokens are columns).
 struct GemmArgs {
-  const void* W;      // [N][K] in Geo::wtype
+  const void* W;      // [N][K] in Geo::wtype (bf16 tensor-core path: 16 KB blocks)
   int N, K;
   const void* X;      // operand [tok][K]: f32, or bf16 hi plane (+ lo plane at x_plane)
   int x_ld;
@@ -112,7 +112,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 void launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
-void launch_gemm_tc(const GemmArgs& a, const void* tmap_w, const void* tmap_x, cudaStream_t s);
+// Tensor-core projection: a.W is the weight in 16 KB blocks (see weights.cu).
+void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s);
+void launch_repack(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base, cudaStream_t s);
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s);
 void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
                          cudaStream_t s);

@@ -193,6 +193,8 @@ void rope_table(const dflash_config& c, std::vector<double>& inv, float& mscale)
   mscale = (float)(0.1 * std::log(c.yarn_factor) + 1.0);
 }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -249,8 +251,7 @@ struct dflash_handle {
   cudaStream_t last_stream = nullptr;
   // measurement: kernel launches issued, and (when enabled) per-kind event pairs
   int64_t launches = 0;
-  // tensor maps of the tensor-core projections: weights per GEMM site, operands per buffer
-  std::vector<CUtensorMap> wmap;
+  // tensor maps of the tensor-core projections' operands (per buffer)
   CUtensorMap xmap_taps, xmap_h, xmap_o, xmap_a;
   CUtensorMap qmap, kmap, vmap;                 // attention: q buffer (3-D), K pool, V^T pool
   bool use_tc = false;
@@ -410,7 +411,7 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     const double bytes = (double)sp.N * sp.K * esize_w(g.wtype) + (g.wtype == W_FP8 ? sp.N * 4.0 : 0.0) + x_b + out_b;
     Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
     a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_GEMM, a.p.grid) : nullptr;
-    if (h->use_tc) launch_gemm_tc(a, &h->wmap[sp.site], sp.xmap, s);
+    if (h->use_tc) launch_gemm_tc(a, sp.xmap, s);
     else launch_gemm_simt(a, s);
   }
   ck(cudaGetLastError(), "gemm launch");
@@ -703,7 +704,6 @@ void plan_attention(dflash_t* h, RoundDesc& rd, const std::vector<int64_t>& lens
   rd.n_items = items;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 template <class F>
 int guarded(F&& f) {
@@ -860,7 +860,14 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       return fail(DFLASH_ERR_INVALID_ARG, "missing tensor in layer %d", l);
     if (fp8 && (!L.q_scale || !L.k_scale || !L.v_scale || !L.o_scale || !L.gate_scale || !L.up_scale || !L.down_scale))
       return fail(DFLASH_ERR_INVALID_ARG, "missing fp8 scale in layer %d", l);
+    // bf16 matrices are re-blocked with 16-byte moves
+    if (cfg->weight_dtype == DFLASH_BF16 &&
+        !(aligned16(L.q) && aligned16(L.k) && aligned16(L.v) && aligned16(L.o) && aligned16(L.gate) &&
+          aligned16(L.up) && aligned16(L.down)))
+      return fail(DFLASH_ERR_INVALID_ARG, "bf16 weight matrices must start on a 16-byte boundary (layer %d)", l);
   }
+  if (cfg->weight_dtype == DFLASH_BF16 && !aligned16(w->fc))
+    return fail(DFLASH_ERR_INVALID_ARG, "bf16 weight matrices must start on a 16-byte boundary (fc)");
   const int n_sm = sm_count();
   Layout lo = make_layout(*cfg, n_sm);
   if (ws_bytes < lo.total) return fail(DFLASH_ERR_CAPACITY, "workspace %zu bytes < required %zu", ws_bytes, lo.total);
@@ -896,27 +903,42 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     auto cp = [&](size_t dst_off, const void* src, size_t bytes) {
       ck(cudaMemcpyAsync(h->ws + dst_off, src, bytes, cudaMemcpyDeviceToDevice, s), "weight copy");
     };
-    cp(lo.fc, w->fc, (size_t)H * g.n * H * ew);
+    // A matrix piece: source rows i land on logical rows base + (i / chunk) *
+    // stride + i % chunk of the [N][K] matrix at dst_off (row-major, or in
+    // 16 KB swizzled blocks for the tensor-core path).
+    const bool tc = cfg->weight_dtype == DFLASH_BF16;
+    auto mat = [&](size_t dst_off, int K, const void* src, int n_rows, int chunk, int stride, int base) {
+      if (tc) {
+        launch_repack(h->ws + dst_off, K, src, n_rows, chunk, stride, base, s);
+        ck(cudaGetLastError(), "weight repack");
+      } else if (chunk == n_rows) {
+        cp(dst_off + (size_t)base * K * ew, src, (size_t)n_rows * K * ew);
+      } else {
+        const size_t cb = (size_t)chunk * K * ew;
+        ck(cudaMemcpy2DAsync(h->ws + dst_off + (size_t)base * K * ew, (size_t)stride * K * ew, src, cb, cb,
+                             n_rows / chunk, cudaMemcpyDeviceToDevice, s),
+           "interleaved weight copy");
+      }
+    };
+    mat(lo.fc, g.n * H, w->fc, H, H, 0, 0);
     if (fp8) cp(lo.s_fc, w->fc_scale, (size_t)H * 4);
     cp(lo.hn, w->hidden_norm, (size_t)H * 4);
     cp(lo.fn, w->norm, (size_t)H * 4);
     for (int l = 0; l < L; ++l) {
       const dflash_layer_weights& W = w->layers[l];
-      const size_t qr = (size_t)Hq * d, kr = (size_t)Hkv * d;
+      const int qr = Hq * d, kr = Hkv * d;
       const size_t qkv0 = lo.qkv + (size_t)l * g.qkv_n * H * ew;
-      cp(qkv0, W.q, qr * H * ew);
-      cp(qkv0 + qr * H * ew, W.k, kr * H * ew);
-      cp(qkv0 + (qr + kr) * H * ew, W.v, kr * H * ew);
-      const size_t kv0 = lo.kvall + (size_t)l * g.kv_n * H * ew;
-      cp(kv0, W.k, kr * H * ew);
-      cp(kv0 + kr * H * ew, W.v, kr * H * ew);
-      cp(lo.o + (size_t)l * H * Hq * d * ew, W.o, (size_t)H * Hq * d * ew);
-      cp(lo.down + (size_t)l * H * I * ew, W.down, (size_t)H * I * ew);
+      mat(qkv0, H, W.q, qr, qr, 0, 0);
+      mat(qkv0, H, W.k, kr, kr, 0, qr);
+      mat(qkv0, H, W.v, kr, kr, 0, qr + kr);
+      mat(lo.kvall, H, W.k, kr, kr, 0, l * g.kv_n);
+      mat(lo.kvall, H, W.v, kr, kr, 0, l * g.kv_n + kr);
+      mat(lo.o + (size_t)l * H * Hq * d * ew, Hq * d, W.o, H, H, 0, 0);
+      mat(lo.down + (size_t)l * H * I * ew, I, W.down, H, H, 0, 0);
       // gate/up interleaved in blocks of 64 rows: [g0..63, u0..63, g64..127, u64..127, ...]
-      const size_t blk = (size_t)64 * H * ew;
       const size_t gu0 = lo.gu + (size_t)l * 2 * I * H * ew;
-      ck(cudaMemcpy2DAsync(h->ws + gu0, 2 * blk, W.gate, blk, blk, I / 64, cudaMemcpyDeviceToDevice, s), "gate copy");
-      ck(cudaMemcpy2DAsync(h->ws + gu0 + blk, 2 * blk, W.up, blk, blk, I / 64, cudaMemcpyDeviceToDevice, s), "up copy");
+      mat(gu0, H, W.gate, I, 64, 128, 0);
+      mat(gu0, H, W.up, I, 64, 128, 64);
       cp(lo.in_ln + (size_t)l * H * 4, W.input_ln, (size_t)H * 4);
       cp(lo.post_ln + (size_t)l * H * 4, W.post_ln, (size_t)H * 4);
       cp(lo.qn + (size_t)l * d * 4, W.q_norm, (size_t)d * 4);
@@ -940,15 +962,6 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     h->use_tc = cfg->weight_dtype == DFLASH_BF16;
     if (h->use_tc) {
       const uint64_t Mt2 = 2ull * lo.Mt;
-      h->wmap.resize(lo.n_sites);
-      h->wmap[0] = make_map_bf16(h->ws + lo.fc, H, (uint64_t)g.n * H, kTileN);
-      h->wmap[1] = make_map_bf16(h->ws + lo.kvall, (uint64_t)L * g.kv_n, H, kTileN);
-      for (int l = 0; l < L; ++l) {
-        h->wmap[2 + 4 * l] = make_map_bf16(h->ws + lo.qkv + (size_t)l * g.qkv_n * H * 2, g.qkv_n, H, kTileN);
-        h->wmap[3 + 4 * l] = make_map_bf16(h->ws + lo.o + (size_t)l * H * Hq * d * 2, H, (uint64_t)Hq * d, kTileN);
-        h->wmap[4 + 4 * l] = make_map_bf16(h->ws + lo.gu + (size_t)l * 2 * I * H * 2, 2ull * I, H, kTileN);
-        h->wmap[5 + 4 * l] = make_map_bf16(h->ws + lo.down + (size_t)l * H * I * 2, H, I, kTileN);
-      }
       h->xmap_taps = make_map_bf16(h->ws + lo.op_taps, Mt2, (uint64_t)g.n * H, 16);
       h->xmap_h = make_map_bf16(h->ws + lo.op_h, Mt2, H, 16);
       h->xmap_o = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, 16);
