@@ -157,6 +157,35 @@ int dflash_forward_round(dflash_t *h, int32_t n_seq, const int32_t *seq_ids,
 int dflash_forward_full(dflash_t *h, int32_t ctx, const float *taps, const float *noise_emb,
                         const int32_t *pos, float *out, void *stream);
 
+/* dflash_forward_full with its context K/V in a fixed device region compiled
+ * into the library (16 MiB per device) instead of pages of the handle's KV
+ * pool.  The pages have no counterpart of this entry point; it exists for
+ * callers that cannot allocate: when every pool page belongs to a live
+ * sequence, dflash_forward_full fails with DFLASH_ERR_CAPACITY, and more
+ * pages would take a larger workspace -- a new device allocation plus a copy
+ * of every live page.  This call uses no pool page and no buffer beyond its
+ * arguments and the handle's workspace, and allocates nothing.
+ *
+ * Arguments, layouts and results are those of dflash_forward_full; no
+ * sequence state changes.
+ *
+ * Limit: ctx + 16 rows must fit floor(16 MiB / (2 * L * Hkv * 64 * d *
+ * kv_bytes)) pages of 64 rows -- 1008 context rows for the 8-layer,
+ * 4-kv-head, head_dim-128 bf16-KV drafter; a larger ctx is rejected with
+ * DFLASH_ERR_CAPACITY before anything is launched.
+ *
+ * Set-up: the first call on a device (with that device current) looks the
+ * region's address up once (cudaGetSymbolAddress; a failure returns
+ * DFLASH_ERR_CUDA); make that first call before any stream capture.  The
+ * region is zero when the library is loaded and calls write only finite
+ * values into it (rows past the last key of a last page are read by the
+ * attention and masked, so they must stay finite).  One region serves every
+ * handle on that device in the process: calls that overlap in time (other
+ * streams, threads or handles) race on it and must be serialised by the
+ * caller. */
+int dflash_forward_full_static(dflash_t *h, int32_t ctx, const float *taps, const float *noise_emb,
+                               const int32_t *pos, float *out, void *stream);
+
 /* Drop a sequence's cache (len = 0, pages back to the pool). */
 int dflash_seq_reset(dflash_t *h, int32_t seq_id);
 

@@ -115,6 +115,11 @@ void launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 // Tensor-core projection: a.W is the weight in 16 KB blocks (see weights.cu).
 void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s);
 void launch_repack(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base, cudaStream_t s);
+
+// Fixed device region of dflash_forward_full_static (static_full.cu).
+constexpr size_t kFixedKvBytes = size_t(16) << 20;
+constexpr int kFixedMaxDevices = 64;
+cudaError_t fixed_kv_region(void** base);
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s);
 void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
                          cudaStream_t s);

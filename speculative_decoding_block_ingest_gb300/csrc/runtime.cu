@@ -246,14 +246,25 @@ struct dflash_handle {
   Geo g;
   int n_sm;
   std::vector<int64_t> len;               // committed rows per slot (slot max_seqs = internal)
-  std::vector<std::vector<int>> pages;    // page ids per slot
-  std::vector<int> free_pages;
+  std::vector<std::vector<int>> pages;    // page ids per slot (in the current KV region)
+  // A KV region: K and V^T pools of `max_pages` pages per layer, their
+  // tensor maps and free list.  `pool` lives in the workspace; `fixed` is the
+  // library's static device region used by dflash_forward_full_static.
+  struct KvRegion {
+    char* kpool = nullptr;
+    char* vpool = nullptr;
+    int max_pages = 0;
+    CUtensorMap kmap, vmap;
+    std::vector<int> free_pages;
+  };
+  KvRegion pool, fixed;
+  KvRegion* kv = &pool;                   // region the enqueued kernels use
   cudaStream_t last_stream = nullptr;
   // measurement: kernel launches issued, and (when enabled) per-kind event pairs
   int64_t launches = 0;
   // tensor maps of the tensor-core projections' operands (per buffer)
   CUtensorMap xmap_taps, xmap_h, xmap_o, xmap_a;
-  CUtensorMap qmap, kmap, vmap;                 // attention: q buffer (3-D), K pool, V^T pool
+  CUtensorMap qmap;                             // attention: q buffer (3-D)
   bool use_tc = false;
   bool prof_on = false;
   struct Rec {
@@ -324,9 +335,10 @@ bool ensure_pages(dflash_t* h, int slot, int64_t rows, InitBlob& blob, std::vect
   const int need = (int)((rows + kPage - 1) / kPage);
   auto& pl = h->pages[slot];
   while ((int)pl.size() < need) {
-    if (h->free_pages.empty() || blob.n_pt >= kMaxPtUpdates) return false;
-    const int page = h->free_pages.back();
-    h->free_pages.pop_back();
+    auto& fl = h->kv->free_pages;
+    if (fl.empty() || blob.n_pt >= kMaxPtUpdates) return false;
+    const int page = fl.back();
+    fl.pop_back();
     taken.push_back(slot);
     blob.pt_idx[blob.n_pt] = slot * h->lo.pps + (int)pl.size();
     blob.pt_page[blob.n_pt] = page;
@@ -340,7 +352,7 @@ bool ensure_pages(dflash_t* h, int slot, int64_t rows, InitBlob& blob, std::vect
 void rollback_pages(dflash_t* h, const InitBlob& blob, const std::vector<int>& taken) {
   for (int i = (int)taken.size() - 1; i >= 0; --i) {
     auto& pl = h->pages[taken[i]];
-    h->free_pages.push_back(pl.back());
+    h->kv->free_pages.push_back(pl.back());
     pl.pop_back();
   }
   (void)blob;
@@ -350,8 +362,8 @@ EpiArgs base_epi(dflash_t* h) {
   EpiArgs e{};
   e.g = h->g;
   e.rope_cs = h->at<float2>(h->lo.rope_cs);
-  e.kpool = h->at<void>(h->lo.kpool);
-  e.vpool = h->at<void>(h->lo.vpool);
+  e.kpool = h->kv->kpool;
+  e.vpool = h->kv->vpool;
   e.err = h->at<int>(h->lo.err);
   e.op_f32 = h->cfg.weight_dtype == DFLASH_F32;
   return e;
@@ -550,8 +562,8 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   fb.rope_cs = h->at<float2>(h->lo.rope_cs);
   fb.dest = h->at<RoundDesc>(h->lo.rdesc)->dest;
   fb.q_out = h->at<void>(h->lo.q);
-  fb.kpool = h->at<void>(h->lo.kpool);
-  fb.vpool = h->at<void>(h->lo.vpool);
+  fb.kpool = h->kv->kpool;
+  fb.vpool = h->kv->vpool;
   fb.g = g;
   auto prep_norm = [&](const float* gain) {
     FinishArgs f = fb;
@@ -595,8 +607,8 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     // attention over [cached ctx ; block] K/V, split over keys, then merge
     AttnArgs a{};
     a.q = h->at<void>(h->lo.q);
-    a.kpool = h->at<void>(h->lo.kpool);
-    a.vpool = h->at<void>(h->lo.vpool);
+    a.kpool = h->kv->kpool;
+    a.vpool = h->kv->vpool;
     a.layer = l;
     a.block_table = h->at<int>(h->lo.btab);
     a.rd = h->at<RoundDesc>(h->lo.rdesc);
@@ -616,7 +628,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
       for (int i = 0; i < rd.n_seq; ++i) kv_b += (double)(rd.len[i] + kBlock) * g.Hkv * g.d * 2 * ekv;
       Launch L(h, DFLASH_KERNEL_ATTENTION, kv_b + (double)n_tok * g.Hq * g.d * ekv + part_b, s);
       a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_ATTENTION, rd.n_items) : nullptr;
-      if (h->use_tc) launch_attention_tc(a, rd.n_items, &h->qmap, &h->kmap, &h->vmap, s);
+      if (h->use_tc) launch_attention_tc(a, rd.n_items, &h->qmap, &h->kv->kmap, &h->kv->vmap, s);
       else launch_attention_simt(a, rd.n_items, s);
     }
     ck(cudaGetLastError(), "attention launch");
@@ -822,9 +834,42 @@ int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos
 }
 
 void release_slot(dflash_t* h, int slot) {
-  for (int p : h->pages[slot]) h->free_pages.push_back(p);
+  for (int p : h->pages[slot]) h->kv->free_pages.push_back(p);
   h->pages[slot].clear();
   h->len[slot] = 0;
+}
+
+// Makes `r` the region the enqueued kernels use (pools, maps, free list and
+// the device geometry's pages-per-layer) until the scope ends.
+struct RegionScope {
+  dflash_t* h;
+  dflash_handle::KvRegion* prev;
+  int prev_pages;
+  RegionScope(dflash_t* h_, dflash_handle::KvRegion* r) : h(h_), prev(h_->kv), prev_pages(h_->g.max_pages) {
+    h->kv = r;
+    h->g.max_pages = r->max_pages;
+  }
+  ~RegionScope() {
+    h->kv = prev;
+    h->g.max_pages = prev_pages;
+  }
+};
+
+// Ingest ctx rows into the internal slot in max_ingest_rows chunks, run the
+// block forward, release the slot (the body of both first-light entries).
+int first_light(dflash_t* h, int32_t ctx, const float* taps, const float* noise_emb, const int32_t* pos,
+                float* out, cudaStream_t s) {
+  const int slot = h->cfg.max_seqs;
+  int rc = DFLASH_OK;
+  const int chunk = h->cfg.max_ingest_rows;
+  const size_t width = (size_t)h->g.n * h->g.H;
+  for (int r0 = 0; r0 < ctx && rc == DFLASH_OK; r0 += chunk) {
+    const int t = std::min(chunk, ctx - r0);
+    rc = ingest_slots(h, 1, &slot, &t, pos + r0, taps + (size_t)r0 * width, s);
+  }
+  if (rc == DFLASH_OK) rc = round_slots(h, 1, &slot, pos + ctx, noise_emb, out, s);
+  release_slot(h, slot);
+  return rc;
 }
 
 }  // namespace
@@ -894,8 +939,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   rope_table(*cfg, inv, g.mscale);
   h->len.assign(cfg->max_seqs + 1, 0);
   h->pages.assign(cfg->max_seqs + 1, {});
-  h->free_pages.resize(cfg->max_pages);
-  for (int i = 0; i < cfg->max_pages; ++i) h->free_pages[i] = cfg->max_pages - 1 - i;
+  h->pool.kpool = h->ws + lo.kpool;
+  h->pool.vpool = h->ws + lo.vpool;
+  h->pool.max_pages = cfg->max_pages;
+  h->pool.free_pages.resize(cfg->max_pages);
+  for (int i = 0; i < cfg->max_pages; ++i) h->pool.free_pages[i] = cfg->max_pages - 1 - i;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = guarded([&]() -> int {
@@ -969,8 +1017,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
 
       const uint64_t pool_rows = (uint64_t)L * cfg->max_pages * Hkv;
-      h->kmap = make_map_bf16(h->ws + lo.kpool, pool_rows * kPage, d, kPage);
-      h->vmap = make_map_bf16(h->ws + lo.vpool, pool_rows * d, kPage, d);
+      h->pool.kmap = make_map_bf16(h->ws + lo.kpool, pool_rows * kPage, d, kPage);
+      h->pool.vmap = make_map_bf16(h->ws + lo.vpool, pool_rows * d, kPage, d);
     }
     // stale pool rows are read (and masked) by the attention MMA: keep them finite
     ck(cudaMemsetAsync(h->ws + lo.kpool, 0, lo.vpool - lo.kpool, s), "K pool clear");
@@ -1027,20 +1075,53 @@ int dflash_forward_full(dflash_t* h, int32_t ctx, const float* taps, const float
     return fail(DFLASH_ERR_INVALID_ARG, "taps / noise_emb / out must start on a 16-byte boundary");
   if (ctx + kBlock > h->cfg.max_seq_len) return fail(DFLASH_ERR_CAPACITY, "ctx exceeds max_seq_len");
   const int need = (ctx + kBlock + kPage - 1) / kPage;
-  if ((int)h->free_pages.size() < need) return fail(DFLASH_ERR_CAPACITY, "out of KV pages");
+  if ((int)h->kv->free_pages.size() < need) return fail(DFLASH_ERR_CAPACITY, "out of KV pages");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int slot = h->cfg.max_seqs;
-  release_slot(h, slot);
-  int rc = DFLASH_OK;
-  const int chunk = h->cfg.max_ingest_rows;
-  const size_t width = (size_t)h->g.n * h->g.H;
-  for (int r0 = 0; r0 < ctx && rc == DFLASH_OK; r0 += chunk) {
-    const int t = std::min(chunk, ctx - r0);
-    rc = ingest_slots(h, 1, &slot, &t, pos + r0, taps + (size_t)r0 * width, s);
+  release_slot(h, h->cfg.max_seqs);
+  return first_light(h, ctx, taps, noise_emb, pos, out, s);
+}
+
+int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, const float* noise_emb,
+                               const int32_t* pos, float* out, void* stream) {
+  g_last_error.clear();
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
+  if (ctx < 0) return fail(DFLASH_ERR_INVALID_ARG, "negative ctx");
+  if (!pos || !noise_emb || !out || (ctx > 0 && !taps)) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  if (!aligned16(noise_emb) || !aligned16(out) || (ctx > 0 && !aligned16(taps)))
+    return fail(DFLASH_ERR_INVALID_ARG, "taps / noise_emb / out must start on a 16-byte boundary");
+  if (ctx + kBlock > h->cfg.max_seq_len) return fail(DFLASH_ERR_CAPACITY, "ctx exceeds max_seq_len");
+  // one page of K (or V^T) for every layer
+  const size_t page_bytes = (size_t)h->g.L * h->g.Hkv * kPage * h->g.d * esize_kv(h->cfg.kv_dtype);
+  const int fixed_pages = (int)(kFixedKvBytes / (2 * page_bytes));
+  const int need = (ctx + kBlock + kPage - 1) / kPage;
+  if (need > fixed_pages)
+    return fail(DFLASH_ERR_CAPACITY, "ctx %d exceeds the static KV region (at most %d context rows for this drafter)",
+                ctx, std::max(0, fixed_pages * kPage - kBlock));
+  if (!h->fixed.kpool) {
+    void* base = nullptr;
+    const cudaError_t e = fixed_kv_region(&base);
+    if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "static KV region lookup: %s", cudaGetErrorString(e));
+    const int rc = guarded([&]() -> int {
+      dflash_handle::KvRegion r;
+      r.kpool = static_cast<char*>(base);
+      r.vpool = r.kpool + (size_t)fixed_pages * page_bytes;
+      r.max_pages = fixed_pages;
+      if (h->use_tc) {
+        const uint64_t rows = (uint64_t)h->g.L * fixed_pages * h->g.Hkv;
+        r.kmap = make_map_bf16(r.kpool, rows * kPage, h->g.d, kPage);
+        r.vmap = make_map_bf16(r.vpool, rows * h->g.d, kPage, h->g.d);
+      }
+      h->fixed = std::move(r);
+      return DFLASH_OK;
+    });
+    if (rc != DFLASH_OK) return rc;
   }
-  if (rc == DFLASH_OK) rc = round_slots(h, 1, &slot, pos + ctx, noise_emb, out, s);
-  release_slot(h, slot);
-  return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  release_slot(h, h->cfg.max_seqs);   // pool pages, if any were left
+  h->fixed.free_pages.resize(h->fixed.max_pages);
+  for (int i = 0; i < h->fixed.max_pages; ++i) h->fixed.free_pages[i] = h->fixed.max_pages - 1 - i;
+  RegionScope scope(h, &h->fixed);
+  return first_light(h, ctx, taps, noise_emb, pos, out, s);
 }
 
 int dflash_seq_reset(dflash_t* h, int32_t seq_id) {

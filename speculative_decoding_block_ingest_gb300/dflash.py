@@ -24,7 +24,7 @@ ROPE_PLAIN, ROPE_YARN = 0, 1
 _DT = {"f32": F32, "bf16": BF16, "fp8": FP8}
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dflash_forward_round",
-           "dflash_forward_full", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
+           "dflash_forward_full", "dflash_forward_full_static", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
            "dflash_device_status", "dflash_destroy", "dflash_last_error", "dflash_profile_enable",
            "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches")
 TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_ingest_ctx.argtypes = [vp, i32, p32, p32, p32, vp, vp]
     lib.dflash_forward_round.argtypes = [vp, i32, p32, p32, vp, vp, vp]
     lib.dflash_forward_full.argtypes = [vp, i32, vp, vp, p32, vp, vp]
+    lib.dflash_forward_full_static.argtypes = [vp, i32, vp, vp, p32, vp, vp]
     lib.dflash_seq_reset.argtypes = [vp, i32]
     lib.dflash_seq_len.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.dflash_kv_read.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
@@ -210,6 +211,18 @@ class Drafter:
         _check(self.lib.dflash_forward_full(self.handle, ctx, ctypes.c_void_p(taps.data_ptr()),
                                             ctypes.c_void_p(noise.data_ptr()), _i32(pos),
                                             ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
+        return out
+
+    def forward_full_static(self, taps: torch.Tensor, noise: torch.Tensor, pos: Sequence[int],
+                            out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+        """forward_full with the context K/V in the library's fixed device
+        region (no KV-pool pages; see dflash_forward_full_static)."""
+        if out is None:
+            out = torch.empty_like(noise)
+        ctx = taps.shape[0]
+        _check(self.lib.dflash_forward_full_static(self.handle, ctx, ctypes.c_void_p(taps.data_ptr()),
+                                                   ctypes.c_void_p(noise.data_ptr()), _i32(pos),
+                                                   ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
         return out
 
     def seq_reset(self, seq_id: int):
