@@ -23,6 +23,7 @@ value sums all ranks' rounds over the slowest rank's time.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -47,6 +48,24 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-rounds", type=int, default=3)
     return p.parse_args()
+
+
+def gemm_traffic(workload: str):
+    """Per-launch DRAM bytes of the projection kernel from the committed ncu
+    record, or None when that record is for another workload or the kernel's
+    sources have changed since it was taken."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
+                        f"gemm_tc_traffic_{workload}.json")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256()
+        for f in rec["sources"]:
+            h.update(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), f), "rb").read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return rec["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
 
 
 def peaks():
@@ -297,7 +316,7 @@ def main():
     peak, peak_kind = peaks()
     achieved = (g_b / 1e9) / (g_ms / 1e3) if g_ms > 0 else 0.0
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": None, "kernel": "gemm_swapab (all projections)",
+                "frac": achieved / peak, "traffic": gemm_traffic(wl.name), "kernel": "gemm_swapab (all projections)",
                 "launches": g_n, "bytes_per_launch": g_b / max(g_n, 1), "peak_source": peak_kind}
     breakdown = {k: {"launches": n, "ms_per_step": m / K, "GB/s": (b / 1e9) / (m / 1e3) if m else None}
                  for k, (n, m, b) in prof.items()}
