@@ -226,6 +226,39 @@ __device__ __forceinline__ void cp_async_wait(int n) {
   else asm volatile("cp.async.wait_group 2;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ cross-CTA counters
+// A producer publishes data with its ordinary stores, then fence_publish()
+// (every writing thread), a CTA barrier, and one counter_add(); a consumer
+// waits with counter_wait() and then reads.  When the consumer reads through
+// the async proxy (TMA), both sides also order the generic and async proxies.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void fence_publish() {
+  fence_proxy_async_global();
+  __threadfence();
+}
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void counter_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Wait until *p >= target; false if `abort` or `*err` was raised or the time
+// limit passed.
+__device__ __forceinline__ bool counter_wait(const unsigned* p, unsigned target, volatile int* abort,
+                                             const int* err) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    if (ld_acquire_u32(p) >= target) return true;
+    if (*abort || *reinterpret_cast<const volatile int*>(err)) return false;
+    if (globaltimer() - t0 > kWaitNs) return false;
+  }
+}
+
 // ------------------------------------------------------------------ programmatic dependent launch
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }

@@ -9,6 +9,7 @@
 // parameter, so no host-to-device copy and no host synchronisation happen on
 // the round's path.
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -60,8 +61,11 @@ struct Layout {
   size_t kpool, vpool, btab, inv_freq;
   size_t h, op_h, op_taps, op_o, op_a, q, qkv_acc, gu_acc, ss;
   size_t gacc, rope_cs, counters, apart_o, apart_ml, rdesc, idesc, err;
+  size_t mkcnt;                                         // persistent round: two counter sets
   size_t total;
   int Mt, pps, max_tiles, grid_max, items_cap, n_sites;
+  MkCounters mk;
+  int mk_words, mk_batch;                               // words per counter set; sequences per round
 };
 
 int sm_count() {
@@ -131,6 +135,24 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.rdesc = take(sizeof(RoundDesc));
   Lo.idesc = take(sizeof(IngestDesc));
   Lo.err = take(256);
+  {
+    const int qkv_tiles = (int)(qkv_n / kTileN), gu_tiles = (int)(2 * I / kTileN);
+    Lo.mk_batch = std::min(c.max_batch, kMkMaxTok / kBlock);
+    MkCounters& m = Lo.mk;
+    m.x_h = 0;
+    m.qkv_t = 1;
+    m.head = m.qkv_t + qkv_tiles;
+    m.att = m.head + (int)Hkv;
+    m.comb = m.att + Lo.mk_batch * (int)Hkv;
+    m.o_done = m.comb + 1;
+    m.x2 = m.o_done + 1;
+    m.gu_t = m.x2 + 1;
+    m.act = m.gu_t + gu_tiles;
+    m.down_done = m.act + gu_tiles;
+    m.per_layer = m.down_done + 1;
+    Lo.mk_words = (int)L * m.per_layer;
+    Lo.mkcnt = take((size_t)2 * Lo.mk_words * 4);
+  }
   Lo.total = off;
   return Lo;
 }
@@ -267,6 +289,10 @@ struct dflash_handle {
   CUtensorMap qmap;                             // attention: q buffer (3-D)
   bool use_tc = false;
   bool prof_on = false;
+  // persistent round kernel: only with DFLASH_ROUND_PATH=persistent at
+  // create; rounds alternate between the two counter sets
+  bool mk_off = false;
+  int mk_parity = 0;
   struct Rec {
     int kind;
     cudaEvent_t a, b;
@@ -505,11 +531,101 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   run_gemm(h, kv, s);
 }
 
+// The persistent round takes bf16 rounds of up to kMkMaxTok block rows whose
+// projection stage fits at least two ring stages beside the attention buffers.
+bool mk_eligible(dflash_t* h, int n_tok) {
+  return h->use_tc && !h->mk_off && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
+         round_mk_stages((n_tok + 15) / 16 * 16, h->g.d) >= 2;
+}
+
 int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens) {
   long units = 0;
   for (auto L : lens) units += (long)h->g.Hkv * ((L + kBlock + kPage - 1) / kPage);
-  const long target = h->use_tc ? (long)h->n_sm : 2L * h->n_sm;
+  // the persistent round runs one item per CTA: at most n_sm items even after
+  // each (sequence, kv head) rounds its split count up
+  const bool mk = mk_eligible(h, (int)lens.size() * kBlock);
+  const long target = mk ? std::max<long>(1, (long)h->n_sm - (long)h->g.Hkv * (long)lens.size())
+                         : (h->use_tc ? (long)h->n_sm : 2L * h->n_sm);
   return (int)std::max<long>(1, (units + target - 1) / target);
+}
+
+// The whole round (after the per-call init) as one persistent kernel.
+void enqueue_round_mk(dflash_t* h, const RoundDesc& rd, float* out, cudaStream_t s) {
+  const Geo& g = h->g;
+  const Layout& lo = h->lo;
+  const int n_tok = rd.n_tok;
+  MkArgs a{};
+  a.g = g;
+  a.n_tok = n_tok;
+  a.nt = (n_tok + 15) / 16 * 16;
+  a.aw = 2 * a.nt;
+  a.stages = round_mk_stages(a.nt, g.d);
+  a.stage_bytes = kTileN * kTileK * 2 + 2 * a.nt * 128;
+  a.n_items = rd.n_items;
+  a.datoms = g.d / 64;
+  a.kv_stage_bytes = a.datoms * 64 * 128 + g.d * 128;
+  a.x_lo_row = lo.Mt;
+  const int grid = h->n_sm;
+  auto part = [&](int n_rows, int K) {
+    const int kb = K / kTileK;
+    return Part{n_rows / kTileN * kb, grid, kb};
+  };
+  a.pq = part(g.qkv_n, g.H);
+  a.po = part(g.H, g.Hq * g.d);
+  a.pg = part(2 * g.I, g.H);
+  a.pd = part(g.H, g.I);
+  a.wq = h->at<uint8_t>(lo.qkv);
+  a.wo = h->at<uint8_t>(lo.o);
+  a.wg = h->at<uint8_t>(lo.gu);
+  a.wd = h->at<uint8_t>(lo.down);
+  a.wq_l = (size_t)g.qkv_n * g.H * 2;
+  a.wo_l = (size_t)g.H * g.Hq * g.d * 2;
+  a.wg_l = (size_t)2 * g.I * g.H * 2;
+  a.wd_l = (size_t)g.H * g.I * 2;
+  a.in_ln = h->at<float>(lo.in_ln);
+  a.post_ln = h->at<float>(lo.post_ln);
+  a.qn = h->at<float>(lo.qn);
+  a.kn = h->at<float>(lo.kn);
+  a.fn = h->at<float>(lo.fn);
+  a.h = h->at<float>(lo.h);
+  a.qkv_acc = h->at<float>(lo.qkv_acc);
+  a.gu_acc = h->at<float>(lo.gu_acc);
+  a.out = out;
+  a.op_h = h->at<void>(lo.op_h);
+  a.op_o = h->at<void>(lo.op_o);
+  a.op_a = h->at<void>(lo.op_a);
+  a.plane_h = (long)lo.Mt * g.H;
+  a.plane_o = (long)lo.Mt * g.Hq * g.d;
+  a.plane_a = (long)lo.Mt * g.I;
+  a.q = h->at<void>(lo.q);
+  a.kpool = h->kv->kpool;
+  a.vpool = h->kv->vpool;
+  a.btab = h->at<int>(lo.btab);
+  a.rd = h->at<RoundDesc>(lo.rdesc);
+  a.rope_cs = h->at<float2>(lo.rope_cs);
+  a.part_o = h->at<float>(lo.apart_o);
+  a.part_ml = h->at<float>(lo.apart_ml);
+  unsigned* sets = h->at<unsigned>(lo.mkcnt);
+  a.cnt = sets + (size_t)h->mk_parity * lo.mk_words;
+  a.cnt_next = sets + (size_t)(1 - h->mk_parity) * lo.mk_words;
+  a.cnt_words = lo.mk_words;
+  a.c = lo.mk;
+  a.err = h->at<int>(lo.err);
+  a.scale_log2 = 1.4426950408889634f / std::sqrt((float)g.d);
+  // algorithmic bytes: every weight once, every cached K/V row once, the
+  // block rows in and out
+  double bytes = (double)g.L * (a.wq_l + a.wo_l + a.wg_l + a.wd_l);
+  for (int i = 0; i < rd.n_seq; ++i)
+    bytes += (double)(rd.len[i] + kBlock) * g.L * g.Hkv * g.d * 2.0 * esize_kv(g.kvtype);
+  bytes += (double)n_tok * g.H * 8;
+  // a trace record of kMkTraceWords per CTA spans kMkTraceWords / kTraceWords slots
+  a.trace = trace_slot(h, DFLASH_KERNEL_ROUND, grid * (kMkTraceWords / kTraceWords));
+  {
+    Launch L(h, DFLASH_KERNEL_ROUND, bytes, s);
+    ck(launch_round_mk(a, grid, &h->xmap_h, &h->xmap_o, &h->xmap_a, &h->qmap, &h->kv->kmap, &h->kv->vmap, s),
+       "persistent round launch");
+  }
+  h->mk_parity ^= 1;
 }
 
 // The round: per layer
@@ -554,6 +670,11 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     launch_init(ia, blob, s);
   }
   ck(cudaGetLastError(), "round init launch");
+
+  if (mk_eligible(h, n_tok) && rd.n_items <= h->n_sm) {
+    enqueue_round_mk(h, rd, out, s);
+    return;
+  }
 
   FinishArgs fb{};
   fb.n_tok = n_tok;
@@ -1008,6 +1129,12 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     }
     ck(cudaMemcpyAsync(h->ws + lo.inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s), "rope table");
     h->use_tc = cfg->weight_dtype == DFLASH_BF16;
+    {
+      // "persistent": the whole round in one kernel (round_mk.cu); by default
+      // one kernel per step, which measured faster at the 8-layer shape
+      const char* path = std::getenv("DFLASH_ROUND_PATH");
+      h->mk_off = !(path && std::string(path) == "persistent");
+    }
     if (h->use_tc) {
       const uint64_t Mt2 = 2ull * lo.Mt;
       h->xmap_taps = make_map_bf16(h->ws + lo.op_taps, Mt2, (uint64_t)g.n * H, 16);
@@ -1024,6 +1151,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     ck(cudaMemsetAsync(h->ws + lo.kpool, 0, lo.vpool - lo.kpool, s), "K pool clear");
     ck(cudaMemsetAsync(h->ws + lo.vpool, 0, lo.btab - lo.vpool, s), "V pool clear");
     ck(cudaMemsetAsync(h->ws + lo.btab, 0xff, (size_t)(cfg->max_seqs + 1) * lo.pps * 4, s), "block table");
+    ck(cudaMemsetAsync(h->ws + lo.mkcnt, 0, (size_t)2 * lo.mk_words * 4, s), "round counters");
     ck(cudaMemsetAsync(h->ws + lo.counters, 0, (size_t)lo.n_sites * lo.max_tiles * 4, s), "counters");
     ck(cudaMemsetAsync(h->ws + lo.gacc, 0, (size_t)lo.max_tiles * kTileN * kPassTok * 4, s), "tile accumulators");
     ck(cudaMemsetAsync(h->ws + lo.qkv_acc, 0, (size_t)lo.Mt * g.qkv_n * 4, s), "QKV accumulator");

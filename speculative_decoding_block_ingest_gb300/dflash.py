@@ -28,7 +28,7 @@ EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dfla
            "dflash_device_status", "dflash_destroy", "dflash_last_error", "dflash_profile_enable",
            "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches")
 TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
-KERNEL_KINDS = ("gemm", "attention", "combine", "init", "norm", "finish")
+KERNEL_KINDS = ("gemm", "attention", "combine", "init", "norm", "finish", "round")
 
 
 class Config(ctypes.Structure):
