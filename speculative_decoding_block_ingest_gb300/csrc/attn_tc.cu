@@ -4,17 +4,24 @@
 // One CTA per work item (sequence, kv head, split of the keys [cached context
 // ; 16 block rows]).  The G q-heads x 16 block rows that share a kv head form
 // one M = 128 query tile (rows padded with zeros when G*16 < 128), so each
-// K/V page is read once per item:
+// K/V page is read once per item.  Keys go in chunks of two pages (128 keys):
+// one S tile per chunk halves the serial S -> softmax -> P V^T steps of a
+// split.
 //   warp 0 (one lane)  TMA: the query tile, then the split's K pages [64 x d]
-//                      and V^T pages [d x 64] through a ring of stages;
-//   warp 1 (one lane)  tcgen05.mma: S = Q K^T into one of two TMEM buffers,
-//                      then O += P V^T into the TMEM output accumulator;
-//   warps 2..5         softmax, one thread per query row: scores from TMEM,
-//                      exp2 with a running max, P (bf16) into one of two
-//                      shared-memory buffers in the 128-byte swizzle the MMA
-//                      reads, so page j+1's softmax overlaps page j's P V^T.  O is rescaled only
-//                      when a row's max grows by more than 2^8 (exact: the
-//                      final division uses the same max).
+//                      and V^T pages [d x 64] into a ring of two chunk stages
+//                      (a chunk's two K pages stacked to one 128-key
+//                      operand);
+//   warp 1 (one lane)  tcgen05.mma: S = Q K^T (N = 128) into one of two TMEM
+//                      buffers, then O += P V^T into the TMEM accumulator;
+//   warps 2..9         softmax, two threads per query row (warps 2..5 the
+//                      chunk's first 64 keys, warps 6..9 the other 64; the
+//                      two halves trade their maxima through TMEM): scores
+//                      from TMEM, exp2 with a running max, P (bf16) into one
+//                      of two shared-memory buffers in the 128-byte swizzle
+//                      the MMA reads, so chunk c+1's softmax overlaps chunk
+//                      c's P V^T.  O is rescaled only when a row's max grows
+//                      by more than 2^8 (exact: the final division uses the
+//                      same max); each half rescales half of O's columns.
 // Each item writes its unnormalised O with (max, sum); the combine kernel
 // merges the splits (all in log2 units).
 #include <algorithm>
@@ -27,16 +34,20 @@ namespace dfl {
 
 struct AttnTcCfg {
   int datoms;        // d / 64 (K-atoms of a row)
-  int stages;
-  int stage_bytes;   // K page (datoms x 8 KB) + V^T page (d x 128 B)
-  uint32_t idesc_s;  // M=128, N=64
+  int stages;        // chunk stages
+  int stage_bytes;   // datoms x 16 KB of K (two pages stacked) + 2 x V^T page (d x 128 B)
+  uint32_t idesc_s;  // M=128, N=128
   uint32_t idesc_o;  // M=128, N=d
   float scale_log2;  // log2(e) / sqrt(d)
 };
 
-constexpr int kAttnThreads = 192;
+constexpr int kAttnThreads = 320;
+constexpr int kSmThreads = 256;          // softmax warps 2..9
+constexpr int kSmBar = 3;                // their named barrier
 constexpr int kQAtomBytes = 128 * 128;   // 128 rows x 128 B
-constexpr int kKAtomBytes = 64 * 128;    // 64 keys x 128 B
+constexpr int kKAtomBytes = 64 * 128;    // 64 keys x 128 B (one page of one K-atom)
+constexpr int kChunk = 2 * kPage;        // keys per S tile
+constexpr int kPBytes = 2 * kQAtomBytes; // P tile: 128 rows x 128 keys bf16 (two atoms)
 constexpr float kRescaleLog2 = 8.f;
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -46,8 +57,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Geo& g = a.g;
   uint8_t* sQ = smem;                                   // datoms x 16 KB
-  uint8_t* sP = sQ + t.datoms * kQAtomBytes;            // 2 x 16 KB (P of pages j, j+1)
-  uint8_t* sKV = sP + 2 * kQAtomBytes;                  // stages x stage_bytes
+  uint8_t* sP = sQ + t.datoms * kQAtomBytes;            // 2 x 32 KB (P of chunks c, c+1)
+  uint8_t* sKV = sP + 2 * kPBytes;                      // stages x stage_bytes
   uint8_t* ctl = sKV + t.stages * t.stage_bytes;
   uint64_t* kvfull = reinterpret_cast<uint64_t*>(ctl);
   uint64_t* kvempty = kvfull + t.stages;
@@ -68,6 +79,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     c0 = c0_shared;
   }
   const int R = g.G * kBlock;
+  const uint32_t vbytes = (uint32_t)g.d * 128;          // one V^T page
   // zero the query tile's padding rows (the MMA reads all 128 rows)
   for (int idx = threadIdx.x; idx < t.datoms * (128 - R) * 32; idx += kAttnThreads) {
     const int atom = idx / ((128 - R) * 32), rem = idx % ((128 - R) * 32);
@@ -83,7 +95,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     mbar_init(&sfull[1], 1);
     mbar_init(qfull, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&pfull[b], kEpiThreads);
+      mbar_init(&pfull[b], kSmThreads);
       mbar_init(&pvdone[b], 1);
     }
     flags[0] = 0;
@@ -92,12 +104,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tma_prefetch_map(&tmK);
     tma_prefetch_map(&tmV);
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 256);
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncwarp();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = *tmem_slot;                     // O: cols [0, d); S buffers at 128 and 256
   if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 1, c0);  // 1: set-up done
 
   // The descriptor, the page table and the cached-context pages were written
@@ -109,15 +121,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   int s, kvh, k0, k1;
   attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1);
   const int n_pages = (k1 - k0 + kPage - 1) / kPage;
-  const int n_all = n_pages;
+  const int n_chunks = (n_pages + 1) / 2;
   const int slot = a.rd->seq_slot[s];
   const int len = a.rd->len[s];
+  auto pages_in = [&](int c) { return min(2, n_pages - 2 * c); };
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- TMA producer
+      // page j of the split goes to chunk stage (j/2) % stages, K rows
+      // [64*(j&1), +64) of each K-atom and V^T slot j&1
       auto load_page = [&](int j) -> bool {
-        const int st = j % t.stages;
+        const int st = (j >> 1) % t.stages, w = j & 1;
         const int page = a.block_table[(long)slot * g.pages_per_seq + k0 / kPage + j];
         if (page < 0 || page >= g.max_pages) {
           atomicExch(a.err, DERR_BAD_PAGE);
@@ -125,29 +140,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         const long base = ((long)a.layer * g.max_pages + page) * g.Hkv + kvh;
         uint8_t* st_k = sKV + st * t.stage_bytes;
-        uint8_t* st_v = st_k + t.datoms * kKAtomBytes;
-        mbar_arrive_expect_tx(&kvfull[st], (uint32_t)t.stage_bytes);
+        uint8_t* st_v = st_k + t.datoms * kQAtomBytes;
         for (int at = 0; at < t.datoms; ++at)
-          tma_load_2d(st_k + at * kKAtomBytes, &tmK, &kvfull[st], at * 64, (int)(base * kPage));
-        tma_load_2d(st_v, &tmV, &kvfull[st], 0, (int)(base * g.d));
+          tma_load_2d(st_k + at * kQAtomBytes + w * kKAtomBytes, &tmK, &kvfull[st], at * 64, (int)(base * kPage));
+        tma_load_2d(st_v + w * vbytes, &tmV, &kvfull[st], 0, (int)(base * g.d));
         return true;
       };
+      auto chunk_bytes = [&](int c) { return (uint32_t)(pages_in(c) * (t.datoms * kKAtomBytes + (int)vbytes)); };
       bool ok = true;
-      int j = 0;
-      // context-only pages that fit the ring, before the launch wait
-      for (; ok && j < n_pages && j < t.stages && k0 + (j + 1) * kPage <= len; ++j) ok = load_page(j);
+      int deferred[2 * 4];
+      int nd = 0;
+      // the first chunk stages are free: announce them and fetch their
+      // context-only pages before the launch wait
+      const int pre = min(n_chunks, t.stages);
+      for (int c = 0; c < pre; ++c) {
+        mbar_arrive_expect_tx(&kvfull[c], chunk_bytes(c));
+        for (int w = 0; w < pages_in(c); ++w) {
+          const int j = 2 * c + w;
+          if (k0 + (j + 1) * kPage <= len) ok = ok && load_page(j);
+          else deferred[nd++] = j;
+        }
+      }
       pdl_wait();
       pdl_launch_dependents();
       mbar_arrive_expect_tx(qfull, (uint32_t)(t.datoms * R * 128));
       for (int at = 0; at < t.datoms; ++at)
         tma_load_3d(sQ + at * kQAtomBytes, &tmQ, qfull, at * 64, kvh * g.G, s * kBlock);
-      for (; ok && j < n_pages; ++j) {
-        const int st = j % t.stages;
-        if (j >= t.stages && !mbar_wait(&kvempty[st], ((j / t.stages) & 1) ^ 1, &flags[0])) {
+      for (int i = 0; i < nd && ok; ++i) ok = load_page(deferred[i]);
+      for (int c = pre; c < n_chunks && ok; ++c) {
+        const int st = c % t.stages;
+        if (!mbar_wait(&kvempty[st], ((c / t.stages) & 1) ^ 1, &flags[0])) {
           ok = false;
           break;
         }
-        ok = load_page(j);
+        mbar_arrive_expect_tx(&kvfull[st], chunk_bytes(c));
+        for (int w = 0; w < pages_in(c) && ok; ++w) ok = load_page(2 * c + w);
       }
       if (!ok) flags[0] = 1;
     }
@@ -158,39 +185,41 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       trace_mark(a.trace, blockIdx.x, 2, c0);                   // 2: query tile ready
       const uint32_t q_addr = smem_u32(sQ);
-      auto kv_addr = [&](int j) -> uint32_t { return smem_u32(sKV + (j % t.stages) * t.stage_bytes); };
-      auto issue_s = [&](int j) -> bool {
-        if (!mbar_wait(&kvfull[j % t.stages], (j / t.stages) & 1, &flags[0])) return false;
+      auto kv_addr = [&](int c) -> uint32_t { return smem_u32(sKV + (c % t.stages) * t.stage_bytes); };
+      auto issue_s = [&](int c) -> bool {
+        if (!mbar_wait(&kvfull[c % t.stages], (c / t.stages) & 1, &flags[0])) return false;
         tc_fence_after();
-        const uint32_t k_addr = kv_addr(j);
-        const uint32_t d_s = tmem + 128u + (uint32_t)((j & 1) * 64);
+        const uint32_t k_addr = kv_addr(c);
+        const uint32_t d_s = tmem + 128u + (uint32_t)((c & 1) * kChunk);
         for (int kk = 0; kk < 4 * t.datoms; ++kk) {
           const int at = kk >> 2;
           const uint64_t adv = (uint64_t)((kk & 3) * 32) >> 4;
-          mma_bf16(d_s, desc_sw128(q_addr + at * kQAtomBytes) + adv, desc_sw128(k_addr + at * kKAtomBytes) + adv,
+          mma_bf16(d_s, desc_sw128(q_addr + at * kQAtomBytes) + adv, desc_sw128(k_addr + at * kQAtomBytes) + adv,
                    t.idesc_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&sfull[j & 1]);
+        mma_commit(&sfull[c & 1]);
         return true;
       };
-      if (ok && n_all > 0) ok = issue_s(0);
-      if (ok && n_all > 1) ok = issue_s(1);
-      for (int j = 0; j < n_all && ok; ++j) {
-        if (!mbar_wait(&pfull[j & 1], (j >> 1) & 1, &flags[0])) {
+      if (ok && n_chunks > 0) ok = issue_s(0);
+      if (ok && n_chunks > 1) ok = issue_s(1);
+      for (int c = 0; c < n_chunks && ok; ++c) {
+        if (!mbar_wait(&pfull[c & 1], (c >> 1) & 1, &flags[0])) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(sP + (j & 1) * kQAtomBytes);
-        const uint32_t v_addr = kv_addr(j) + (uint32_t)(t.datoms * kKAtomBytes);
-#pragma unroll
-        for (int kk = 0; kk < kPage / 16; ++kk) {
-          const uint64_t adv = (uint64_t)(kk * 32) >> 4;
-          mma_bf16(tmem, desc_sw128(p_addr) + adv, desc_sw128(v_addr) + adv, t.idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+        const uint32_t p_addr = smem_u32(sP + (c & 1) * kPBytes);
+        const uint32_t v_addr = kv_addr(c) + (uint32_t)(t.datoms * kQAtomBytes);
+        const int steps = pages_in(c) * (kPage / 16);   // 16 keys per MMA; a missing second page is skipped
+        for (int kk = 0; kk < steps; ++kk) {
+          const int pa = kk >> 2;                        // page (P atom / V^T slot) of this K-step
+          const uint64_t adv = (uint64_t)((kk & 3) * 32) >> 4;
+          mma_bf16(tmem, desc_sw128(p_addr + pa * kQAtomBytes) + adv, desc_sw128(v_addr + pa * vbytes) + adv,
+                   t.idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&pvdone[j & 1]);
-        mma_commit(&kvempty[j % t.stages]);
-        if (j + 2 < n_all) ok = issue_s(j + 2);
+        mma_commit(&pvdone[c & 1]);
+        mma_commit(&kvempty[c % t.stages]);
+        if (c + 2 < n_chunks) ok = issue_s(c + 2);
       }
       if (!ok) flags[0] = 1;
       trace_mark(a.trace, blockIdx.x, 3, c0);                   // 3: last MMA issued
@@ -199,98 +228,122 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     // ------------------------------------------------------------------ softmax warps
     pdl_wait();
     const int q = warp & 3;
+    const int hg = (warp - 2) >> 2;              // key half of every chunk (and half of O's columns)
     const int r = 32 * q + lane;                 // query row of this thread
     const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-    float m_run = -INFINITY, l_run = 0.f;
+    const uint32_t xcol = tmem + lane_base + 384u;   // exchange columns: [c&1][half] maxima, then [half] sums
+    const int ocols = g.d / 2;                   // O columns this half rescales / writes
+    float m_run = -INFINITY, l_run = 0.f;        // l_run: this half's share of the row sum
     bool ok = true;
-    for (int j = 0; j < n_all; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&sfull[j & 1], (j >> 1) & 1, &flags[0]))) {
-        ok = false;
-        break;
-      }
+    auto sm_sync = [&]() { asm volatile("barrier.sync %0, %1;" ::"r"(kSmBar), "r"(kSmThreads) : "memory"); };
+    for (int c = 0; c < n_chunks; ++c) {
+      // a failed wait still reaches every barrier below (skipping the work)
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&sfull[c & 1], (c >> 1) & 1, &flags[0]));
+      if (!got) ok = false;
       __syncwarp();
       tc_fence_after();
       float sc[kPage];
-      tmem_ld32(tmem + lane_base + 128u + (uint32_t)((j & 1) * 64), sc);
-      tmem_ld32(tmem + lane_base + 128u + (uint32_t)((j & 1) * 64) + 32u, sc + 32);
-      const int kc = min(kPage, k1 - (k0 + j * kPage));
-      float mj = -INFINITY;
+      const uint32_t sbase = tmem + lane_base + 128u + (uint32_t)((c & 1) * kChunk + hg * kPage);
+      const int kc = min(kPage, k1 - (k0 + c * kChunk + hg * kPage));   // valid keys of this half (may be <= 0)
+      float mh = -INFINITY;
+      if (ok) {
+        tmem_ld32(sbase, sc);
+        tmem_ld32(sbase + 32u, sc + 32);
 #pragma unroll
-      for (int i = 0; i < kPage; ++i) {
-        sc[i] = (i < kc) ? sc[i] * t.scale_log2 : -INFINITY;
-        mj = fmaxf(mj, sc[i]);
+        for (int i = 0; i < kPage; ++i) {
+          sc[i] = (i < kc) ? sc[i] * t.scale_log2 : -INFINITY;
+          mh = fmaxf(mh, sc[i]);
+        }
+      }
+      tmem_st1(xcol + (uint32_t)(2 * (c & 1) + hg), mh);
+      tc_fence_before();
+      sm_sync();
+      tc_fence_after();
+      const float mj = fmaxf(mh, tmem_ld1(xcol + (uint32_t)(2 * (c & 1) + (hg ^ 1))));
+      if (!ok || flags[0]) {
+        ok = false;
+        mbar_arrive(&pfull[c & 1]);
+        continue;
       }
       const bool need = mj > m_run + kRescaleLog2;
-      // P buffer j&1 is free once O += P V^T of page j-2 has completed
-      if (j >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[j & 1], ((j - 2) >> 1) & 1, &flags[0]))) {
+      // P buffer c&1 is free once O += P V^T of chunk c-2 has completed
+      if (c >= 2) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[c & 1], ((c - 2) >> 1) & 1, &flags[0]))) {
           ok = false;
-          break;
+          mbar_arrive(&pfull[c & 1]);
+          continue;
         }
         __syncwarp();
         tc_fence_after();
       }
-      const bool resc = __any_sync(0xffffffffu, need && j > 0);
-      // rescaling O needs every product issued so far (through page j-1) done
+      const bool resc = __any_sync(0xffffffffu, need && c > 0);
+      // rescaling O needs every product issued so far (through chunk c-1) done
       if (resc) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[(j - 1) & 1], ((j - 1) >> 1) & 1, &flags[0]))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[(c - 1) & 1], ((c - 1) >> 1) & 1, &flags[0]))) {
           ok = false;
-          break;
+          mbar_arrive(&pfull[c & 1]);
+          continue;
         }
         __syncwarp();
         tc_fence_after();
-      }
-      if (resc) {
         const float alpha = need ? exp2f(m_run - mj) : 1.f;
-        for (int c = 0; c < g.d / 32; ++c) {
+        for (int cc = 0; cc < ocols / 32; ++cc) {
           float o[32];
-          tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), o);
+          const uint32_t oa = tmem + lane_base + (uint32_t)(hg * ocols + cc * 32);
+          tmem_ld32(oa, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= alpha;
-          tmem_st32(tmem + lane_base + (uint32_t)(c * 32), o);
+          tmem_st32(oa, o);
         }
         l_run *= alpha;
       }
       if (need) m_run = mj;
       float lsum = 0.f;
-      uint8_t* prow = sP + (j & 1) * kQAtomBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      uint8_t* prow = sP + (c & 1) * kPBytes + hg * kQAtomBytes + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int cc = 0; cc < 8; ++cc) {
         uint32_t w[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          const float p0 = exp2f(sc[8 * c + 2 * h] - m_run);
-          const float p1 = exp2f(sc[8 * c + 2 * h + 1] - m_run);
+          const float p0 = ex2_fast(sc[8 * cc + 2 * h] - m_run);
+          const float p1 = ex2_fast(sc[8 * cc + 2 * h + 1] - m_run);
           lsum += p0 + p1;
           const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
           w[h] = *reinterpret_cast<const uint32_t*>(&b);
         }
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       l_run += lsum;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&pfull[j & 1]);
+      mbar_arrive(&pfull[c & 1]);
     }
-    if (ok && n_all > 0 &&
-        __all_sync(0xffffffffu, mbar_wait(&pvdone[(n_all - 1) & 1], ((n_all - 1) >> 1) & 1, &flags[0]))) {
-      __syncwarp();
-      tc_fence_after();
+    bool fin = ok && n_chunks > 0 &&
+               __all_sync(0xffffffffu, mbar_wait(&pvdone[(n_chunks - 1) & 1], ((n_chunks - 1) >> 1) & 1, &flags[0]));
+    __syncwarp();
+    tc_fence_after();
+    // the row sum is the two halves' shares
+    tmem_st1(xcol + 4u + (uint32_t)hg, l_run);
+    tc_fence_before();
+    sm_sync();
+    tc_fence_after();
+    const float l_tot = l_run + tmem_ld1(xcol + 4u + (uint32_t)(hg ^ 1));
+    if (fin) {
       const long prow = (long)item * R + r;
-      for (int c = 0; c < g.d / 32; ++c) {
+      for (int cc = 0; cc < ocols / 32; ++cc) {
         float o[32];
-        tmem_ld32(tmem + lane_base + (uint32_t)(c * 32), o);
+        tmem_ld32(tmem + lane_base + (uint32_t)(hg * ocols + cc * 32), o);
         if (r < R) {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * g.d + c * 32);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + prow * g.d + hg * ocols + cc * 32);
 #pragma unroll
           for (int i = 0; i < 8; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
         }
       }
-      if (r < R) {
+      if (r < R && hg == 0) {
         a.part_ml[prow * 2] = m_run;
-        a.part_ml[prow * 2 + 1] = l_run;
+        a.part_ml[prow * 2 + 1] = l_tot;
       }
-    } else if (n_all > 0) {
+    } else if (n_chunks > 0) {
       flags[0] = 1;
     }
   }
@@ -303,14 +356,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
 size_t attn_tc_smem_bytes(int d, int stages) {
   const int datoms = d / 64;
-  const int stage_bytes = datoms * kKAtomBytes + d * 128;
-  return (size_t)datoms * kQAtomBytes + 2 * kQAtomBytes + (size_t)stages * stage_bytes + 256 + 1024;
+  const int stage_bytes = datoms * kQAtomBytes + 2 * d * 128;
+  return (size_t)datoms * kQAtomBytes + 2 * kPBytes + (size_t)stages * stage_bytes + 256 + 1024;
 }
 
 void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
@@ -318,9 +371,9 @@ void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const 
   AttnTcCfg t{};
   const int d = a.g.d;
   t.datoms = d / 64;
-  t.stage_bytes = t.datoms * kKAtomBytes + d * 128;
-  t.stages = 4;
-  t.idesc_s = idesc_bf16(128, kPage);
+  t.stage_bytes = t.datoms * kQAtomBytes + 2 * d * 128;
+  t.stages = 2;
+  t.idesc_s = idesc_bf16(128, kChunk);
   t.idesc_o = idesc_bf16(128, d);
   t.scale_log2 = 1.4426950408889634f / std::sqrt((float)d);
   const size_t smem = attn_tc_smem_bytes(d, t.stages);
