@@ -190,6 +190,8 @@ void launch_prep_norm(const FinishArgs& f, cudaStream_t s) {
   launch_pdl(prep_norm_kernel, dim3(f.n_tok), dim3(kRowThreads), 0, s, f);
 }
 
+const void* final_norm_kernel_entry() { return reinterpret_cast<const void*>(final_norm_kernel); }
+
 void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s) {
   launch_pdl(final_norm_kernel, dim3(n_tok), dim3(kRowThreads), 0, s, h, gain, out, g.H, g.eps);
 }

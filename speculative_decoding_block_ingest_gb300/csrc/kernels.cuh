@@ -175,6 +175,8 @@ void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s);
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s);
+const void* init_kernel_entry();       // kernel function addresses, to find
+const void* final_norm_kernel_entry(); // their nodes in a captured graph
 void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s);
 void launch_kv_read(const Geo& g, const void* kpool, const void* vpool, const int* block_table,
                     int slot, int layer, int row0, int nrows, float* k_out, float* v_out,

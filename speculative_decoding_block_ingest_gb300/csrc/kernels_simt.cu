@@ -341,6 +341,8 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
   }
 }
 
+const void* init_kernel_entry() { return reinterpret_cast<const void*>(init_kernel); }
+
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s) {
   launch_pdl(init_kernel, dim3(a.n_rows + 1), dim3(kInitThreads), 0, s, a, blob);
 }

@@ -293,6 +293,22 @@ struct dflash_handle {
   // create; rounds alternate between the two counter sets
   bool mk_off = false;
   int mk_parity = 0;
+  // replayable rounds: one instantiated graph per (sequences, attention
+  // items, KV region); only the per-call init and final-norm nodes change
+  struct RoundGraph {
+    int n_seq = 0, n_items = 0;
+    const void* region = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    cudaGraphNode_t init_node = nullptr, norm_node = nullptr;
+    cudaKernelNodeParams init_p{}, norm_p{};
+    int64_t launches = 0;
+    uint64_t used = 0;
+  };
+  std::vector<RoundGraph> graphs;
+  uint64_t graph_clock = 0;
+  bool graphs_off = false;
+  cudaStream_t cap_stream = nullptr;   // private stream the rounds are captured on
   struct Rec {
     int kind;
     cudaEvent_t a, b;
@@ -549,6 +565,28 @@ int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens) {
   return (int)std::max<long>(1, (units + target - 1) / target);
 }
 
+// Arguments of a round's init kernel (copied into the kernel's parameters).
+InitArgs round_init_args(dflash_t* h, int n_tok, const float* noise) {
+  InitArgs ia{};
+  ia.src = noise;
+  ia.n_rows = n_tok;
+  ia.width = h->g.H;
+  ia.h = h->at<float>(h->lo.h);
+  ia.desc_dst = h->at<void>(h->lo.rdesc);
+  ia.cp_off[0] = 0;
+  ia.cp_len[0] = (int)(offsetof(RoundDesc, pos) / 4);
+  ia.cp_off[1] = (int)(offsetof(RoundDesc, pos) / 4);
+  ia.cp_len[1] = n_tok;
+  ia.cp_off[2] = (int)(offsetof(RoundDesc, dest) / 4);
+  ia.cp_len[2] = n_tok;
+  ia.block_table = h->at<int>(h->lo.btab);
+  ia.inv_freq = h->at<double>(h->lo.inv_freq);
+  ia.rope_cs = h->at<float2>(h->lo.rope_cs);
+  ia.is_round = 1;
+  ia.g = h->g;
+  return ia;
+}
+
 // The whole round (after the per-call init) as one persistent kernel.
 void enqueue_round_mk(dflash_t* h, const RoundDesc& rd, float* out, cudaStream_t s) {
   const Geo& g = h->g;
@@ -648,23 +686,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   float* qkv_acc = h->at<float>(h->lo.qkv_acc);
   float* gu_acc = h->at<float>(h->lo.gu_acc);
 
-  InitArgs ia{};
-  ia.src = noise;
-  ia.n_rows = n_tok;
-  ia.width = g.H;
-  ia.h = hres;
-  ia.desc_dst = h->at<void>(h->lo.rdesc);
-  ia.cp_off[0] = 0;
-  ia.cp_len[0] = (int)(offsetof(RoundDesc, pos) / 4);
-  ia.cp_off[1] = (int)(offsetof(RoundDesc, pos) / 4);
-  ia.cp_len[1] = n_tok;
-  ia.cp_off[2] = (int)(offsetof(RoundDesc, dest) / 4);
-  ia.cp_len[2] = n_tok;
-  ia.block_table = h->at<int>(h->lo.btab);
-  ia.inv_freq = h->at<double>(h->lo.inv_freq);
-  ia.rope_cs = h->at<float2>(h->lo.rope_cs);
-  ia.is_round = 1;
-  ia.g = g;
+  InitArgs ia = round_init_args(h, n_tok, noise);
   {
     Launch L(h, DFLASH_KERNEL_INIT, (double)n_tok * g.H * 8, s);
     launch_init(ia, blob, s);
@@ -910,6 +932,110 @@ int ingest_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* t_
   return DFLASH_OK;
 }
 
+// A round through a cached graph: the ~80 launches of the per-step path cost
+// the host about as long as the GPU takes to run them, so they are captured
+// once per (sequences, attention items, KV region) and replayed; a replay
+// changes only the init node (descriptor blob, noise rows) and the final-norm
+// node (output rows).  Off while profiling or tracing, for the persistent
+// kernel, when the caller's stream is itself being captured, and with
+// DFLASH_GRAPHS=0 at create.
+void enqueue_round_graph(dflash_t* h, InitBlob& blob, const float* noise, float* out, cudaStream_t s) {
+  const RoundDesc& rd = blob.round;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  ck(cudaStreamIsCapturing(s, &cap), "stream capture query");
+  const bool mk = mk_eligible(h, rd.n_tok) && rd.n_items <= h->n_sm;
+  if (h->graphs_off || h->prof_on || h->trace_buf || mk || cap != cudaStreamCaptureStatusNone) {
+    enqueue_round(h, blob, noise, out, s);
+    return;
+  }
+  const void* region = h->kv;
+  dflash_handle::RoundGraph* gr = nullptr;
+  for (auto& e : h->graphs)
+    if (e.n_seq == rd.n_seq && e.n_items == rd.n_items && e.region == region) gr = &e;
+  InitArgs ia = round_init_args(h, rd.n_tok, noise);
+  if (gr) {
+    cudaKernelNodeParams p = gr->init_p;
+    void* ip[2] = {&ia, &blob};
+    p.kernelParams = ip;
+    ck(cudaGraphExecKernelNodeSetParams(gr->exec, gr->init_node, &p), "round graph init update");
+    const float* hres = h->at<float>(h->lo.h);
+    const float* fn = h->at<float>(h->lo.fn);
+    int H = h->g.H;
+    float eps = h->g.eps;
+    cudaKernelNodeParams q = gr->norm_p;
+    void* np[5] = {&hres, &fn, &out, &H, &eps};
+    q.kernelParams = np;
+    ck(cudaGraphExecKernelNodeSetParams(gr->exec, gr->norm_node, &q), "round graph output update");
+    ck(cudaGraphLaunch(gr->exec, s), "round graph launch");
+    h->launches += gr->launches;
+    gr->used = ++h->graph_clock;
+    return;
+  }
+  // capture this round on the private stream (the caller's may be the legacy
+  // default stream, which cannot be captured), keep it, and run it on the
+  // caller's stream
+  if (!h->cap_stream) ck(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking), "capture stream");
+  cudaStream_t cs = h->cap_stream;
+  const int64_t l0 = h->launches;
+  ck(cudaStreamBeginCapture(cs, cudaStreamCaptureModeRelaxed), "round capture begin");
+  cudaGraph_t graph = nullptr;
+  try {
+    enqueue_round(h, blob, noise, out, cs);
+  } catch (...) {
+    cudaStreamEndCapture(cs, &graph);
+    if (graph) cudaGraphDestroy(graph);
+    throw;
+  }
+  ck(cudaStreamEndCapture(cs, &graph), "round capture end");
+  dflash_handle::RoundGraph e;
+  e.n_seq = rd.n_seq;
+  e.n_items = rd.n_items;
+  e.region = region;
+  e.launches = h->launches - l0;
+  size_t n = 0;
+  ck(cudaGraphGetNodes(graph, nullptr, &n), "round graph nodes");
+  std::vector<cudaGraphNode_t> nodes(n);
+  ck(cudaGraphGetNodes(graph, nodes.data(), &n), "round graph nodes");
+  for (auto nd : nodes) {
+    cudaGraphNodeType t;
+    ck(cudaGraphNodeGetType(nd, &t), "round graph node type");
+    if (t != cudaGraphNodeTypeKernel) continue;
+    cudaKernelNodeParams p{};
+    ck(cudaGraphKernelNodeGetParams(nd, &p), "round graph node params");
+    if (p.func == init_kernel_entry()) {
+      e.init_node = nd;
+      e.init_p = p;
+    } else if (p.func == final_norm_kernel_entry()) {
+      e.norm_node = nd;
+      e.norm_p = p;
+    }
+  }
+  if (!e.init_node || !e.norm_node) {
+    cudaGraphDestroy(graph);
+    throw CudaError{"round graph: init or final-norm node not found"};
+  }
+  cudaError_t ie = cudaGraphInstantiate(&e.exec, graph, 0);
+  if (ie != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    throw CudaError{std::string("round graph instantiate: ") + cudaGetErrorString(ie)};
+  }
+  // node handles of the source graph address the same nodes in the exec graph
+  // for parameter updates, so the source graph stays alive with it
+  e.used = ++h->graph_clock;
+  if (h->graphs.size() >= 8) {   // drop the least recently used
+    auto it = std::min_element(h->graphs.begin(), h->graphs.end(),
+                               [](const dflash_handle::RoundGraph& a, const dflash_handle::RoundGraph& b) {
+                                 return a.used < b.used;
+                               });
+    cudaGraphExecDestroy(it->exec);
+    cudaGraphDestroy(it->graph);
+    h->graphs.erase(it);
+  }
+  e.graph = graph;
+  h->graphs.push_back(e);
+  ck(cudaGraphLaunch(e.exec, s), "round graph launch");
+}
+
 int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos_block, const float* noise,
                 float* out, cudaStream_t s) {
   if (!pos_block || !noise || !out) return fail(DFLASH_ERR_INVALID_ARG, "pos_block / noise_emb / out is null");
@@ -945,7 +1071,7 @@ int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos
     return fail(DFLASH_ERR_CAPACITY, "attention plan exceeds its scratch");
   }
   int rc = guarded([&]() -> int {
-    enqueue_round(h, *blob, noise, out, s);
+    enqueue_round_graph(h, *blob, noise, out, s);
     return DFLASH_OK;
   });
   if (rc != DFLASH_OK) rollback_pages(h, *blob, taken);
@@ -1134,6 +1260,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       // one kernel per step, which measured faster at the 8-layer shape
       const char* path = std::getenv("DFLASH_ROUND_PATH");
       h->mk_off = !(path && std::string(path) == "persistent");
+    }
+    {
+      const char* gs = std::getenv("DFLASH_GRAPHS");   // "0": launch every round's kernels directly
+      h->graphs_off = gs && std::string(gs) == "0";
     }
     if (h->use_tc) {
       const uint64_t Mt2 = 2ull * lo.Mt;
@@ -1376,6 +1506,11 @@ void dflash_destroy(dflash_t* h) {
     cudaEventDestroy(r.b);
   }
   for (auto e : h->event_pool) cudaEventDestroy(e);
+  for (auto& gr : h->graphs) {
+    cudaGraphExecDestroy(gr.exec);
+    cudaGraphDestroy(gr.graph);
+  }
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   delete h;
 }
 
