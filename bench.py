@@ -159,8 +159,9 @@ def cpu_cores():
 
 
 def run_reference(args, wl):
-    done, secs = oracle_rounds(wl, args.steps, args.warmup)
-    value = done / secs
+    # bounded: the timed rounds stop after about two minutes of host time
+    done, secs = oracle_rounds(wl, args.steps, args.warmup, budget_s=120.0)
+    value = done / secs / wl.batch
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": args.gpus,
             "steps": done, "warmup": args.warmup, "ms_per_step": 1e3 * secs / done, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
@@ -176,7 +177,8 @@ def workload_config(wl):
     c = wl.cfg
     return {"workload": wl.name, "layers": c.n_layers, "hidden": c.hidden, "heads": f"{c.n_heads}:{c.n_kv_heads}",
             "head_dim": c.head_dim, "intermediate": c.intermediate, "taps": c.n_taps, "block": c.block,
-            "batch": wl.batch, "ctx": wl.ctx, "ingest_rows": f"U{{{wl.ingest_lo}..{wl.ingest_hi}}}",
+            "batch": wl.batch, "ctx": wl.ctx if wl.ctx_hi == 0 else f"U[{wl.ctx_lo},{wl.ctx_hi}]",
+            "ingest_rows": f"U{{{wl.ingest_lo}..{wl.ingest_hi}}}",
             "weights": c.weight_dtype, "kv": c.kv_dtype, "rope": c.rope_type,
             "l2": "no flush: every round streams >1 GB of weights and KV, far above the 129 MB L2"}
 
@@ -204,47 +206,63 @@ def main():
     dev = f"cuda:{local}"
     torch.cuda.set_device(dev)
     cfg = wl.cfg
-    if wl.batch != 1:
-        raise SystemExit("bench.py times the single-sequence drafting round")
+    B = wl.batch
     K, Wm = args.steps, args.warmup
-    counts = [c[0] for c in wl.ingest_counts(Wm + K)]
-    ctx = wl.ctx
+    counts = wl.ingest_counts(Wm + K)          # [step][sequence]
+    lens0 = wl.ctx_lengths()
     SLOTS = 3                                    # device-timed, e2e, profiled passes
-    grow = sum(counts) + 16
-    max_len = ctx + grow + 64
-    pages_per = (max_len + 63) // 64
-    dr = dflash.Drafter(cfg, synth.make_weights(cfg), max_seqs=SLOTS, max_pages=SLOTS * pages_per,
-                        max_seq_len=max_len, max_batch=1, max_ingest_rows=512, device=dev)
+    grow = [sum(c[i] for c in counts) for i in range(B)]
+    max_len = max(l + g for l, g in zip(lens0, grow)) + 16 + 64
+    pages = sum((l + g + 16 + 63) // 64 + 1 for l, g in zip(lens0, grow))
+    dr = dflash.Drafter(cfg, synth.make_weights(cfg), max_seqs=SLOTS * B, max_pages=SLOTS * pages,
+                        max_seq_len=max_len, max_batch=B, max_ingest_rows=512, device=dev)
     stream = torch.cuda.current_stream()
-    # untimed cache build: the same ctx rows into every slot
-    per_call = 512 // SLOTS
-    for r0 in range(0, ctx, per_call):
-        n = min(per_call, ctx - r0)
-        taps = synth.taps_rows(cfg, 0, r0, n).to(dev)
-        dr.ingest(list(range(SLOTS)), [n] * SLOTS, list(range(r0, r0 + n)) * SLOTS,
-                  torch.cat([taps] * SLOTS))
+    width = cfg.n_taps * cfg.hidden
+
+    def taps_for(seq, row0, n):
+        # one sequence: the seeded host rows; batches: seeded device rows (same
+        # distribution; generating ~10^5 rows x n*H on the host would dominate)
+        if B == 1:
+            return synth.taps_rows(cfg, 0, row0, n).to(dev)
+        gen = torch.Generator(device=dev).manual_seed(1_000_003 * (seq + 1) + row0)
+        return torch.randn(n, width, generator=gen, device=dev)
+
+    # untimed cache build: the same ctx rows into every pass's slots
+    for p in range(SLOTS):
+        for i in range(B):
+            for r0 in range(0, lens0[i], 512):
+                n = min(512, lens0[i] - r0)
+                dr.ingest([p * B + i], [n], list(range(r0, r0 + n)), taps_for(i, r0, n))
     torch.cuda.synchronize()
     # per-step inputs, resident in HBM
     taps_steps, noise_steps, lens = [], [], []
-    length = ctx
+    cur = list(lens0)
     for k in range(Wm + K):
-        taps_steps.append(synth.taps_rows(cfg, 0, length, counts[k]).to(dev))
-        noise_steps.append(synth.noise_rows(cfg, 0, k)[None].to(dev))
-        lens.append(length)
-        length += counts[k]
-    out = torch.empty(1, 16, cfg.hidden, device=dev)
+        taps_steps.append(torch.cat([taps_for(i, cur[i], counts[k][i]) for i in range(B)]))
+        noise_steps.append(torch.stack([synth.noise_rows(cfg, i, k) for i in range(B)]).to(dev))
+        lens.append(list(cur))
+        cur = [c + counts[k][i] for i, c in enumerate(cur)]
+    out = torch.empty(B, 16, cfg.hidden, device=dev)
 
-    def step(slot, k):
-        t, L0 = counts[k], lens[k]
-        dr.ingest([slot], [t], list(range(L0, L0 + t)), taps_steps[k])
-        dr.forward_round([slot], list(range(L0 + t, L0 + t + 16)), noise_steps[k], out)
+    def step_args(p, k):
+        seqs = [p * B + i for i in range(B)]
+        ts = counts[k]
+        pos_new = [r for i in range(B) for r in range(lens[k][i], lens[k][i] + ts[i])]
+        pos_block = [r for i in range(B) for r in range(lens[k][i] + ts[i], lens[k][i] + ts[i] + 16)]
+        return seqs, ts, pos_new, pos_block
+
+    def step(p, k):
+        seqs, ts, pos_new, pos_block = step_args(p, k)
+        if sum(ts):
+            dr.ingest(seqs, ts, pos_new, taps_steps[k])
+        dr.forward_round(seqs, pos_block, noise_steps[k], out)
 
     def barrier():
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- device-timed pass (slot 0)
+    # ---- device-timed pass (pass 0)
     for k in range(Wm):
         step(0, k)
     clocks = ClockSampler(local)
@@ -268,20 +286,21 @@ def main():
         ms = float(t.item())
     value = world * K / (ms / 1e3)
 
-    # ---- end-to-end pass (slot 1): pinned host inputs, copies inside the timed region
+    # ---- end-to-end pass (pass 1): pinned host inputs, copies inside the timed region
     host_taps = [t.cpu().pin_memory() for t in taps_steps]
     host_noise = [n.cpu().pin_memory() for n in noise_steps]
-    host_out = torch.empty(1, 16, cfg.hidden).pin_memory()
-    dev_taps = torch.empty(16, cfg.n_taps * cfg.hidden, device=dev)
-    dev_noise = torch.empty(1, 16, cfg.hidden, device=dev)
+    host_out = torch.empty(B, 16, cfg.hidden).pin_memory()
+    dev_taps = torch.empty(max(1, max(sum(c) for c in counts)), width, device=dev)
+    dev_noise = torch.empty(B, 16, cfg.hidden, device=dev)
 
     def step_e2e(k):
-        t, L0 = counts[k], lens[k]
-        dt = dev_taps[:t]
-        dt.copy_(host_taps[k], non_blocking=True)
+        seqs, ts, pos_new, pos_block = step_args(1, k)
+        if sum(ts):
+            dt = dev_taps[:sum(ts)]
+            dt.copy_(host_taps[k], non_blocking=True)
+            dr.ingest(seqs, ts, pos_new, dt)
         dev_noise.copy_(host_noise[k], non_blocking=True)
-        dr.ingest([1], [t], list(range(L0, L0 + t)), dt)
-        dr.forward_round([1], list(range(L0 + t, L0 + t + 16)), dev_noise, out)
+        dr.forward_round(seqs, pos_block, dev_noise, out)
         host_out.copy_(out, non_blocking=True)
 
     for k in range(Wm):
@@ -298,8 +317,8 @@ def main():
         t = torch.tensor([ms_e2e], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_e2e = float(t.item())
-    h2d = sum(counts[Wm:]) * cfg.n_taps * cfg.hidden * 4 / K + 16 * cfg.hidden * 4
-    d2h = 16 * cfg.hidden * 4
+    h2d = sum(sum(c) for c in counts[Wm:]) * width * 4 / K + B * 16 * cfg.hidden * 4
+    d2h = B * 16 * cfg.hidden * 4
 
     # ---- profiled pass (slot 2): per-launch event pairs, same steps
     for k in range(Wm):
@@ -328,9 +347,11 @@ def main():
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         done, secs = oracle_rounds(wl, args.cpu_rounds, 0)
-        cpu = {"value": done / secs, "unit": "rounds/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{done} rounds (ingest t~U{{1..16}} + 16-row forward over the {ctx}-row cache), "
-                         f"f64 numpy on host cores; cache build excluded"}
+        # the oracle follows sequence 0; a batch round costs it B sequence rounds
+        cpu = {"value": done / secs / B, "unit": "rounds/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{done} rounds of sequence 0 (ingest + 16-row forward over its {lens0[0]}-row cache)"
+                         + (f", scaled to the batch of {B}" if B > 1 else "")
+                         + ", f64 numpy on host cores; cache build excluded"}
     line = {
         "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -339,7 +360,7 @@ def main():
         "e2e": {"value": world * K / (ms_e2e / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk, "gpu_launches": launches,
-        "drafted_tokens_per_s": 15 * value, "block_rows_per_s": 16 * value,
+        "drafted_tokens_per_s": 15 * B * value, "block_rows_per_s": 16 * B * value,
         "kernel_breakdown": breakdown,
     }
     print(json.dumps(line))

@@ -118,7 +118,10 @@ typedef struct dflash_weights {
 
 /* Bytes of device workspace the handle needs for this config (256-byte
  * aligned start required).  Holds the repacked weights, the paged KV pools,
- * page tables, activations and reduction scratch. */
+ * page tables, activations and reduction scratch.  bf16 and e4m3 weights are
+ * stored as bf16 blocks for the tensor cores (e4m3 values expand exactly;
+ * their per-row scales are applied to the projections' sums), f32 weights
+ * as given. */
 int dflash_workspace_bytes(const dflash_config *cfg, size_t *bytes);
 
 /* Validate cfg, carve the caller's workspace, copy and repack the weights

@@ -115,6 +115,8 @@ void launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 // Tensor-core projection: a.W is the weight in 16 KB blocks (see weights.cu).
 void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s);
 void launch_repack(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base, cudaStream_t s);
+void launch_repack_e4m3(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base,
+                        cudaStream_t s);
 
 // Persistent round (round_mk.cu).  Counter offsets (u32 words) within one
 // layer's block of a counter set.

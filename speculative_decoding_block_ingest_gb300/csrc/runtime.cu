@@ -50,7 +50,9 @@ void ck(cudaError_t e, const char* what) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-int esize_w(int wtype) { return wtype == DFLASH_F32 ? 4 : (wtype == DFLASH_BF16 ? 2 : 1); }
+// Bytes per stored weight element: f32 stays f32; bf16 and e4m3 weights are
+// stored as bf16 blocks for the tensor cores (e4m3 expands exactly).
+int esize_w(int wtype) { return wtype == DFLASH_F32 ? 4 : 2; }
 int esize_kv(int kvtype) { return kvtype == DFLASH_F32 ? 4 : 2; }
 
 // Workspace carve-up, computed identically by dflash_workspace_bytes and dflash_create.
@@ -287,7 +289,8 @@ struct dflash_handle {
   // tensor maps of the tensor-core projections' operands (per buffer)
   CUtensorMap xmap_taps, xmap_h, xmap_o, xmap_a;
   CUtensorMap qmap;                             // attention: q buffer (3-D)
-  bool use_tc = false;
+  bool use_tc = false;    // tensor-core projections (bf16 weights)
+  bool attn_tc = false;   // tensor-core attention (bf16 KV, any weights)
   bool prof_on = false;
   // persistent round kernel: only with DFLASH_ROUND_PATH=persistent at
   // create; rounds alternate between the two counter sets
@@ -550,7 +553,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
 // The persistent round takes bf16 rounds of up to kMkMaxTok block rows whose
 // projection stage fits at least two ring stages beside the attention buffers.
 bool mk_eligible(dflash_t* h, int n_tok) {
-  return h->use_tc && !h->mk_off && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
+  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && !h->mk_off && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
          round_mk_stages((n_tok + 15) / 16 * 16, h->g.d) >= 2;
 }
 
@@ -561,7 +564,7 @@ int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens) {
   // each (sequence, kv head) rounds its split count up
   const bool mk = mk_eligible(h, (int)lens.size() * kBlock);
   const long target = mk ? std::max<long>(1, (long)h->n_sm - (long)h->g.Hkv * (long)lens.size())
-                         : (h->use_tc ? (long)h->n_sm : 2L * h->n_sm);
+                         : (h->attn_tc ? (long)h->n_sm : 2L * h->n_sm);
   return (int)std::max<long>(1, (units + target - 1) / target);
 }
 
@@ -770,8 +773,8 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
       double kv_b = 0;
       for (int i = 0; i < rd.n_seq; ++i) kv_b += (double)(rd.len[i] + kBlock) * g.Hkv * g.d * 2 * ekv;
       Launch L(h, DFLASH_KERNEL_ATTENTION, kv_b + (double)n_tok * g.Hq * g.d * ekv + part_b, s);
-      a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_ATTENTION, rd.n_items) : nullptr;
-      if (h->use_tc) launch_attention_tc(a, rd.n_items, &h->qmap, &h->kv->kmap, &h->kv->vmap, s);
+      a.trace = h->attn_tc ? trace_slot(h, DFLASH_KERNEL_ATTENTION, rd.n_items) : nullptr;
+      if (h->attn_tc) launch_attention_tc(a, rd.n_items, &h->qmap, &h->kv->kmap, &h->kv->vmap, s);
       else launch_attention_simt(a, rd.n_items, s);
     }
     ck(cudaGetLastError(), "attention launch");
@@ -1152,13 +1155,13 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       return fail(DFLASH_ERR_INVALID_ARG, "missing tensor in layer %d", l);
     if (fp8 && (!L.q_scale || !L.k_scale || !L.v_scale || !L.o_scale || !L.gate_scale || !L.up_scale || !L.down_scale))
       return fail(DFLASH_ERR_INVALID_ARG, "missing fp8 scale in layer %d", l);
-    // bf16 matrices are re-blocked with 16-byte moves
-    if (cfg->weight_dtype == DFLASH_BF16 &&
+    // bf16 and e4m3 matrices are re-blocked with 16- and 8-byte moves
+    if (cfg->weight_dtype != DFLASH_F32 &&
         !(aligned16(L.q) && aligned16(L.k) && aligned16(L.v) && aligned16(L.o) && aligned16(L.gate) &&
           aligned16(L.up) && aligned16(L.down)))
       return fail(DFLASH_ERR_INVALID_ARG, "bf16 weight matrices must start on a 16-byte boundary (layer %d)", l);
   }
-  if (cfg->weight_dtype == DFLASH_BF16 && !aligned16(w->fc))
+  if (cfg->weight_dtype != DFLASH_F32 && !aligned16(w->fc))
     return fail(DFLASH_ERR_INVALID_ARG, "bf16 weight matrices must start on a 16-byte boundary (fc)");
   const int n_sm = sm_count();
   Layout lo = make_layout(*cfg, n_sm);
@@ -1201,10 +1204,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     // A matrix piece: source rows i land on logical rows base + (i / chunk) *
     // stride + i % chunk of the [N][K] matrix at dst_off (row-major, or in
     // 16 KB swizzled blocks for the tensor-core path).
-    const bool tc = cfg->weight_dtype == DFLASH_BF16;
+    const bool tc = cfg->weight_dtype != DFLASH_F32;
     auto mat = [&](size_t dst_off, int K, const void* src, int n_rows, int chunk, int stride, int base) {
       if (tc) {
-        launch_repack(h->ws + dst_off, K, src, n_rows, chunk, stride, base, s);
+        if (fp8) launch_repack_e4m3(h->ws + dst_off, K, src, n_rows, chunk, stride, base, s);
+        else launch_repack(h->ws + dst_off, K, src, n_rows, chunk, stride, base, s);
         ck(cudaGetLastError(), "weight repack");
       } else if (chunk == n_rows) {
         cp(dst_off + (size_t)base * K * ew, src, (size_t)n_rows * K * ew);
@@ -1254,7 +1258,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       }
     }
     ck(cudaMemcpyAsync(h->ws + lo.inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s), "rope table");
-    h->use_tc = cfg->weight_dtype == DFLASH_BF16;
+    h->use_tc = cfg->weight_dtype != DFLASH_F32;
+    h->attn_tc = cfg->kv_dtype == DFLASH_BF16;
     {
       // "persistent": the whole round in one kernel (round_mk.cu); by default
       // one kernel per step, which measured faster at the 8-layer shape
@@ -1271,6 +1276,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       h->xmap_h = make_map_bf16(h->ws + lo.op_h, Mt2, H, 16);
       h->xmap_o = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, 16);
       h->xmap_a = make_map_bf16(h->ws + lo.op_a, Mt2, I, 16);
+    }
+    if (h->attn_tc) {
       h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
 
       const uint64_t pool_rows = (uint64_t)L * cfg->max_pages * Hkv;
@@ -1364,7 +1371,7 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
       r.kpool = static_cast<char*>(base);
       r.vpool = r.kpool + (size_t)fixed_pages * page_bytes;
       r.max_pages = fixed_pages;
-      if (h->use_tc) {
+      if (h->attn_tc) {
         const uint64_t rows = (uint64_t)h->g.L * fixed_pages * h->g.Hkv;
         r.kmap = make_map_bf16(r.kpool, rows * kPage, h->g.d, kPage);
         r.vmap = make_map_bf16(r.vpool, rows * h->g.d, kPage, h->g.d);
