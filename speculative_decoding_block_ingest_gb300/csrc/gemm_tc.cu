@@ -36,14 +36,14 @@ struct TcCfg {
   uint32_t idesc;
 };
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 224;   // warps: 0 producer, 1 and 6 MMA issuers, 2..5 drain
 constexpr int kWTileBytes = kTileN * kTileK * 2;   // 16 KB
 constexpr int kXBox = 16;                           // operand rows per TMA box
 
 // One CTA per SM with a deep ring: every stage it can hold is filled with
 // weights before the programmatic-launch wait, so HBM keeps streaming while
 // the small kernel before it finishes.
-template <bool kFused>
+template <bool kFused, int kIss>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, GemmArgs a, TcCfg t) {
   extern __shared__ uint8_t smem_raw[];
@@ -51,9 +51,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* ctl = smem + t.stages * t.stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctl);
   uint64_t* empty = full + t.stages;
-  uint64_t* accfull = empty + t.stages;
-  uint64_t* accempty = accfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2);
+  uint64_t* accfull = empty + t.stages;   // [issuer][buffer]
+  uint64_t* accempty = accfull + 4;       // [issuer][buffer]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 4);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);   // abort, last
   float* red = reinterpret_cast<float*>(ctl + 512);
 
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], kEpiThreads);
     }
@@ -142,9 +142,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 6) {
+    // ---------------------------------------------------------------- MMA issuers
+    // One thread issuing tcgen05.mma at small N is bound by its own issue
+    // latency, so when four accumulators fit in TMEM (N = 2*nt <= 128) two
+    // issuers split every segment's units (even / odd ring slots), each into
+    // its own pair of TMEM accumulators; the drain adds the two.
+    const int j = warp == 1 ? 0 : 1;
+    if (lane == 0 && j < kIss) {
       // descriptor start fields are address >> 4 (14 bits, shared memory
       // < 256 KB), so stage and K-step offsets add without carries
       const uint64_t d0 = desc_sw128(smem_u32(smem));
@@ -152,29 +157,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t xo = kWTileBytes >> 4;
       const uint32_t lo = (kWTileBytes + x_plane_bytes) >> 4;
       const uint32_t idesc = t.idesc;
-      int seg = 0, st = 0;
-      uint32_t ph = 0;
+      int seg = 0, st = j % t.stages;
+      uint32_t ph = (uint32_t)(j / t.stages) & 1;
       bool ok = true;
-      unsigned long long wait_cyc = 0, issue_cyc = 0, first_full = 0;
       for (int u = u0; u < u1 && ok; ++seg) {
         const int T = u / p.kb;
         const int seg_end = min(u1, (T + 1) * p.kb);
         const int b = seg & 1, use = seg >> 1;
-        if (!mbar_wait(&accempty[b], (use & 1) ^ 1, &flags[0])) {
+        if (!mbar_wait(&accempty[2 * j + b], (use & 1) ^ 1, &flags[0])) {
           flags[0] = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(b * t.aw);
-        for (int k = 0; u < seg_end; ++u, ++k) {
-          const unsigned long long w0 = a.trace ? trace_clock() : 0;
+        const uint32_t d_tmem = tmem + (uint32_t)((2 * j + b) * t.aw);
+        // this issuer's units of the segment: ring slots i = u - u0 with i % kIss == j
+        int k = 0;
+        for (int uu = u + ((j - (u - u0)) % kIss + kIss) % kIss; uu < seg_end; uu += kIss, ++k) {
           if (!mbar_wait(&full[st], ph, &flags[0])) {
             flags[0] = 1;
             ok = false;
             break;
           }
           tc_fence_after();
-          const unsigned long long w1 = a.trace ? trace_clock() : 0;
           const uint64_t dw = d0 + (uint64_t)(st * dstage);
           // 4 K-steps of 16 (32 bytes = 2 descriptor units each)
           mma_bf16(d_tmem, dw, dw + xo, idesc, k > 0 ? 1u : 0u);
@@ -185,24 +189,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!kFused) mma_bf16(d_tmem, dw + kk, dw + lo + kk, idesc, 1u);
           }
           mma_commit(&empty[st]);
-          if (a.trace) {
-            wait_cyc += w1 - w0;
-            issue_cyc += trace_clock() - w1;
-            if (u == u0) first_full = w1 - c0;
-          }
-          if (++st == t.stages) {
-            st = 0;
+          st += kIss;
+          if (st >= t.stages) {
+            st -= t.stages;
             ph ^= 1;
           }
         }
-        if (ok) mma_commit(&accfull[b]);
+        // every segment is committed, also one without units of this issuer
+        if (ok) mma_commit(&accfull[2 * j + b]);
+        u = seg_end;
       }
-      trace_mark(a.trace, blockIdx.x, 3, c0);                   // 3: last MMA issued
-      if (a.trace) {   // 8, 9, 10: issuer cycles waiting for stages, issuing; first stage ready
-        a.trace[(long)blockIdx.x * kTraceWords + 9] = wait_cyc;
-        a.trace[(long)blockIdx.x * kTraceWords + 10] = issue_cyc;
-        a.trace[(long)blockIdx.x * kTraceWords + 11] = first_full;
-      }
+      if (j == 0) trace_mark(a.trace, blockIdx.x, 3, c0);       // 3: last MMA issued
     }
   } else {
     // ------------------------------------------------------------------ drain
@@ -210,16 +207,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int et = threadIdx.x - 64;
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
     const int row = 32 * q + lane;          // tile row (output feature) of this thread
-    // the thread's row of accumulator buffer b, token columns j0..j0+15
-    // (hi + lo halves when fused)
-    auto acc_ld16 = [&](int b, int j0, float* v) {
-      const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * t.aw + j0);
-      tmem_ld16(base, v);
+    // the thread's row of accumulator buffer b of issuer j, token columns
+    // j0..j0+15 (hi + lo halves when fused), added into v
+    auto acc_add_ld16 = [&](int jb, int j0, float* v) {
+      const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(jb * t.aw + j0);
+      float w[16];
+      tmem_ld16(base, w);
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] += w[e];
       if (kFused) {
-        float w[16];
         tmem_ld16(base + (uint32_t)t.nt, w);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] += w[j];
+        for (int e = 0; e < 16; ++e) v[e] += w[e];
       }
     };
     int seg = 0;
@@ -228,9 +227,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int seg_end = min(u1, (T + 1) * p.kb);
       const int b = seg & 1, use = seg >> 1;
       const bool last_seg = seg_end == u1;
+      // units of each issuer in this segment (ring slots i = uu - u0, issuer i % kIss)
+      int nu[2] = {seg_end - u, 0};
+      if (kIss == 2) {
+        nu[0] = ((u - u0) & 1) == 0 ? (seg_end - u + 1) / 2 : (seg_end - u) / 2;
+        nu[1] = seg_end - u - nu[0];
+      }
       // a failed wait skips the TMEM read but keeps every barrier arrival, so
       // no thread is left waiting at a named barrier
-      const bool got = __all_sync(0xffffffffu, mbar_wait(&accfull[b], use & 1, &flags[0]));
+      bool got = true;
+      for (int jj = 0; jj < kIss; ++jj)
+        got = __all_sync(0xffffffffu, mbar_wait(&accfull[2 * jj + b], use & 1, &flags[0])) && got;
       if (!got) flags[0] = 1;
       if (et == 0 && last_seg) trace_mark(a.trace, blockIdx.x, 6, c0);   // 6: last accumulator ready
       __syncwarp();
@@ -240,8 +247,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float* dcol = a.dst + (long)a.e.tok_base * a.dst_ld + T * kTileN + row;
           const float wsc = a.e.wscale ? a.e.wscale[T * kTileN + row] : 1.f;
           for (int j0 = 0; j0 < a.e.n_tok; j0 += 16) {
-            float v[16];
-            acc_ld16(b, j0, v);
+            float v[16] = {};
+            for (int jj = 0; jj < kIss; ++jj)
+              if (nu[jj] > 0) acc_add_ld16(2 * jj + b, j0, v);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               if (j0 + j < a.e.n_tok)
@@ -250,18 +258,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&accempty[b]);
+        for (int jj = 0; jj < kIss; ++jj) mbar_arrive(&accempty[2 * jj + b]);
       } else {
         float* acc_tile = a.acc + (long)T * kTileN * t.nt;
         if (got) {
           for (int j0 = 0; j0 < a.e.n_tok; j0 += 16) {
-            float v[16];
-            acc_ld16(b, j0, v);
+            float v[16] = {};
+            for (int jj = 0; jj < kIss; ++jj)
+              if (nu[jj] > 0) acc_add_ld16(2 * jj + b, j0, v);
             acc_add16(acc_tile + (long)row * t.nt, j0, a.e.n_tok, v);
           }
         }
         tc_fence_before();
-        mbar_arrive(&accempty[b]);
+        for (int jj = 0; jj < kIss; ++jj) mbar_arrive(&accempty[2 * jj + b]);
         __threadfence();
         epi_sync();
         if (et == 0) {
@@ -317,16 +326,23 @@ void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s) {
   // the two column halves)
   const bool fused = 2 * t.nt <= 256;
   t.aw = fused ? 2 * t.nt : t.nt;
-  t.tmem_cols = pow2_at_least(2 * t.aw);
+  // two issuers when their four accumulators fit in the 512 TMEM columns
+  const int iss = fused && 4 * t.aw <= 512 ? 2 : 1;
+  t.tmem_cols = pow2_at_least(2 * iss * t.aw);   // [issuer][buffer] accumulators
+  // nt <= 256 per pass keeps this within an SM's 512 columns (fused: aw <= 256
+  // and two issuers only at aw <= 128; unfused: aw = nt <= 256); a larger
+  // request would fault tcgen05.alloc, so it is never launched
+  if (t.tmem_cols > 512) return;
   t.x_row_lo = a.e.g.Mt;
   t.idesc = idesc_bf16(kTileN, t.aw);
   const size_t smem = gemm_tc_smem_bytes(t.nt, t.stages);
-  static size_t attr_bytes[2] = {0, 0};
-  auto kern = fused ? gemm_tc_kernel<true> : gemm_tc_kernel<false>;
-  if (smem > attr_bytes[fused]) {
+  static size_t attr_bytes[3] = {0, 0, 0};
+  const int var = !fused ? 0 : (iss == 1 ? 1 : 2);
+  auto kern = var == 0 ? gemm_tc_kernel<false, 1> : (var == 1 ? gemm_tc_kernel<true, 1> : gemm_tc_kernel<true, 2>);
+  if (smem > attr_bytes[var]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return;   // the launch below is skipped; the caller's cudaGetLastError reports it
-    attr_bytes[fused] = smem;
+    attr_bytes[var] = smem;
   }
   const CUtensorMap* mx = static_cast<const CUtensorMap*>(tmap_x);
   launch_pdl(kern, dim3(a.p.grid), dim3(kTcThreads), smem, s, *mx, a, t);
