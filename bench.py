@@ -320,7 +320,27 @@ def main():
     h2d = sum(sum(c) for c in counts[Wm:]) * width * 4 / K + B * 16 * cfg.hidden * 4
     d2h = B * 16 * cfg.hidden * 4
 
-    # ---- profiled pass (slot 2): per-launch event pairs, same steps
+    # ---- greedy draft tokens through a seeded target lm_head (vocab 32768)
+    lm_line = None
+    if cfg.weight_dtype != "f32":
+        vocab = 32768
+        packed, V = dr.pack_lm_head(synth.lm_head(cfg, vocab=vocab).to(torch.bfloat16).to(dev))
+        for _ in range(3):
+            dr.draft_tokens(out, packed, V)
+        barrier()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(stream)
+        for _ in range(K):
+            dr.draft_tokens(out, packed, V)
+        l1.record(stream)
+        barrier()
+        ms_lm = l0.elapsed_time(l1) / K
+        lm_bytes = vocab * cfg.hidden * 2 + B * 16 * (cfg.hidden * 4 + vocab * 4)
+        lm_line = {"vocab": vocab, "ms_per_call": ms_lm, "GB/s": lm_bytes / 1e9 / (ms_lm / 1e3),
+                   "note": "projection of the round's rows through the lm_head + argmax, not in value"}
+        del packed
+
+
     for k in range(Wm):
         step(2, k)
     barrier()
@@ -361,7 +381,7 @@ def main():
                 "d2h_bytes_per_step": d2h},
         "clocks": clk, "gpu_launches": launches,
         "drafted_tokens_per_s": 15 * B * value, "block_rows_per_s": 16 * B * value,
-        "kernel_breakdown": breakdown,
+        "kernel_breakdown": breakdown, "lm_head": lm_line,
     }
     print(json.dumps(line))
     if dist is not None:

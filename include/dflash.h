@@ -193,6 +193,29 @@ int dflash_forward_full(dflash_t *h, int32_t ctx, const float *taps, const float
 int dflash_forward_full_static(dflash_t *h, int32_t ctx, const float *taps, const float *noise_emb,
                                const int32_t *pos, float *out, void *stream);
 
+/* Greedy draft tokens through the target model's lm_head (the pages'
+ * DflashDraft page: the drafter reuses the target's lm_head on its block
+ * rows; module index, dflash2_walk_greedy: argmax, lowest index on ties).
+ *
+ * The lm_head is packed once into a caller buffer of dflash_lm_head_bytes
+ * (the library never allocates): vocab weight blocks for the tensor-core
+ * projection, then a logits scratch of max_batch*16 rows.  Requires bf16 or
+ * e4m3 drafter weights (the tensor-core path); vocab a multiple of 128.
+ *
+ *   dflash_lm_head_bytes  bytes of the packed buffer for `vocab` rows.
+ *   dflash_pack_lm_head   lm_head: device bf16 [vocab, H] row-major, read
+ *                         during the call; packed: device, 256-byte aligned.
+ *   dflash_draft_tokens   hidden: device f32 [n_seq, 16, H] (16-byte aligned;
+ *                         e.g. forward_round's out); tokens: device int32
+ *                         [n_seq, 16].  Logits are f32-accurate sums of bf16
+ *                         weights times the f32 rows (hi/lo split).  Calls
+ *                         sharing one packed buffer must not overlap (its
+ *                         logits scratch is reused). */
+int dflash_lm_head_bytes(const dflash_t *h, int32_t vocab, size_t *bytes);
+int dflash_pack_lm_head(dflash_t *h, const void *lm_head, int32_t vocab, void *packed, size_t bytes, void *stream);
+int dflash_draft_tokens(dflash_t *h, int32_t n_seq, const float *hidden, const void *packed, int32_t vocab,
+                        int32_t *tokens, void *stream);
+
 /* Drop a sequence's cache (len = 0, pages back to the pool). */
 int dflash_seq_reset(dflash_t *h, int32_t seq_id);
 

@@ -14,6 +14,7 @@
 //   swiglu       act = silu(g) * u from the gate/up accumulator as hi/lo
 //                planes; the entries are cleared.
 #include <algorithm>
+#include <cmath>
 
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -184,6 +185,72 @@ __global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
     for (int q = 0; q < 4; ++q)
       put_operand(f.op, (long)tok * g.I + j + q, f.op_plane, gg[q] / (1.f + __expf(-gg[q])) * uu[q], f.op_f32);
   }
+}
+
+// f32 rows -> hi/lo bf16 operand planes (no norm): the lm_head's operand.
+__global__ void __launch_bounds__(kRowThreads) to_operand_kernel(const float* src, int width, void* op, long plane) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int row = blockIdx.x, n4 = width / 4;
+  const float4* r4 = reinterpret_cast<const float4*>(src + (long)row * width);
+  for (int c = threadIdx.x; c < n4; c += kRowThreads) {
+    const float4 v = __ldg(r4 + c);
+    const long idx = (long)row * width + 4 * c;
+    put_operand(op, idx + 0, plane, v.x, 0);
+    put_operand(op, idx + 1, plane, v.y, 0);
+    put_operand(op, idx + 2, plane, v.z, 0);
+    put_operand(op, idx + 3, plane, v.w, 0);
+  }
+}
+
+// Row argmax over `V` logits, lowest index among equal maxima.
+__device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
+  if (v > bv || (v == bv && i < bi)) {
+    bv = v;
+    bi = i;
+  }
+}
+
+__global__ void __launch_bounds__(kRowThreads) argmax_kernel(const float* logits, int V, int32_t* tokens) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int row = blockIdx.x;
+  const float4* l4 = reinterpret_cast<const float4*>(logits + (long)row * V);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  // each thread walks its float4s in increasing index order
+  for (int c = threadIdx.x; c < V / 4; c += kRowThreads) {
+    const float4 v = __ldcg(l4 + c);
+    better(bv, bi, v.x, 4 * c);
+    better(bv, bi, v.y, 4 * c + 1);
+    better(bv, bi, v.z, 4 * c + 2);
+    better(bv, bi, v.w, 4 * c + 3);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    better(bv, bi, ov, oi);
+  }
+  __shared__ float sv[kRowThreads / 32];
+  __shared__ int si[kRowThreads / 32];
+  if ((threadIdx.x & 31) == 0) {
+    sv[threadIdx.x >> 5] = bv;
+    si[threadIdx.x >> 5] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRowThreads / 32; ++w) better(bv, bi, sv[w], si[w]);
+    tokens[row] = bi;
+  }
+}
+
+void launch_to_operand(const float* src, int n_rows, int width, void* op, long plane, cudaStream_t s) {
+  launch_pdl(to_operand_kernel, dim3(n_rows), dim3(kRowThreads), 0, s, src, width, op, plane);
+}
+
+void launch_argmax(const float* logits, int n_rows, int V, int32_t* tokens, cudaStream_t s) {
+  launch_pdl(argmax_kernel, dim3(n_rows), dim3(kRowThreads), 0, s, logits, V, tokens);
 }
 
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s) {

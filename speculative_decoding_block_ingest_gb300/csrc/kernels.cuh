@@ -180,6 +180,8 @@ void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s);
 const void* init_kernel_entry();       // kernel function addresses, to find
 const void* final_norm_kernel_entry(); // their nodes in a captured graph
 void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s);
+void launch_to_operand(const float* src, int n_rows, int width, void* op, long plane, cudaStream_t s);
+void launch_argmax(const float* logits, int n_rows, int V, int32_t* tokens, cudaStream_t s);
 void launch_kv_read(const Geo& g, const void* kpool, const void* vpool, const int* block_table,
                     int slot, int layer, int row0, int nrows, float* k_out, float* v_out,
                     cudaStream_t s);

@@ -429,8 +429,8 @@ struct GemmSpec {
   EpiArgs e;
 };
 
-// Passes of <= 256 token columns; tensor cores for bf16 weights, CUDA cores
-// for f32 weights (and, for now, fp8 weights).
+// Passes of <= 256 token columns; tensor cores for bf16 and e4m3 weights
+// (stored as bf16 blocks), CUDA cores for f32 weights.
 void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
   const Geo& g = h->g;
   const int n_all = sp.e.n_tok;
@@ -465,7 +465,7 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     else if (sp.e.kind == EPI_SWIGLU) out_b = nt * sp.N / 2 * 4;
     else if (sp.e.kind == EPI_FC) out_b = nt * sp.N * 4;
     else out_b = nt * sp.N * (g.kvtype == KV_F32 ? 4 : 2);
-    const double bytes = (double)sp.N * sp.K * esize_w(g.wtype) + (g.wtype == W_FP8 ? sp.N * 4.0 : 0.0) + x_b + out_b;
+    const double bytes = (double)sp.N * sp.K * esize_w(g.wtype) + (sp.wscale ? sp.N * 4.0 : 0.0) + x_b + out_b;
     Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
     a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_GEMM, a.p.grid) : nullptr;
     if (h->use_tc) launch_gemm_tc(a, sp.xmap, s);
@@ -1403,6 +1403,85 @@ int dflash_seq_len(dflash_t* h, int32_t seq_id, int64_t* len) {
   if (seq_id < 0 || seq_id >= h->cfg.max_seqs) return fail(DFLASH_ERR_INVALID_ARG, "seq id %d out of range", seq_id);
   *len = h->len[seq_id];
   return DFLASH_OK;
+}
+
+// ---------------------------------------------------------------- draft tokens
+static size_t lm_blocks_bytes(const dflash_t* h, int32_t vocab) {
+  return ((size_t)vocab * h->g.H * 2 + 255) / 256 * 256;
+}
+
+static int check_lm(const dflash_t* h, int32_t vocab) {
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
+  if (!h->use_tc) return fail(DFLASH_ERR_UNSUPPORTED, "draft tokens need bf16 or e4m3 drafter weights");
+  if (vocab <= 0 || vocab % kTileN) return fail(DFLASH_ERR_INVALID_ARG, "vocab must be a positive multiple of 128");
+  return DFLASH_OK;
+}
+
+int dflash_lm_head_bytes(const dflash_t* h, int32_t vocab, size_t* bytes) {
+  g_last_error.clear();
+  if (int rc = check_lm(h, vocab)) return rc;
+  if (!bytes) return fail(DFLASH_ERR_INVALID_ARG, "bytes is null");
+  *bytes = lm_blocks_bytes(h, vocab) + (size_t)h->lo.Mt * vocab * 4;
+  return DFLASH_OK;
+}
+
+int dflash_pack_lm_head(dflash_t* h, const void* lm_head, int32_t vocab, void* packed, size_t bytes, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_lm(h, vocab)) return rc;
+  if (!lm_head || !packed) return fail(DFLASH_ERR_INVALID_ARG, "lm_head / packed is null");
+  if (!aligned16(lm_head)) return fail(DFLASH_ERR_INVALID_ARG, "lm_head must start on a 16-byte boundary");
+  if (reinterpret_cast<uintptr_t>(packed) % 256) return fail(DFLASH_ERR_INVALID_ARG, "packed must be 256-byte aligned");
+  if (bytes < lm_blocks_bytes(h, vocab) + (size_t)h->lo.Mt * vocab * 4)
+    return fail(DFLASH_ERR_CAPACITY, "packed buffer smaller than dflash_lm_head_bytes");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return guarded([&]() -> int {
+    launch_repack(packed, h->g.H, lm_head, vocab, vocab, 0, 0, s);
+    ck(cudaGetLastError(), "lm_head repack");
+    return DFLASH_OK;
+  });
+}
+
+int dflash_draft_tokens(dflash_t* h, int32_t n_seq, const float* hidden, const void* packed, int32_t vocab,
+                        int32_t* tokens, void* stream) {
+  g_last_error.clear();
+  if (int rc = check_lm(h, vocab)) return rc;
+  if (!hidden || !packed || !tokens) return fail(DFLASH_ERR_INVALID_ARG, "null argument");
+  if (n_seq < 1 || n_seq > h->cfg.max_batch) return fail(DFLASH_ERR_INVALID_ARG, "n_seq out of range");
+  if (!aligned16(hidden)) return fail(DFLASH_ERR_INVALID_ARG, "hidden must start on a 16-byte boundary");
+  if (reinterpret_cast<uintptr_t>(packed) % 256) return fail(DFLASH_ERR_INVALID_ARG, "packed must be 256-byte aligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int n_tok = n_seq * kBlock;
+  return guarded([&]() -> int {
+    const Geo& g = h->g;
+    float* logits = reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(packed)) + lm_blocks_bytes(h, vocab));
+    {
+      Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * 8, s);
+      launch_to_operand(hidden, n_tok, g.H, h->at<void>(h->lo.op_h), (long)h->lo.Mt * g.H, s);
+    }
+    ck(cudaGetLastError(), "lm_head operand launch");
+    ck(cudaMemsetAsync(logits, 0, (size_t)n_tok * vocab * 4, s), "logits clear");
+    GemmSpec sp;
+    sp.site = 0;
+    sp.W = packed;
+    sp.wscale = nullptr;
+    sp.N = vocab;
+    sp.K = g.H;
+    sp.X = h->at<void>(h->lo.op_h);
+    sp.xmap = &h->xmap_h;
+    sp.omode = O_RED;
+    sp.dst = logits;
+    sp.dst_ld = vocab;
+    sp.e = base_epi(h);
+    sp.e.n_tok = n_tok;
+    run_gemm(h, sp, s);
+    {
+      Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * vocab * 4, s);
+      launch_argmax(logits, n_tok, vocab, tokens, s);
+    }
+    ck(cudaGetLastError(), "argmax launch");
+    h->last_stream = s;
+    return DFLASH_OK;
+  });
 }
 
 int dflash_kv_read(dflash_t* h, int32_t seq_id, int32_t layer, int32_t row0, int32_t nrows, float* k_out,

@@ -24,7 +24,8 @@ ROPE_PLAIN, ROPE_YARN = 0, 1
 _DT = {"f32": F32, "bf16": BF16, "fp8": FP8}
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dflash_forward_round",
-           "dflash_forward_full", "dflash_forward_full_static", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
+           "dflash_forward_full", "dflash_forward_full_static", "dflash_lm_head_bytes", "dflash_pack_lm_head",
+           "dflash_draft_tokens", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
            "dflash_device_status", "dflash_destroy", "dflash_last_error", "dflash_profile_enable",
            "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches")
 TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
@@ -75,6 +76,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_forward_round.argtypes = [vp, i32, p32, p32, vp, vp, vp]
     lib.dflash_forward_full.argtypes = [vp, i32, vp, vp, p32, vp, vp]
     lib.dflash_forward_full_static.argtypes = [vp, i32, vp, vp, p32, vp, vp]
+    lib.dflash_lm_head_bytes.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_size_t)]
+    lib.dflash_pack_lm_head.argtypes = [vp, vp, i32, vp, ctypes.c_size_t, vp]
+    lib.dflash_draft_tokens.argtypes = [vp, i32, vp, vp, i32, vp, vp]
     lib.dflash_seq_reset.argtypes = [vp, i32]
     lib.dflash_seq_len.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.dflash_kv_read.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
@@ -224,6 +228,28 @@ class Drafter:
                                                    ctypes.c_void_p(noise.data_ptr()), _i32(pos),
                                                    ctypes.c_void_p(out.data_ptr()), _stream_ptr(stream)))
         return out
+
+    def pack_lm_head(self, lm_head: torch.Tensor, stream=None):
+        """Pack a bf16 [vocab, H] lm_head for draft_tokens; returns the packed
+        buffer (device, owned by the caller) and vocab."""
+        vocab = lm_head.shape[0]
+        n = ctypes.c_size_t(0)
+        _check(self.lib.dflash_lm_head_bytes(self.handle, vocab, ctypes.byref(n)))
+        packed = torch.empty(n.value, dtype=torch.uint8, device=self.device)
+        w = lm_head.to(device=self.device, dtype=torch.bfloat16).contiguous()
+        _check(self.lib.dflash_pack_lm_head(self.handle, ctypes.c_void_p(w.data_ptr()), vocab,
+                                            ctypes.c_void_p(packed.data_ptr()), n.value, _stream_ptr(stream)))
+        return packed, vocab
+
+    def draft_tokens(self, hidden: torch.Tensor, packed: torch.Tensor, vocab: int, stream=None) -> torch.Tensor:
+        """Greedy tokens [n_seq, 16] (int32) of hidden [n_seq, 16, H] through a packed lm_head."""
+        hidden = hidden.contiguous()
+        n_seq = hidden.shape[0]
+        tokens = torch.empty(n_seq, 16, dtype=torch.int32, device=self.device)
+        _check(self.lib.dflash_draft_tokens(self.handle, n_seq, ctypes.c_void_p(hidden.data_ptr()),
+                                            ctypes.c_void_p(packed.data_ptr()), vocab,
+                                            ctypes.c_void_p(tokens.data_ptr()), _stream_ptr(stream)))
+        return tokens
 
     def seq_reset(self, seq_id: int):
         _check(self.lib.dflash_seq_reset(self.handle, seq_id))

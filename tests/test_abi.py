@@ -91,3 +91,11 @@ def test_yarn_config_validation(lib):
     rc, _ = _ws(_cfg(rope_type=dflash.ROPE_YARN, yarn_factor=32.0, yarn_original_max_pos=8192,
                      yarn_beta_fast=32.0, yarn_beta_slow=1.0))
     assert rc == 0
+
+
+def test_draft_token_calls_reject_null_handle(lib):
+    import ctypes
+    n = ctypes.c_size_t(0)
+    assert lib.dflash_lm_head_bytes(None, 128, ctypes.byref(n)) == -1
+    assert lib.dflash_pack_lm_head(None, None, 128, None, 0, None) == -1
+    assert lib.dflash_draft_tokens(None, 1, None, None, 128, None, None) == -1

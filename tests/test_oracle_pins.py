@@ -510,3 +510,24 @@ def test_planted_transposed_operand_is_caught(monkeypatch):
         return O.rms_norm(c, self.hidden_norm, self.cfg.rms_eps)
     monkeypatch.setattr(O.Drafter, "ctx_features", bad)
     assert _micro_vs_torch(cfg) > 1e-3
+
+
+def test_argmax_tokens_brute_force_and_ties():
+    """Greedy tokens: brute force over every vocabulary row in plain Python,
+    and equal maxima resolved to the lowest index (module index,
+    dflash2_walk_greedy: torch argmax convention)."""
+    rng = np.random.default_rng(7)
+    hid = rng.integers(-3, 4, size=(6, 8)).astype(np.float64)
+    lm = rng.integers(-3, 4, size=(13, 8)).astype(np.float64)
+    lm[9] = lm[4]
+    lm[12] = lm[4]
+    hid[0] = np.sign(lm[4]) * 5          # rows 4, 9, 12 tie for the maximum
+    got = O.argmax_tokens(hid, lm)
+    for r in range(hid.shape[0]):
+        best, arg = None, None
+        for v in range(lm.shape[0]):
+            val = sum(float(hid[r, k]) * float(lm[v, k]) for k in range(hid.shape[1]))
+            if best is None or val > best:
+                best, arg = val, v
+        assert got[r] == arg
+    assert got[0] == 4
