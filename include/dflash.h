@@ -216,6 +216,19 @@ int dflash_pack_lm_head(dflash_t *h, const void *lm_head, int32_t vocab, void *p
 int dflash_draft_tokens(dflash_t *h, int32_t n_seq, const float *hidden, const void *packed, int32_t vocab,
                         int32_t *tokens, void *stream);
 
+/* Context window (spark_model::layers::dflash_head, dflash_ctx_cap: the
+ * most recent target positions the drafter may accumulate and attend to).
+ * cap = 0: unbounded (the default).  cap > 0: after every ingest a sequence
+ * keeps only its most recent `cap` context positions -- pages wholly older
+ * return to the pool, and the attention masks the older keys of the first
+ * kept page -- and rounds attend to [len - cap, len) plus the block rows.
+ * Setting the cap applies it to every sequence at once; positions already
+ * dropped stay dropped when the cap is raised or cleared.  dflash_seq_len
+ * still counts every committed position (RoPE positions keep growing);
+ * dflash_kv_read rejects rows of dropped pages.  dflash_forward_full is not
+ * windowed (the first-light forward attends to its whole context). */
+int dflash_set_ctx_cap(dflash_t *h, int32_t cap);
+
 /* Drop a sequence's cache (len = 0, pages back to the pool). */
 int dflash_seq_reset(dflash_t *h, int32_t seq_id);
 

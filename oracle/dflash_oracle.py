@@ -285,8 +285,13 @@ class DraftKV:
     layer per sequence.
     """
 
-    def __init__(self, drafter: Drafter):
+    def __init__(self, drafter: Drafter, ctx_cap: int = 0):
+        """``ctx_cap`` > 0: rounds attend to only the most recent ``ctx_cap``
+        cached positions (spark_model::layers::dflash_head, dflash_ctx_cap:
+        the most recent target positions the drafter may accumulate and
+        attend to); 0 = all."""
         self.d = drafter
+        self.ctx_cap = ctx_cap
         self.k: Dict[int, List[np.ndarray]] = {}
         self.v: Dict[int, List[np.ndarray]] = {}
 
@@ -330,7 +335,11 @@ class DraftKV:
         for i, s in enumerate(seqs):
             if s not in self.k:
                 self.ingest(s, np.zeros((0, self.d.cfg.n_taps * self.d.cfg.hidden)), [])
-            out.append(self.d.block_forward(noise[i], pos_block[i], self.k[s], self.v[s]))
+            ks, vs = self.k[s], self.v[s]
+            if self.ctx_cap > 0:
+                ks = [k[-self.ctx_cap:] for k in ks]
+                vs = [v[-self.ctx_cap:] for v in vs]
+            out.append(self.d.block_forward(noise[i], pos_block[i], ks, vs))
         return np.stack(out)
 
 

@@ -118,8 +118,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // kernel's wait; only the pages holding this round's block rows and the
   // query tile (both written by the predecessor) wait for it.
   const int item = blockIdx.x;
-  int s, kvh, k0, k1;
-  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1);
+  int s, kvh, k0, k1, ks;
+  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &ks);
   const int n_pages = (k1 - k0 + kPage - 1) / kPage;
   const int n_chunks = (n_pages + 1) / 2;
   const int slot = a.rd->seq_slot[s];
@@ -244,14 +244,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       tc_fence_after();
       float sc[kPage];
       const uint32_t sbase = tmem + lane_base + 128u + (uint32_t)((c & 1) * kChunk + hg * kPage);
-      const int kc = min(kPage, k1 - (k0 + c * kChunk + hg * kPage));   // valid keys of this half (may be <= 0)
+      const int kbase = k0 + c * kChunk + hg * kPage;
+      const int kc = min(kPage, k1 - kbase);   // valid keys of this half (may be <= 0)
+      const int klo = ks - kbase;              // keys below the window start (first page only)
       float mh = -INFINITY;
       if (ok) {
         tmem_ld32(sbase, sc);
         tmem_ld32(sbase + 32u, sc + 32);
 #pragma unroll
         for (int i = 0; i < kPage; ++i) {
-          sc[i] = (i < kc) ? sc[i] * t.scale_log2 : -INFINITY;
+          sc[i] = (i < kc && i >= klo) ? sc[i] * t.scale_log2 : -INFINITY;
           mh = fmaxf(mh, sc[i]);
         }
       }

@@ -76,6 +76,7 @@ struct RoundDesc {
   int seq_slot[kMaxBatch];
   int len[kMaxBatch];
   int item0[kMaxBatch + 1];        // attention work items of seq s: [item0[s], item0[s+1])
+  int kstart[kMaxBatch];           // first attended key position (context window; 0 = all)
   int pos[kMaxBatch * kBlock];     // absolute position of each block row
   int dest[kMaxBatch * kBlock];    // page*64 + offset of the row's transient K/V
 };
@@ -197,19 +198,23 @@ __device__ __forceinline__ void rope_sincos(int pos, const double* inv_freq, int
 }
 
 // Locate attention work item `item`: sequence s, kv head, and its key range
-// [k0, k1) within [cached context ; 16 block rows].
+// [k0, k1) within [cached context ; 16 block rows], splits counted from the
+// page holding the sequence's first attended key ks (keys below ks, in that
+// first page only, are masked by the kernels).
 __device__ __forceinline__ void attn_item(const RoundDesc* rd, int Hkv, int item, int* s_out, int* g_out,
-                                          int* k0, int* k1) {
+                                          int* k0, int* k1, int* ks = nullptr) {
   int s = 0;
   while (s + 1 < rd->n_seq && rd->item0[s + 1] <= item) ++s;
   const int local = item - rd->item0[s];
   const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / Hkv;
   const int g = local / nsplit, sp = local % nsplit;
   const int n_keys = rd->len[s] + kBlock;
+  const int base = rd->kstart[s] / kPage * kPage;
   *s_out = s;
   *g_out = g;
-  *k0 = sp * rd->split_pages * kPage;
-  *k1 = min(n_keys, (sp + 1) * rd->split_pages * kPage);
+  *k0 = base + sp * rd->split_pages * kPage;
+  *k1 = min(n_keys, base + (sp + 1) * rd->split_pages * kPage);
+  if (ks) *ks = rd->kstart[s];
 }
 
 // ------------------------------------------------------------------ stream-K reduction

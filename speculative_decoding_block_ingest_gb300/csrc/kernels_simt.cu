@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   float* Vs = Ks + kPage * dp;    // [d][65]
   const int tid = threadIdx.x;
   const int item = blockIdx.x;
-  int s, kvh, k0, k1;
-  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1);
+  int s, kvh, k0, k1, ks;
+  attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &ks);
   const int slot = a.rd->seq_slot[s];
   for (int idx = tid; idx < R * d; idx += 128) {
     const int r = idx / d, dim = idx % d;
@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
 #pragma unroll
       for (int j = 0; j < kPage; ++j) {
         float acc = 0.f;
-        if (j < kc) {
+        if (j < kc && kp + j >= ks) {
           for (int dim = 0; dim < d; ++dim) acc = fmaf(Qs[tid * dp + dim], Ks[j * dp + dim], acc);
           acc *= a.scale_log2;
           mx = fmaxf(mx, acc);
@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
       float lsum = 0.f;
 #pragma unroll
       for (int j = 0; j < kPage; ++j) {
-        sc[j] = j < kc ? exp2f(sc[j] - mx) : 0.f;
+        sc[j] = (j < kc && kp + j >= ks) ? exp2f(sc[j] - mx) : 0.f;
         lsum += sc[j];
       }
       l = l * alpha + lsum;

@@ -270,7 +270,12 @@ struct dflash_handle {
   Geo g;
   int n_sm;
   std::vector<int64_t> len;               // committed rows per slot (slot max_seqs = internal)
-  std::vector<std::vector<int>> pages;    // page ids per slot (in the current KV region)
+  std::vector<std::vector<int>> pages;    // page ids per slot (in the current KV region); -1 = evicted
+  // context window (dflash_set_ctx_cap): 0 = unbounded; per slot the first
+  // position still kept and attended
+  int64_t ctx_cap = 0;
+  std::vector<int64_t> kstart;
+  bool evicted_any = false;
   // A KV region: K and V^T pools of `max_pages` pages per layer, their
   // tensor maps and free list.  `pool` lives in the workspace; `fixed` is the
   // library's static device region used by dflash_forward_full_static.
@@ -553,13 +558,14 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
 // The persistent round takes bf16 rounds of up to kMkMaxTok block rows whose
 // projection stage fits at least two ring stages beside the attention buffers.
 bool mk_eligible(dflash_t* h, int n_tok) {
-  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && !h->mk_off && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
+  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && !h->mk_off && !h->evicted_any && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
          round_mk_stages((n_tok + 15) / 16 * 16, h->g.d) >= 2;
 }
 
-int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens) {
+int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int* kstart) {
   long units = 0;
-  for (auto L : lens) units += (long)h->g.Hkv * ((L + kBlock + kPage - 1) / kPage);
+  for (size_t i = 0; i < lens.size(); ++i)
+    units += (long)h->g.Hkv * ((lens[i] + kBlock + kPage - 1) / kPage - kstart[i] / kPage);
   // the persistent round runs one item per CTA: at most n_sm items even after
   // each (sequence, kv head) rounds its split count up
   const bool mk = mk_eligible(h, (int)lens.size() * kBlock);
@@ -851,11 +857,12 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
 
 // Fill the attention split plan of a round descriptor.
 void plan_attention(dflash_t* h, RoundDesc& rd, const std::vector<int64_t>& lens) {
-  rd.split_pages = choose_split_pages(h, lens);
+  rd.split_pages = choose_split_pages(h, lens, rd.kstart);
   int items = 0;
   for (int s = 0; s < rd.n_seq; ++s) {
     rd.item0[s] = items;
-    const int pages = (int)((lens[s] + kBlock + kPage - 1) / kPage);   // context + block rows
+    // pages from the one holding the first attended key through the block rows
+    const int pages = (int)((lens[s] + kBlock + kPage - 1) / kPage - rd.kstart[s] / kPage);
     items += h->g.Hkv * ((pages + rd.split_pages - 1) / rd.split_pages);
   }
   rd.item0[rd.n_seq] = items;
@@ -882,6 +889,24 @@ int check_seq_ids(dflash_t* h, int n_seq, const int32_t* ids) {
     seen[ids[i]] = 1;
   }
   return DFLASH_OK;
+}
+
+// Context window: keep the most recent ctx_cap positions of a sequence.
+// Pages wholly before the window return to the pool; keys before the window
+// in its first page are masked by the attention.  The first-light forward's
+// internal slot keeps its whole context.
+void evict_window(dflash_t* h, int slot) {
+  if (h->ctx_cap <= 0 || slot >= h->cfg.max_seqs) return;
+  const int64_t ks = std::max<int64_t>(h->kstart[slot], h->len[slot] - h->ctx_cap);
+  if (ks <= h->kstart[slot]) return;
+  h->kstart[slot] = ks;
+  auto& pl = h->pages[slot];
+  for (int64_t i = 0; i < ks / kPage && i < (int64_t)pl.size(); ++i)
+    if (pl[i] >= 0) {
+      h->kv->free_pages.push_back(pl[i]);
+      pl[i] = -1;
+    }
+  h->evicted_any = true;
 }
 
 // Validated ingest of rows into explicit slots (used by the public entry and
@@ -929,7 +954,10 @@ int ingest_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* t_
     delete blob;
     return rc;
   }
-  for (int i = 0; i < n_seq; ++i) h->len[slots[i]] += t_per_seq[i];
+  for (int i = 0; i < n_seq; ++i) {
+    h->len[slots[i]] += t_per_seq[i];
+    evict_window(h, slots[i]);
+  }
   h->last_stream = s;
   delete blob;
   return DFLASH_OK;
@@ -1056,6 +1084,7 @@ int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos
     lens[i] = h->len[slot];
     rd.seq_slot[i] = slot;
     rd.len[i] = (int)lens[i];
+    rd.kstart[i] = (int)h->kstart[slot];
     for (int j = 0; j < kBlock; ++j) rd.pos[i * kBlock + j] = pos_block[i * kBlock + j];
     if (!ensure_pages(h, slot, lens[i] + kBlock, *blob, taken)) {
       rollback_pages(h, *blob, taken);
@@ -1084,9 +1113,11 @@ int round_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* pos
 }
 
 void release_slot(dflash_t* h, int slot) {
-  for (int p : h->pages[slot]) h->kv->free_pages.push_back(p);
+  for (int p : h->pages[slot])
+    if (p >= 0) h->kv->free_pages.push_back(p);
   h->pages[slot].clear();
   h->len[slot] = 0;
+  h->kstart[slot] = 0;
 }
 
 // Makes `r` the region the enqueued kernels use (pools, maps, free list and
@@ -1189,6 +1220,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   rope_table(*cfg, inv, g.mscale);
   h->len.assign(cfg->max_seqs + 1, 0);
   h->pages.assign(cfg->max_seqs + 1, {});
+  h->kstart.assign(cfg->max_seqs + 1, 0);
   h->pool.kpool = h->ws + lo.kpool;
   h->pool.vpool = h->ws + lo.vpool;
   h->pool.max_pages = cfg->max_pages;
@@ -1389,6 +1421,15 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
   return first_light(h, ctx, taps, noise_emb, pos, out, s);
 }
 
+int dflash_set_ctx_cap(dflash_t* h, int32_t cap) {
+  g_last_error.clear();
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
+  if (cap < 0) return fail(DFLASH_ERR_INVALID_ARG, "negative context cap");
+  h->ctx_cap = cap;
+  for (int slot = 0; slot < h->cfg.max_seqs; ++slot) evict_window(h, slot);
+  return DFLASH_OK;
+}
+
 int dflash_seq_reset(dflash_t* h, int32_t seq_id) {
   g_last_error.clear();
   if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
@@ -1493,6 +1534,9 @@ int dflash_kv_read(dflash_t* h, int32_t seq_id, int32_t layer, int32_t row0, int
   if (row0 < 0 || nrows < 0 || row0 + (int64_t)nrows > h->len[seq_id])
     return fail(DFLASH_ERR_INVALID_ARG, "rows [%d, %d) outside the %lld committed rows", row0, row0 + nrows,
                 (long long)h->len[seq_id]);
+  if (nrows > 0 && row0 / kPage < h->kstart[seq_id] / kPage)
+    return fail(DFLASH_ERR_INVALID_ARG, "rows before %lld were evicted by the context window",
+                (long long)(h->kstart[seq_id] / kPage * kPage));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return guarded([&]() -> int {
     launch_kv_read(h->g, h->at<void>(h->lo.kpool), h->at<void>(h->lo.vpool), h->at<int>(h->lo.btab), seq_id, layer,

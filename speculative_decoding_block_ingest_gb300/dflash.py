@@ -25,7 +25,7 @@ _DT = {"f32": F32, "bf16": BF16, "fp8": FP8}
 
 EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dflash_forward_round",
            "dflash_forward_full", "dflash_forward_full_static", "dflash_lm_head_bytes", "dflash_pack_lm_head",
-           "dflash_draft_tokens", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
+           "dflash_draft_tokens", "dflash_set_ctx_cap", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
            "dflash_device_status", "dflash_destroy", "dflash_last_error", "dflash_profile_enable",
            "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches")
 TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
@@ -80,6 +80,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_pack_lm_head.argtypes = [vp, vp, i32, vp, ctypes.c_size_t, vp]
     lib.dflash_draft_tokens.argtypes = [vp, i32, vp, vp, i32, vp, vp]
     lib.dflash_seq_reset.argtypes = [vp, i32]
+    lib.dflash_set_ctx_cap.argtypes = [vp, i32]
     lib.dflash_seq_len.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.dflash_kv_read.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
     lib.dflash_device_status.argtypes = [vp, vp]
@@ -250,6 +251,10 @@ class Drafter:
                                             ctypes.c_void_p(packed.data_ptr()), vocab,
                                             ctypes.c_void_p(tokens.data_ptr()), _stream_ptr(stream)))
         return tokens
+
+    def set_ctx_cap(self, cap: int):
+        """Keep and attend to only the most recent `cap` context positions (0: all)."""
+        _check(self.lib.dflash_set_ctx_cap(self.handle, cap))
 
     def seq_reset(self, seq_id: int):
         _check(self.lib.dflash_seq_reset(self.handle, seq_id))

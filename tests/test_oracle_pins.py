@@ -531,3 +531,28 @@ def test_argmax_tokens_brute_force_and_ties():
                 best, arg = val, v
         assert got[r] == arg
     assert got[0] == 4
+
+
+def test_context_window_equals_first_light_on_the_last_rows():
+    """A round over a cache windowed to the last W positions equals the
+    first-light forward over just those W context rows (same positions):
+    the window drops keys, and RoPE depends only on the kept positions."""
+    cfg = synth.TINY_F32
+    D = O.Drafter(cfg, oracle_weights(synth.make_weights(cfg)))
+    ctx, W = 150, 70
+    taps = synth.taps_rows(cfg, 0, 0, ctx).double().numpy()
+    noise = synth.noise_rows(cfg, 0, 0).double().numpy()
+    kv = O.DraftKV(D, ctx_cap=W)
+    kv.ingest(0, taps[:90], list(range(90)))
+    kv.ingest(0, taps[90:], list(range(90, ctx)))
+    got = kv.forward_round([0], noise[None], np.arange(ctx, ctx + 16)[None])[0]
+    ref = D.forward_full(taps[ctx - W:], noise, list(range(ctx - W, ctx)) + list(range(ctx, ctx + 16)))
+    assert np.max(np.abs(got - ref)) < 1e-10 * max(1.0, np.max(np.abs(ref)))
+    # a window at least as long as the context changes nothing
+    full = O.DraftKV(D)
+    full.ingest(0, taps, list(range(ctx)))
+    wide = O.DraftKV(D, ctx_cap=ctx)
+    wide.ingest(0, taps, list(range(ctx)))
+    a = full.forward_round([0], noise[None], np.arange(ctx, ctx + 16)[None])
+    b = wide.forward_round([0], noise[None], np.arange(ctx, ctx + 16)[None])
+    assert np.array_equal(a, b)

@@ -185,3 +185,48 @@ def test_invalid_calls_change_no_state():
     assert dr.seq_len(0) == 0
     torch.cuda.synchronize()
     dr.device_status()
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY_F32, SMALL_BF16], ids=["tiny_f32", "small_bf16"])
+def test_context_window_matches_oracle(cfg):
+    """Context window of 100 positions over ragged sequences that outgrow it:
+    every round equals the windowed oracle; the pool is sized so that the
+    ingests only fit because pages past the window are returned; rows of
+    returned pages cannot be read back."""
+    from speculative_decoding_block_ingest_gb300 import dflash
+    W = 100
+    # 13 pages: the last ingest needs 13 live pages with eviction and 14
+    # without it
+    dr, D = _setup(cfg, max_seqs=3, max_pages=13, max_seq_len=2048, max_batch=3, max_ingest_rows=512)
+    dr.set_ctx_cap(W)
+    kv = O.DraftKV(D, ctx_cap=W)
+    seqs = [0, 1, 2]
+    lens = {0: 0, 1: 0, 2: 0}
+    plan = [[70, 5, 130], [60, 200, 1], [170, 60, 100]]
+    for rnd, ts in enumerate(plan):
+        pos_new, taps = [], []
+        for s, t in zip(seqs, ts):
+            taps.append(synth.taps_rows(cfg, s, lens[s], t))
+            pos_new += list(range(lens[s], lens[s] + t))
+        taps_all = torch.cat(taps)
+        dr.ingest(seqs, ts, pos_new, taps_all.to(DEV))
+        r = 0
+        for s, t in zip(seqs, ts):
+            kv.ingest(s, taps_all[r:r + t].double().numpy(), pos_new[r:r + t])
+            r += t
+            lens[s] += t
+        noise = torch.stack([synth.noise_rows(cfg, s, rnd) for s in seqs])
+        pos_block = [p for s in seqs for p in range(lens[s], lens[s] + 16)]
+        got = dr.forward_round(seqs, pos_block, noise.to(DEV))
+        torch.cuda.synchronize()
+        dr.device_status()
+        ref = kv.forward_round(seqs, noise.double().numpy(), np.array(pos_block).reshape(len(seqs), 16))
+        for i in range(len(seqs)):
+            assert rel_err(_np(got[i]), ref[i]) <= tol(cfg), (rnd, i)
+        for s in seqs:
+            assert dr.seq_len(s) == lens[s]
+    with pytest.raises(dflash.DflashError):
+        dr.kv_read(0, 0, 0, 16)          # the first rows of sequence 0 were returned to the pool
+    k, v = dr.kv_read(0, 0, lens[0] - 16, 16)
+    torch.cuda.synchronize()
+    assert rel_err(_np(k), kv.k[0][0][-16:]) <= tol(cfg)
