@@ -186,8 +186,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       trace_mark(a.trace, blockIdx.x, 2, c0);                   // 2: query tile ready
       const uint32_t q_addr = smem_u32(sQ);
       auto kv_addr = [&](int c) -> uint32_t { return smem_u32(sKV + (c % t.stages) * t.stage_bytes); };
-      auto issue_s = [&](int c) -> bool {
-        if (!mbar_wait(&kvfull[c % t.stages], (c / t.stages) & 1, &flags[0])) return false;
+      // S(c) = Q K(c)^T, once the caller has seen chunk c's keys land
+      auto issue_s = [&](int c) {
         tc_fence_after();
         const uint32_t k_addr = kv_addr(c);
         const uint32_t d_s = tmem + 128u + (uint32_t)((c & 1) * kChunk);
@@ -198,15 +198,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                    t.idesc_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&sfull[c & 1]);
-        return true;
       };
-      if (ok && n_chunks > 0) ok = issue_s(0);
-      if (ok && n_chunks > 1) ok = issue_s(1);
-      for (int c = 0; c < n_chunks && ok; ++c) {
-        if (!mbar_wait(&pfull[c & 1], (c >> 1) & 1, &flags[0])) {
-          ok = false;
-          break;
-        }
+      // O += P(c) V(c)^T, once the caller has seen softmax(c) publish P
+      auto issue_pv = [&](int c) {
         tc_fence_after();
         const uint32_t p_addr = smem_u32(sP + (c & 1) * kPBytes);
         const uint32_t v_addr = kv_addr(c) + (uint32_t)(t.datoms * kQAtomBytes);
@@ -219,7 +213,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit(&pvdone[c & 1]);
         mma_commit(&kvempty[c % t.stages]);
-        if (c + 2 < n_chunks) ok = issue_s(c + 2);
+      };
+      // Issue in dependency order rather than program order: S(ns) once its
+      // keys have landed and S buffer ns&1 is free (softmax(ns-2) is done
+      // with it, which PV(ns-2) having been issued implies); PV(np) once
+      // softmax(np) has written P.  Polling both keeps a K/V refill still in
+      // flight from holding back the P V^T of the chunk before it, whose
+      // completion frees the next stage.
+      int ns = 0, np = 0;
+      uint64_t t_last = globaltimer();
+      while (ok && np < n_chunks) {
+        bool prog = false;
+        if (np < ns && mbar_try_wait(&pfull[np & 1], (np >> 1) & 1)) {
+          issue_pv(np++);
+          prog = true;
+        }
+        if (ns < n_chunks && ns <= np + 1 && mbar_try_wait(&kvfull[ns % t.stages], (ns / t.stages) & 1)) {
+          issue_s(ns++);
+          prog = true;
+        }
+        if (prog) t_last = globaltimer();
+        else if (flags[0] || globaltimer() - t_last > kWaitNs) ok = false;
       }
       if (!ok) flags[0] = 1;
       trace_mark(a.trace, blockIdx.x, 3, c0);                   // 3: last MMA issued

@@ -563,15 +563,38 @@ bool mk_eligible(dflash_t* h, int n_tok) {
 }
 
 int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int* kstart) {
-  long units = 0;
-  for (size_t i = 0; i < lens.size(); ++i)
-    units += (long)h->g.Hkv * ((lens[i] + kBlock + kPage - 1) / kPage - kstart[i] / kPage);
+  std::vector<long> pages(lens.size());
+  long units = 0, longest = 1;
+  for (size_t i = 0; i < lens.size(); ++i) {
+    pages[i] = (lens[i] + kBlock + kPage - 1) / kPage - kstart[i] / kPage;
+    units += (long)h->g.Hkv * pages[i];
+    longest = std::max(longest, pages[i]);
+  }
   // the persistent round runs one item per CTA: at most n_sm items even after
   // each (sequence, kv head) rounds its split count up
   const bool mk = mk_eligible(h, (int)lens.size() * kBlock);
-  const long target = mk ? std::max<long>(1, (long)h->n_sm - (long)h->g.Hkv * (long)lens.size())
-                         : (h->attn_tc ? (long)h->n_sm : 2L * h->n_sm);
-  return (int)std::max<long>(1, (units + target - 1) / target);
+  if (mk) {
+    const long target = std::max<long>(1, (long)h->n_sm - (long)h->g.Hkv * (long)lens.size());
+    return (int)std::max<long>(1, (units + target - 1) / target);
+  }
+  // Items run in waves of `slots` CTAs and each walks its pages serially, so
+  // take the split that minimises waves x (pages per item + a fixed per-item
+  // cost of about two chunks); among equals the larger split (fewer partials
+  // to merge).
+  const long slots = h->attn_tc ? (long)h->n_sm : 2L * h->n_sm;
+  constexpr long kItemCost = 4;
+  long best = 1, best_cost = -1;
+  for (long sp = 1; sp <= longest; ++sp) {
+    long items = 0;
+    for (long p : pages) items += (long)h->g.Hkv * ((p + sp - 1) / sp);
+    if (items > h->lo.items_cap) continue;   // sp = longest always fits: Hkv items a sequence
+    const long cost = (items + slots - 1) / slots * (sp + kItemCost);
+    if (best_cost < 0 || cost <= best_cost) {
+      best = sp;
+      best_cost = cost;
+    }
+  }
+  return (int)best;
 }
 
 // Arguments of a round's init kernel (copied into the kernel's parameters).
