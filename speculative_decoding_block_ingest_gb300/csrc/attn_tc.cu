@@ -8,20 +8,22 @@
 // one S tile per chunk halves the serial S -> softmax -> P V^T steps of a
 // split.
 //   warp 0 (one lane)  TMA: the query tile, then the split's K pages [64 x d]
-//                      and V^T pages [d x 64] into a ring of two chunk stages
-//                      (a chunk's two K pages stacked to one 128-key
-//                      operand);
+//                      and V^T pages [d x 64] into a ring of chunk stages
+//                      (three at d = 128; a chunk's two K pages stacked to
+//                      one 128-key operand);
 //   warp 1 (one lane)  tcgen05.mma: S = Q K^T (N = 128) into one of two TMEM
-//                      buffers, then O += P V^T into the TMEM accumulator;
+//                      buffers, then O += P V^T into the TMEM accumulator
+//                      with P read from TMEM, issued in dependency order;
 //   warps 2..9         softmax, two threads per query row (warps 2..5 the
 //                      chunk's first 64 keys, warps 6..9 the other 64; the
 //                      two halves trade their maxima through TMEM): scores
-//                      from TMEM, exp2 with a running max, P (bf16) into one
-//                      of two shared-memory buffers in the 128-byte swizzle
-//                      the MMA reads, so chunk c+1's softmax overlaps chunk
-//                      c's P V^T.  O is rescaled only when a row's max grows
-//                      by more than 2^8 (exact: the final division uses the
-//                      same max); each half rescales half of O's columns.
+//                      from TMEM, exp2 with a running max, P (bf16 pairs)
+//                      written back over the half's own scores, so chunk
+//                      c+1's softmax overlaps chunk c's P V^T and shared
+//                      memory holds only Q and the K/V ring.  O is rescaled
+//                      only when a row's max grows by more than 2^8 (exact:
+//                      the final division uses the same max); each half
+//                      rescales half of O's columns.
 // Each item writes its unnormalised O with (max, sum); the combine kernel
 // merges the splits (all in log2 units).
 #include <algorithm>
@@ -47,7 +49,7 @@ constexpr int kSmBar = 3;                // their named barrier
 constexpr int kQAtomBytes = 128 * 128;   // 128 rows x 128 B
 constexpr int kKAtomBytes = 64 * 128;    // 64 keys x 128 B (one page of one K-atom)
 constexpr int kChunk = 2 * kPage;        // keys per S tile
-constexpr int kPBytes = 2 * kQAtomBytes; // P tile: 128 rows x 128 keys bf16 (two atoms)
+constexpr int kMaxAttnStages = 4;
 constexpr float kRescaleLog2 = 8.f;
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -57,8 +59,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Geo& g = a.g;
   uint8_t* sQ = smem;                                   // datoms x 16 KB
-  uint8_t* sP = sQ + t.datoms * kQAtomBytes;            // 2 x 32 KB (P of chunks c, c+1)
-  uint8_t* sKV = sP + 2 * kPBytes;                      // stages x stage_bytes
+  uint8_t* sKV = sQ + t.datoms * kQAtomBytes;           // stages x stage_bytes
   uint8_t* ctl = sKV + t.stages * t.stage_bytes;
   uint64_t* kvfull = reinterpret_cast<uint64_t*>(ctl);
   uint64_t* kvempty = kvfull + t.stages;
@@ -109,7 +110,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   __syncwarp();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;                     // O: cols [0, d); S buffers at 128 and 256
+  const uint32_t tmem = *tmem_slot;                     // O: cols [0, d); S / P buffers at 128 and 256
   if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 1, c0);  // 1: set-up done
 
   // The descriptor, the page table and the cached-context pages were written
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       };
       auto chunk_bytes = [&](int c) { return (uint32_t)(pages_in(c) * (t.datoms * kKAtomBytes + (int)vbytes)); };
       bool ok = true;
-      int deferred[2 * 4];
+      int deferred[2 * kMaxAttnStages];
       int nd = 0;
       // the first chunk stages are free: announce them and fetch their
       // context-only pages before the launch wait
@@ -199,24 +200,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit(&sfull[c & 1]);
       };
-      // O += P(c) V(c)^T, once the caller has seen softmax(c) publish P
+      // O += P(c) V(c)^T, once the caller has seen softmax(c) publish P.
+      // P of key half h sits in columns [64h, 64h + 32) of S buffer c&1
+      // (two keys per column), so a 16-key step reads 8 columns.
       auto issue_pv = [&](int c) {
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(sP + (c & 1) * kPBytes);
+        const uint32_t p_tmem = tmem + 128u + (uint32_t)((c & 1) * kChunk);
         const uint32_t v_addr = kv_addr(c) + (uint32_t)(t.datoms * kQAtomBytes);
         const int steps = pages_in(c) * (kPage / 16);   // 16 keys per MMA; a missing second page is skipped
         for (int kk = 0; kk < steps; ++kk) {
-          const int pa = kk >> 2;                        // page (P atom / V^T slot) of this K-step
+          const int pa = kk >> 2;                        // page (key half / V^T slot) of this K-step
           const uint64_t adv = (uint64_t)((kk & 3) * 32) >> 4;
-          mma_bf16(tmem, desc_sw128(p_addr + pa * kQAtomBytes) + adv, desc_sw128(v_addr + pa * vbytes) + adv,
-                   t.idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem, p_tmem + (uint32_t)(pa * kPage + (kk & 3) * 8), desc_sw128(v_addr + pa * vbytes) + adv,
+                      t.idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&pvdone[c & 1]);
         mma_commit(&kvempty[c % t.stages]);
       };
       // Issue in dependency order rather than program order: S(ns) once its
       // keys have landed and S buffer ns&1 is free (softmax(ns-2) is done
-      // with it, which PV(ns-2) having been issued implies); PV(np) once
+      // with it and PV(ns-2), which reads P from it, was issued before: the
+      // tensor pipe runs one thread's MMAs in issue order); PV(np) once
       // softmax(np) has written P.  Polling both keeps a K/V refill still in
       // flight from holding back the P V^T of the chunk before it, whose
       // completion frees the next stage.
@@ -282,16 +286,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         continue;
       }
       const bool need = mj > m_run + kRescaleLog2;
-      // P buffer c&1 is free once O += P V^T of chunk c-2 has completed
-      if (c >= 2) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&pvdone[c & 1], ((c - 2) >> 1) & 1, &flags[0]))) {
-          ok = false;
-          mbar_arrive(&pfull[c & 1]);
-          continue;
-        }
-        __syncwarp();
-        tc_fence_after();
-      }
       const bool resc = __any_sync(0xffffffffu, need && c > 0);
       // rescaling O needs every product issued so far (through chunk c-1) done
       if (resc) {
@@ -315,22 +309,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       }
       if (need) m_run = mj;
       float lsum = 0.f;
-      uint8_t* prow = sP + (c & 1) * kPBytes + hg * kQAtomBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      // P over this half's own scores (both halves loaded theirs before the
+      // max exchange): 32 columns of bf16 pairs
+      float pw[kPage / 2];
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t w[4];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const float p0 = ex2_fast(sc[8 * cc + 2 * h] - m_run);
-          const float p1 = ex2_fast(sc[8 * cc + 2 * h + 1] - m_run);
-          lsum += p0 + p1;
-          const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-          w[h] = *reinterpret_cast<const uint32_t*>(&b);
-        }
-        *reinterpret_cast<uint4*>(prow + ((cc ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int i = 0; i < kPage / 2; ++i) {
+        const float p0 = ex2_fast(sc[2 * i] - m_run);
+        const float p1 = ex2_fast(sc[2 * i + 1] - m_run);
+        lsum += p0 + p1;
+        const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+        pw[i] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&b));
       }
+      tmem_st32(sbase, pw);
       l_run += lsum;
-      fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(&pfull[c & 1]);
     }
@@ -379,7 +370,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 size_t attn_tc_smem_bytes(int d, int stages) {
   const int datoms = d / 64;
   const int stage_bytes = datoms * kQAtomBytes + 2 * d * 128;
-  return (size_t)datoms * kQAtomBytes + 2 * kPBytes + (size_t)stages * stage_bytes + 256 + 1024;
+  return (size_t)datoms * kQAtomBytes + (size_t)stages * stage_bytes + 256 + 1024;
+}
+
+// As many chunk stages as 227 KB of shared memory holds (at most four).
+static int attn_tc_stages(int d) {
+  int st = kMaxAttnStages;
+  while (st > 2 && attn_tc_smem_bytes(d, st) > 227u * 1024u) --st;
+  return st;
 }
 
 void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
@@ -388,7 +386,7 @@ void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const 
   const int d = a.g.d;
   t.datoms = d / 64;
   t.stage_bytes = t.datoms * kQAtomBytes + 2 * d * 128;
-  t.stages = 2;
+  t.stages = attn_tc_stages(d);
   t.idesc_s = idesc_bf16(128, kChunk);
   t.idesc_o = idesc_bf16(128, d);
   t.scale_log2 = 1.4426950408889634f / std::sqrt((float)d);
