@@ -38,14 +38,16 @@ struct TcCfg {
 
 constexpr int kTcThreads = 224;   // warps: 0 producer, 1 and 6 MMA issuers, 2..5 drain
 constexpr int kWTileBytes = kTileN * kTileK * 2;   // 16 KB
-constexpr int kXBox = 16;                           // operand rows per TMA box
+constexpr int kXBox = 16;                           // operand rows per short TMA box
+constexpr int kXBoxTall = 128;                      // operand rows per tall TMA box
 
 // One CTA per SM with a deep ring: every stage it can hold is filled with
 // weights before the programmatic-launch wait, so HBM keeps streaming while
 // the small kernel before it finishes.
 template <bool kFused, int kIss>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, GemmArgs a, TcCfg t) {
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmXT, GemmArgs a,
+                   TcCfg t) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ctl = smem + t.stages * t.stage_bytes;
@@ -78,6 +80,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     flags[0] = flags[1] = 0;
     fence_barrier_init();
     tma_prefetch_map(&tmX);
+    if (t.nt >= kXBoxTall) tma_prefetch_map(&tmXT);
   }
   if (warp == 1) tmem_alloc(tmem_slot, t.tmem_cols);
   tc_fence_before();
@@ -117,7 +120,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int y_hi = a.e.tok_base, y_lo = t.x_row_lo + a.e.tok_base;
       int kx = (u0 % p.kb) * kTileK;                        // operand column of the next unit
       auto load_x = [&](uint8_t* st, uint64_t* bar) {
-        for (int r = 0; r < t.nt; r += kXBox) {
+        // 128-row boxes while they fit in the pass, then 16-row boxes, so
+        // the boxes tile exactly nt rows of each plane
+        int r = 0;
+        for (; r + kXBoxTall <= t.nt; r += kXBoxTall) {
+          tma_load_2d(st + kWTileBytes + r * 128, &tmXT, bar, kx, y_hi + r);
+          tma_load_2d(st + kWTileBytes + x_plane_bytes + r * 128, &tmXT, bar, kx, y_lo + r);
+        }
+        for (; r < t.nt; r += kXBox) {
           tma_load_2d(st + kWTileBytes + r * 128, &tmX, bar, kx, y_hi + r);
           tma_load_2d(st + kWTileBytes + x_plane_bytes + r * 128, &tmX, bar, kx, y_lo + r);
         }
@@ -344,8 +354,9 @@ void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s) {
       return;   // the launch below is skipped; the caller's cudaGetLastError reports it
     attr_bytes[var] = smem;
   }
+  // tmap_x: the operand's [16-row, 128-row] box maps
   const CUtensorMap* mx = static_cast<const CUtensorMap*>(tmap_x);
-  launch_pdl(kern, dim3(a.p.grid), dim3(kTcThreads), smem, s, *mx, a, t);
+  launch_pdl(kern, dim3(a.p.grid), dim3(kTcThreads), smem, s, mx[0], mx[1], a, t);
 }
 
 }  // namespace dfl

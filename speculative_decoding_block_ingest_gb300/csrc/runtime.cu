@@ -292,7 +292,8 @@ struct dflash_handle {
   // measurement: kernel launches issued, and (when enabled) per-kind event pairs
   int64_t launches = 0;
   // tensor maps of the tensor-core projections' operands (per buffer)
-  CUtensorMap xmap_taps, xmap_h, xmap_o, xmap_a;
+  // operand maps: [0] boxes of 16 rows, [1] boxes of 128 rows (passes of >= 128 tokens)
+  CUtensorMap xmap_taps[2], xmap_h[2], xmap_o[2], xmap_a[2];
   CUtensorMap qmap;                             // attention: q buffer (3-D)
   bool use_tc = false;    // tensor-core projections (bf16 weights)
   bool attn_tc = false;   // tensor-core attention (bf16 KV, any weights)
@@ -427,7 +428,7 @@ struct GemmSpec {
   const float* wscale;
   int N, K;
   const void* X = nullptr;      // operand planes (bf16 hi/lo, or f32)
-  const CUtensorMap* xmap = nullptr;
+  const CUtensorMap* xmap = nullptr;   // [short, tall] operand maps
   int omode = O_TILE;
   float* dst = nullptr;         // O_RED destination [tok][dst_ld]
   int dst_ld = 0;
@@ -525,7 +526,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   fc.N = g.H;
   fc.K = width;
   fc.X = h->at<void>(h->lo.op_taps);
-  fc.xmap = &h->xmap_taps;
+  fc.xmap = h->xmap_taps;
   fc.e = base_epi(h);
   fc.e.kind = EPI_FC;
   fc.e.n_tok = n_rows;
@@ -545,7 +546,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   kv.N = g.L * g.kv_n;
   kv.K = g.H;
   kv.X = h->at<void>(h->lo.op_h);
-  kv.xmap = &h->xmap_h;
+  kv.xmap = h->xmap_h;
   kv.e = base_epi(h);
   kv.e.kind = EPI_KV;
   kv.e.n_tok = n_rows;
@@ -692,7 +693,7 @@ void enqueue_round_mk(dflash_t* h, const RoundDesc& rd, float* out, cudaStream_t
   a.trace = trace_slot(h, DFLASH_KERNEL_ROUND, grid * (kMkTraceWords / kTraceWords));
   {
     Launch L(h, DFLASH_KERNEL_ROUND, bytes, s);
-    ck(launch_round_mk(a, grid, &h->xmap_h, &h->xmap_o, &h->xmap_a, &h->qmap, &h->kv->kmap, &h->kv->vmap, s),
+    ck(launch_round_mk(a, grid, h->xmap_h, h->xmap_o, h->xmap_a, &h->qmap, &h->kv->kmap, &h->kv->vmap, s),
        "persistent round launch");
   }
   h->mk_parity ^= 1;
@@ -760,7 +761,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     q.N = g.qkv_n;
     q.K = g.H;
     q.X = h->at<void>(h->lo.op_h);
-    q.xmap = &h->xmap_h;
+    q.xmap = h->xmap_h;
     q.omode = O_RED;
     q.dst = qkv_acc;
     q.dst_ld = g.qkv_n;
@@ -820,7 +821,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     o.N = g.H;
     o.K = g.Hq * g.d;
     o.X = h->at<void>(h->lo.op_o);
-    o.xmap = &h->xmap_o;
+    o.xmap = h->xmap_o;
     o.omode = O_RED;
     o.dst = hres;
     o.dst_ld = g.H;
@@ -838,7 +839,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     gu.N = 2 * g.I;
     gu.K = g.H;
     gu.X = h->at<void>(h->lo.op_h);
-    gu.xmap = &h->xmap_h;
+    gu.xmap = h->xmap_h;
     gu.omode = O_RED;
     gu.dst = gu_acc;
     gu.dst_ld = 2 * g.I;
@@ -863,7 +864,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     dn.N = g.H;
     dn.K = g.I;
     dn.X = h->at<void>(h->lo.op_a);
-    dn.xmap = &h->xmap_a;
+    dn.xmap = h->xmap_a;
     dn.omode = O_RED;
     dn.dst = hres;
     dn.dst_ld = g.H;
@@ -1327,10 +1328,14 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     }
     if (h->use_tc) {
       const uint64_t Mt2 = 2ull * lo.Mt;
-      h->xmap_taps = make_map_bf16(h->ws + lo.op_taps, Mt2, (uint64_t)g.n * H, 16);
-      h->xmap_h = make_map_bf16(h->ws + lo.op_h, Mt2, H, 16);
-      h->xmap_o = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, 16);
-      h->xmap_a = make_map_bf16(h->ws + lo.op_a, Mt2, I, 16);
+      const uint32_t tall = Mt2 >= 256 ? 128u : 16u;   // 128-row boxes only where a pass can reach 128 tokens
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t box = b ? tall : 16u;
+        h->xmap_taps[b] = make_map_bf16(h->ws + lo.op_taps, Mt2, (uint64_t)g.n * H, box);
+        h->xmap_h[b] = make_map_bf16(h->ws + lo.op_h, Mt2, H, box);
+        h->xmap_o[b] = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, box);
+        h->xmap_a[b] = make_map_bf16(h->ws + lo.op_a, Mt2, I, box);
+      }
     }
     if (h->attn_tc) {
       h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
@@ -1531,7 +1536,7 @@ int dflash_draft_tokens(dflash_t* h, int32_t n_seq, const float* hidden, const v
     sp.N = vocab;
     sp.K = g.H;
     sp.X = h->at<void>(h->lo.op_h);
-    sp.xmap = &h->xmap_h;
+    sp.xmap = h->xmap_h;
     sp.omode = O_RED;
     sp.dst = logits;
     sp.dst_ld = vocab;
