@@ -68,6 +68,17 @@ enum dflash_status {
 enum dflash_dtype { DFLASH_F32 = 0, DFLASH_BF16 = 1, DFLASH_FP8_E4M3 = 2 };
 enum dflash_rope { DFLASH_ROPE_PLAIN = 0, DFLASH_ROPE_YARN = 1 };
 
+/* e4m3 KV cache (the FP8 block attention named on the dflash_head page;
+ * its storage format is not given there, this library's reading): every
+ * cached K and V head row (one layer, one position, one kv head, d values)
+ * is stored as OCP E4M3 codes with one f32 scale s = max|x| / 448 (an
+ * all-zero row takes s = 1), each code the round-to-nearest-even,
+ * saturating e4m3 value of x / s taken in f32.  The round's block K/V rows
+ * pass through the same format, and so do its queries (one scale per token
+ * and q head): the scores run on e4m3 tensor cores, the P V product in f16
+ * with V decoded exactly from its codes.  The cache holds half the bytes of
+ * a bf16 cache plus 4 bytes per row and kv head. */
+
 /* Drafter shape and capacity (the pages' DflashCfg plus storage sizes). */
 typedef struct dflash_config {
   int32_t n_layers;      /* L                                              */
@@ -84,7 +95,9 @@ typedef struct dflash_config {
   int32_t yarn_original_max_pos;
   double yarn_factor, yarn_beta_fast, yarn_beta_slow;
   int32_t weight_dtype;  /* DFLASH_F32, DFLASH_BF16 or DFLASH_FP8_E4M3     */
-  int32_t kv_dtype;      /* DFLASH_F32 or DFLASH_BF16                      */
+  int32_t kv_dtype;      /* DFLASH_F32 (f32 weights), DFLASH_BF16, or
+                            DFLASH_FP8_E4M3 (bf16/e4m3 weights, head_dim
+                            128): see "e4m3 KV cache" below               */
   int32_t page_size;     /* KV page rows, must be 64                       */
   int32_t max_seqs;      /* sequence slots: ids 0 .. max_seqs-1            */
   int32_t max_pages;     /* pages in the shared pool (all seqs, all calls) */
@@ -237,7 +250,8 @@ int dflash_seq_len(dflash_t *h, int32_t seq_id, int64_t *len);
 
 /* Copy cached rows row0 .. row0+nrows-1 of one layer of a sequence out of
  * the paged pools as f32: k_out, v_out device [nrows, Hkv, d] (K normed and
- * roped, V raw).  Inspection entry point for tests. */
+ * roped, V raw; an e4m3 cache returns code times scale).  Inspection entry
+ * point for tests. */
 int dflash_kv_read(dflash_t *h, int32_t seq_id, int32_t layer, int32_t row0, int32_t nrows,
                    float *k_out, float *v_out, void *stream);
 

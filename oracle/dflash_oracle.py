@@ -61,6 +61,48 @@ def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
     return sign * val
 
 
+E4M3_MAX = 448.0   # largest finite OCP E4M3 value (1.75 * 2^8)
+
+
+def e4m3_round(y: np.ndarray) -> np.ndarray:
+    """Round values to the nearest OCP E4M3 value, ties to even, saturating.
+
+    In the binade ``[2^e, 2^(e+1))`` (e from -6 to 8) E4M3 has 8 values
+    spaced ``2^(e-3)``; below ``2^-6`` the subnormals are spaced ``2^-9``.
+    So the rounding is ``rint(|y| / 2^(e-3)) * 2^(e-3)`` with e the binade of
+    ``|y|`` clamped to [-6, 8] (``numpy.rint`` rounds halves to even, and a
+    value rounding up to the next power of two lands on that value exactly).
+    Magnitudes beyond 448 saturate to 448 (the satfinite convert; the code
+    S.1111.111 is NaN, so 480 does not exist).
+    """
+    y = np.asarray(y, dtype=np.float64)
+    a = np.abs(y)
+    _, ex = np.frexp(a)                      # a = f * 2^ex, f in [0.5, 1): binade ex - 1
+    e = np.clip(ex.astype(np.float64) - 1.0, -6.0, 8.0)
+    q = np.exp2(e - 3.0)
+    v = np.minimum(np.rint(a / q) * q, E4M3_MAX)
+    return np.where(y < 0, -v, v)
+
+
+def fp8_rows(x: np.ndarray) -> np.ndarray:
+    """Per-row e4m3 storage of ``x[..., d]`` (one scale per last-axis row),
+    returned dequantised (code value times scale, exact in f64).
+
+    Reading (FP8 KV cache, spark_model::layers::dflash_head module summary
+    and DflashQuantization): each head row gets the scale ``amax / 448`` (the
+    largest magnitude maps to the largest finite code; an all-zero row takes
+    scale 1), like the per-row scales of the FP8 weights.  The scale and the
+    division that picks each code are taken in float32, the precision the
+    kernels decide them in; the code is the round-to-nearest-even E4M3 value
+    of the quotient.
+    """
+    x32 = np.asarray(x, dtype=np.float64).astype(np.float32)
+    amax = np.max(np.abs(x32), axis=-1, keepdims=True)
+    scale = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    y = (x32 / scale).astype(np.float32)
+    return e4m3_round(y.astype(np.float64)) * scale.astype(np.float64)
+
+
 def decode_weight(w) -> np.ndarray:
     """A stored projection -> float64 ``[out, in]``.
 
@@ -229,7 +271,7 @@ class Drafter:
         return out.reshape(b, cfg.n_heads * cfg.head_dim)
 
     def block_forward(self, noise: np.ndarray, pos_block: Sequence[int],
-                      ctx_k: List[np.ndarray], ctx_v: List[np.ndarray]) -> np.ndarray:
+                      ctx_k: List[np.ndarray], ctx_v: List[np.ndarray], kv_fp8: bool = False) -> np.ndarray:
         """One non-causal forward of the block rows over given ctx K/V.
 
         ``noise [b, H]`` starts the residual stream; per layer: input RMSNorm,
@@ -238,6 +280,12 @@ class Drafter:
         post RMSNorm, SwiGLU MLP plus residual; the final norm gives
         ``[b, H]`` (module summary: qwen3-class; DflashDraft page,
         ``forward_round`` and first-light contract).
+
+        ``kv_fp8``: an FP8 KV cache (the FP8 block attention kernel named in
+        spark_model::layers::dflash_head): the block rows' K and V pass
+        through the cache format like context rows (:func:`fp8_rows`), and so
+        do the queries, whose scores are taken in e4m3; the given ctx K/V are
+        already in that format.
         """
         cfg = self.cfg
         b = noise.shape[0]
@@ -250,6 +298,8 @@ class Drafter:
             v = (x @ L["v"].T).reshape(b, cfg.n_kv_heads, cfg.head_dim)
             q = rope_neox(rms_norm(q, L["q_norm"], cfg.rms_eps), pos_block, self.inv_freq, self.mscale)
             k = rope_neox(rms_norm(k, L["k_norm"], cfg.rms_eps), pos_block, self.inv_freq, self.mscale)
+            if kv_fp8:
+                q, k, v = fp8_rows(q), fp8_rows(k), fp8_rows(v)
             keys = np.concatenate([ctx_k[li], k], axis=0)
             vals = np.concatenate([ctx_v[li], v], axis=0)
             o = self.attention(q, keys, vals)
@@ -259,11 +309,13 @@ class Drafter:
             h = h + a @ L["down"].T
         return rms_norm(h, self.norm, cfg.rms_eps)
 
-    def forward_full(self, taps: np.ndarray, noise: np.ndarray, pos: Sequence[int]) -> np.ndarray:
+    def forward_full(self, taps: np.ndarray, noise: np.ndarray, pos: Sequence[int],
+                     kv_fp8: bool = False) -> np.ndarray:
         """First-light forward: no draft KV cache, ctx K/V recomputed.
 
         ``pos`` holds the ctx rows' positions then the block rows'
         (DflashDraft page, first-light contract under ``ctx_features``).
+        ``kv_fp8``: K/V (and queries) in the FP8 cache format.
         """
         pos = list(pos)
         ctx = taps.shape[0]
@@ -271,9 +323,11 @@ class Drafter:
         ks, vs = [], []
         for li in range(self.cfg.n_layers):
             k, v = self.ctx_kv(li, feats, pos[:ctx])
+            if kv_fp8:
+                k, v = fp8_rows(k), fp8_rows(v)
             ks.append(k)
             vs.append(v)
-        return self.block_forward(noise, pos[ctx:], ks, vs)
+        return self.block_forward(noise, pos[ctx:], ks, vs, kv_fp8)
 
 
 class DraftKV:
@@ -285,13 +339,15 @@ class DraftKV:
     layer per sequence.
     """
 
-    def __init__(self, drafter: Drafter, ctx_cap: int = 0):
+    def __init__(self, drafter: Drafter, ctx_cap: int = 0, kv_fp8: bool = False):
         """``ctx_cap`` > 0: rounds attend to only the most recent ``ctx_cap``
         cached positions (spark_model::layers::dflash_head, dflash_ctx_cap:
         the most recent target positions the drafter may accumulate and
-        attend to); 0 = all."""
+        attend to); 0 = all.  ``kv_fp8``: the cache stores K/V rows in e4m3
+        with per-row scales (:func:`fp8_rows`)."""
         self.d = drafter
         self.ctx_cap = ctx_cap
+        self.kv_fp8 = kv_fp8
         self.k: Dict[int, List[np.ndarray]] = {}
         self.v: Dict[int, List[np.ndarray]] = {}
 
@@ -320,6 +376,8 @@ class DraftKV:
         feats = self.d.ctx_features(taps)
         for li in range(self.d.cfg.n_layers):
             k, v = self.d.ctx_kv(li, feats, pos_new)
+            if self.kv_fp8:
+                k, v = fp8_rows(k), fp8_rows(v)
             self.k[seq][li] = np.concatenate([self.k[seq][li], k], axis=0)
             self.v[seq][li] = np.concatenate([self.v[seq][li], v], axis=0)
 
@@ -339,7 +397,7 @@ class DraftKV:
             if self.ctx_cap > 0:
                 ks = [k[-self.ctx_cap:] for k in ks]
                 vs = [v[-self.ctx_cap:] for v in vs]
-            out.append(self.d.block_forward(noise[i], pos_block[i], ks, vs))
+            out.append(self.d.block_forward(noise[i], pos_block[i], ks, vs, self.kv_fp8))
         return np.stack(out)
 
 

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int kk = 0; kk < steps; ++kk) {
           const int pa = kk >> 2;                        // page (key half / V^T slot) of this K-step
           const uint64_t adv = (uint64_t)((kk & 3) * 32) >> 4;
-          mma_bf16_ts(tmem, p_tmem + (uint32_t)(pa * kPage + (kk & 3) * 8), desc_sw128(v_addr + pa * vbytes) + adv,
+          mma_f16_ts(tmem, p_tmem + (uint32_t)(pa * kPage + (kk & 3) * 8), desc_sw128(v_addr + pa * vbytes) + adv,
                       t.idesc_o, (c > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(&pvdone[c & 1]);
@@ -265,21 +265,28 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const int kbase = k0 + c * kChunk + hg * kPage;
       const int kc = min(kPage, k1 - kbase);   // valid keys of this half (may be <= 0)
       const int klo = ks - kbase;              // keys below the window start (first page only)
+      // raw scores (masked keys -inf; whole pages skip the mask); the
+      // log2-domain scale is applied to the maximum and inside exp2's argument
       float mh = -INFINITY;
       if (ok) {
         tmem_ld32(sbase, sc);
         tmem_ld32(sbase + 32u, sc + 32);
+        if (kc >= kPage && klo <= 0) {
 #pragma unroll
-        for (int i = 0; i < kPage; ++i) {
-          sc[i] = (i < kc && i >= klo) ? sc[i] * t.scale_log2 : -INFINITY;
-          mh = fmaxf(mh, sc[i]);
+          for (int i = 0; i < kPage; ++i) mh = fmaxf(mh, sc[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kPage; ++i) {
+            sc[i] = (i < kc && i >= klo) ? sc[i] : -INFINITY;
+            mh = fmaxf(mh, sc[i]);
+          }
         }
       }
       tmem_st1(xcol + (uint32_t)(2 * (c & 1) + hg), mh);
       tc_fence_before();
       sm_sync();
       tc_fence_after();
-      const float mj = fmaxf(mh, tmem_ld1(xcol + (uint32_t)(2 * (c & 1) + (hg ^ 1))));
+      const float mj = t.scale_log2 * fmaxf(mh, tmem_ld1(xcol + (uint32_t)(2 * (c & 1) + (hg ^ 1))));
       if (!ok || flags[0]) {
         ok = false;
         mbar_arrive(&pfull[c & 1]);
@@ -311,11 +318,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       float lsum = 0.f;
       // P over this half's own scores (both halves loaded theirs before the
       // max exchange): 32 columns of bf16 pairs
+      const float nm = -m_run;
       float pw[kPage / 2];
 #pragma unroll
       for (int i = 0; i < kPage / 2; ++i) {
-        const float p0 = ex2_fast(sc[2 * i] - m_run);
-        const float p1 = ex2_fast(sc[2 * i + 1] - m_run);
+        const float p0 = ex2_fast(fmaf(sc[2 * i], t.scale_log2, nm));
+        const float p1 = ex2_fast(fmaf(sc[2 * i + 1], t.scale_log2, nm));
         lsum += p0 + p1;
         const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
         pw[i] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&b));

@@ -38,7 +38,9 @@ constexpr int kEpiBar = 1;        // named barrier id used by the epilogue
 constexpr int kRedFloats = kEpiTokChunk * (kTileN + 1) + kEpiTokChunk;   // epilogue shared scratch
 
 enum WType { W_F32 = 0, W_BF16 = 1, W_FP8 = 2 };
-enum KvType { KV_F32 = 0, KV_BF16 = 1 };
+// KV cache element: f32, bf16, or OCP e4m3 codes with one f32 scale per
+// (layer, page row, kv head) for K and for V.
+enum KvType { KV_F32 = 0, KV_BF16 = 1, KV_FP8 = 2 };
 enum EpiKind { EPI_FC = 0, EPI_KV = 1, EPI_QKV = 2, EPI_RESID = 3, EPI_SWIGLU = 4 };
 enum DevErr { DERR_NONE = 0, DERR_TIMEOUT = 4, DERR_BAD_PAGE = 6 };
 
@@ -146,6 +148,12 @@ struct Part {
 };
 
 // ------------------------------------------------------------------ helpers
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -178,6 +186,35 @@ __device__ __forceinline__ void put_kv(void* base, long idx, float v, int kvtype
 __device__ __forceinline__ long pool_layer_elems(const Geo& g) {
   return (long)g.max_pages * g.Hkv * kPage * g.d;
 }
+
+// FP8 cache: each pool holds its e4m3 codes ([L][page][Hkv][64][d] for K,
+// [L][page][Hkv][d][64] for V^T, one byte each) followed by its scales
+// [L][page][Hkv][64] f32; the query buffer holds codes [Mt][Hq][d] followed
+// by scales [Mt][Hq].
+__host__ __device__ __forceinline__ long fp8_pool_codes(const Geo& g) {
+  return (long)g.L * g.max_pages * g.Hkv * kPage * g.d;
+}
+__host__ __device__ __forceinline__ long kv_scale_index(const Geo& g, int layer, int page, int head, int off) {
+  return (((long)layer * g.max_pages + page) * g.Hkv + head) * kPage + off;
+}
+__host__ __device__ __forceinline__ float* fp8_pool_scales(const Geo& g, void* pool) {
+  return reinterpret_cast<float*>(static_cast<char*>(pool) + fp8_pool_codes(g));
+}
+__host__ __device__ __forceinline__ const float* fp8_pool_scales(const Geo& g, const void* pool) {
+  return reinterpret_cast<const float*>(static_cast<const char*>(pool) + fp8_pool_codes(g));
+}
+__host__ __device__ __forceinline__ long fp8_q_codes(const Geo& g) { return (long)g.Mt * g.Hq * g.d; }
+
+// e4m3 scale of one head row from its absolute maximum: the largest value
+// maps to the largest finite code (448); an all-zero row takes scale 1.
+__device__ __forceinline__ float fp8_row_scale(float amax) { return amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f; }
+
+// Two values divided by the row scale (IEEE division) and rounded to
+// nearest-even e4m3 with saturation; a in the low byte.
+__device__ __forceinline__ uint16_t fp8_pair(float a, float b, float s) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)), __NV_SATFINITE, __NV_E4M3);
+}
+
 // K pool: [L][page][Hkv][64][d]
 __device__ __forceinline__ long k_index(const Geo& g, int layer, int page, int head, int off, int dim) {
   return layer * pool_layer_elems(g) + (((long)page * g.Hkv + head) * kPage + off) * g.d + dim;
@@ -185,6 +222,45 @@ __device__ __forceinline__ long k_index(const Geo& g, int layer, int page, int h
 // V^T pool: [L][page][Hkv][d][64]
 __device__ __forceinline__ long v_index(const Geo& g, int layer, int page, int head, int off, int dim) {
   return layer * pool_layer_elems(g) + (((long)page * g.Hkv + head) * g.d + dim) * kPage + off;
+}
+
+// Store one head row (PER dims per lane of a warp, lane l holds dims
+// l*PER ..) of q (kind 0), K (1) or V (2) in e4m3 with its scale.
+template <int PER>
+__device__ __forceinline__ void put_row_fp8(const Geo& g, const float* x, int lane, int kind, int layer, int tok,
+                                            int head, int dst, void* q, void* kpool, void* vpool) {
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) am = fmaxf(am, fabsf(x[i]));
+  const float sc = fp8_row_scale(warp_max(am));
+  uint8_t c[PER];
+#pragma unroll
+  for (int i = 0; i < PER; i += 2) {
+    const uint16_t w = fp8_pair(x[i], x[i + 1], sc);
+    c[i] = (uint8_t)(w & 0xFF);
+    c[i + 1] = (uint8_t)(w >> 8);
+  }
+  constexpr int d = 32 * PER;
+  const int dim0 = lane * PER;
+  if (kind == 0) {
+    uint8_t* row = static_cast<uint8_t*>(q) + ((long)tok * g.Hq + head) * d + dim0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) row[i] = c[i];
+    if (lane == 0) reinterpret_cast<float*>(static_cast<char*>(q) + fp8_q_codes(g))[(long)tok * g.Hq + head] = sc;
+    return;
+  }
+  const int page = dst >> 6, off = dst & (kPage - 1);
+  if (kind == 1) {
+    uint8_t* row = static_cast<uint8_t*>(kpool) + k_index(g, layer, page, head, off, dim0);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) row[i] = c[i];
+    if (lane == 0) fp8_pool_scales(g, kpool)[kv_scale_index(g, layer, page, head, off)] = sc;
+  } else {
+    uint8_t* vp = static_cast<uint8_t*>(vpool);
+#pragma unroll
+    for (int i = 0; i < PER; ++i) vp[v_index(g, layer, page, head, off, dim0 + i)] = c[i];
+    if (lane == 0) fp8_pool_scales(g, vpool)[kv_scale_index(g, layer, page, head, off)] = sc;
+  }
 }
 
 // NeoX rotation angle for pair j at position p, reduced to [-pi, pi] in f64
@@ -294,7 +370,9 @@ static __device__ void epi_heads_t(const EpiArgs& e, int tile, const float* red,
         x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
       }
     }
-    if (kind == 0) {
+    if (g.kvtype == KV_FP8) {
+      put_row_fp8<PER>(g, x, lane, kind, layer, tok, head, dst, e.q_out, e.kpool, e.vpool);
+    } else if (kind == 0) {
       const long base = ((long)tok * g.Hq + head) * d + dim0;
 #pragma unroll
       for (int q = 0; q < PER; ++q) put_kv(e.q_out, base + q, x[q], g.kvtype);

@@ -141,7 +141,9 @@ __device__ void qk_finish_row(const FinishArgs& f, int tok, int hh) {
       x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
     }
   }
-  if (kind == 0) {
+  if (g.kvtype == KV_FP8) {
+    put_row_fp8<PER>(g, x, lane, kind, f.layer, tok, head, dst, f.q_out, f.kpool, f.vpool);
+  } else if (kind == 0) {
     const long base = ((long)tok * g.Hq + head) * d + dim0;
 #pragma unroll
     for (int q = 0; q < PER; ++q) put_kv(f.q_out, base + q, x[q], g.kvtype);

@@ -168,10 +168,14 @@ cudaError_t launch_round_mk(const MkArgs& a, int grid, const void* tmxh, const v
 // Fixed device region of dflash_forward_full_static (static_full.cu).
 constexpr size_t kFixedKvBytes = size_t(16) << 20;
 constexpr int kFixedMaxDevices = 64;
-cudaError_t fixed_kv_region(void** base);
+cudaError_t fixed_kv_region(void** base, uint64_t user, bool* fresh);
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s);
 void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
                          cudaStream_t s);
+// Same over an e4m3 cache (head dim 128): tmq / tmk / tmv are the byte maps of
+// the e4m3 queries, K pages and V^T pages.
+void launch_attention_tc8(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
+                          cudaStream_t s);
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s);
 void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);

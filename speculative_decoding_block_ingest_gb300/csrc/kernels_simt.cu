@@ -355,6 +355,17 @@ __global__ void kv_read_kernel(Geo g, const void* kpool, const void* vpool, cons
   const int off = row % kPage;
   for (int idx = threadIdx.x; idx < g.Hkv * g.d; idx += blockDim.x) {
     const int head = idx / g.d, dim = idx % g.d;
+    if (g.kvtype == KV_FP8) {
+      // code (exact in f16) times the row's scale
+      const long si = kv_scale_index(g, layer, page, head, off);
+      const uint8_t kc = static_cast<const uint8_t*>(kpool)[k_index(g, layer, page, head, off, dim)];
+      const uint8_t vc = static_cast<const uint8_t*>(vpool)[v_index(g, layer, page, head, off, dim)];
+      k_out[(long)rr * g.Hkv * g.d + idx] =
+          __half2float(__half(__nv_cvt_fp8_to_halfraw(kc, __NV_E4M3))) * fp8_pool_scales(g, kpool)[si];
+      v_out[(long)rr * g.Hkv * g.d + idx] =
+          __half2float(__half(__nv_cvt_fp8_to_halfraw(vc, __NV_E4M3))) * fp8_pool_scales(g, vpool)[si];
+      continue;
+    }
     k_out[(long)rr * g.Hkv * g.d + idx] = load_kv(kpool, k_index(g, layer, page, head, off, dim), g.kvtype);
     v_out[(long)rr * g.Hkv * g.d + idx] = load_kv(vpool, v_index(g, layer, page, head, off, dim), g.kvtype);
   }

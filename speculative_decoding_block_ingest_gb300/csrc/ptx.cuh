@@ -143,15 +143,33 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       : "memory");
 }
 
-// Same, with A read from tensor memory: M rows in TMEM lanes, K along the
-// columns, two bf16 per 32-bit column (the lower K index in the low half).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+// kind::f16 (bf16 or f16 operands, as the instruction descriptor says) with
+// A read from tensor memory: M rows in TMEM lanes, K along the columns, two
+// 16-bit values per 32-bit column (the lower K index in the low half).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
                                             uint32_t accumulate) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+
+// kind::f8f6f4 with both operands from shared memory (e4m3 A and B in the
+// descriptors' layout; 32 K values = 32 bytes per instruction).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor: f32 accumulate, both operands K-major, shape M x N,
+// A/B format code 0 (f16 under kind::f16, e4m3 under kind::f8f6f4).
+__host__ __device__ __forceinline__ uint32_t idesc_fmt0(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Arrive once on `bar` when every tcgen05 op this thread issued has completed.

@@ -9,6 +9,7 @@
 // parameter, so no host-to-device copy and no host synchronisation happen on
 // the round's path.
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cmath>
 #include <cstdarg>
@@ -53,7 +54,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Bytes per stored weight element: f32 stays f32; bf16 and e4m3 weights are
 // stored as bf16 blocks for the tensor cores (e4m3 expands exactly).
 int esize_w(int wtype) { return wtype == DFLASH_F32 ? 4 : 2; }
-int esize_kv(int kvtype) { return kvtype == DFLASH_F32 ? 4 : 2; }
+int esize_kv(int kvtype) { return kvtype == DFLASH_F32 ? 4 : (kvtype == DFLASH_FP8_E4M3 ? 1 : 2); }
 
 // Workspace carve-up, computed identically by dflash_workspace_bytes and dflash_create.
 struct Layout {
@@ -116,8 +117,10 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.post_ln = take(L * H * 4);
   Lo.qn = take(L * d * 4);
   Lo.kn = take(L * d * 4);
-  Lo.kpool = take(L * (size_t)c.max_pages * Hkv * kPage * d * ek);
-  Lo.vpool = take(L * (size_t)c.max_pages * Hkv * kPage * d * ek);
+  // e4m3 pools carry their per-row scales after the codes
+  const size_t kv_scales = c.kv_dtype == DFLASH_FP8_E4M3 ? L * (size_t)c.max_pages * Hkv * kPage * 4 : 0;
+  Lo.kpool = take(L * (size_t)c.max_pages * Hkv * kPage * d * ek + kv_scales);
+  Lo.vpool = take(L * (size_t)c.max_pages * Hkv * kPage * d * ek + kv_scales);
   Lo.btab = take((size_t)(c.max_seqs + 1) * Lo.pps * 4);
   Lo.inv_freq = take(d / 2 * 8);
   Lo.h = take(Mt * H * 4);
@@ -175,11 +178,14 @@ int validate_config(const dflash_config* c) {
       c->intermediate % 64 || ((long)c->n_heads * c->head_dim) % kTileK)
     return fail(DFLASH_ERR_UNSUPPORTED, "projection sizes must be multiples of 128 rows / 64 columns");
   if (c->weight_dtype < DFLASH_F32 || c->weight_dtype > DFLASH_FP8_E4M3) return fail(DFLASH_ERR_INVALID_ARG, "weight_dtype");
-  if (c->kv_dtype != DFLASH_F32 && c->kv_dtype != DFLASH_BF16) return fail(DFLASH_ERR_INVALID_ARG, "kv_dtype");
+  if (c->kv_dtype != DFLASH_F32 && c->kv_dtype != DFLASH_BF16 && c->kv_dtype != DFLASH_FP8_E4M3)
+    return fail(DFLASH_ERR_INVALID_ARG, "kv_dtype");
   if (c->weight_dtype == DFLASH_F32 && c->kv_dtype != DFLASH_F32)
     return fail(DFLASH_ERR_UNSUPPORTED, "f32 weights need an f32 KV cache");
-  if (c->weight_dtype != DFLASH_F32 && c->kv_dtype != DFLASH_BF16)
-    return fail(DFLASH_ERR_UNSUPPORTED, "bf16/fp8 weights need a bf16 KV cache");
+  if (c->weight_dtype != DFLASH_F32 && c->kv_dtype == DFLASH_F32)
+    return fail(DFLASH_ERR_UNSUPPORTED, "bf16/fp8 weights need a bf16 or e4m3 KV cache");
+  if (c->kv_dtype == DFLASH_FP8_E4M3 && c->head_dim != 128)
+    return fail(DFLASH_ERR_UNSUPPORTED, "an e4m3 KV cache needs head_dim 128");
   if (c->rope_type != DFLASH_ROPE_PLAIN && c->rope_type != DFLASH_ROPE_YARN) return fail(DFLASH_ERR_INVALID_ARG, "rope_type");
   if (!(c->rope_theta > 1.0)) return fail(DFLASH_ERR_INVALID_ARG, "rope_theta must be > 1");
   if (c->rope_type == DFLASH_ROPE_YARN &&
@@ -261,6 +267,36 @@ CUtensorMap make_map_bf16_3d(const void* base, uint64_t d0, uint64_t d1, uint64_
   return m;
 }
 
+// 2-D byte map over [rows][cols] (e4m3 codes), box [box_rows][box_cols].
+CUtensorMap make_map_u8(const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+                        CUtensorMapSwizzle swz) {
+  CUtensorMap m;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = tensor_map_encoder()(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) throw CudaError{"cuTensorMapEncodeTiled (u8) failed (" + std::to_string((int)r) + ")"};
+  return m;
+}
+
+// 3-D byte map over [d2][d1][d0], box {d0, b1, b2} in the 128-byte swizzle
+// (d0 = 128: one swizzle row per (d2, d1) index).
+CUtensorMap make_map_u8_3d(const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, uint32_t b2) {
+  CUtensorMap m;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {d0, d0 * d1};
+  cuuint32_t box[3] = {(cuuint32_t)d0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = tensor_map_encoder()(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) throw CudaError{"cuTensorMapEncodeTiled (u8 3-D) failed (" + std::to_string((int)r) + ")"};
+  return m;
+}
+
 }  // namespace
 
 struct dflash_handle {
@@ -317,6 +353,8 @@ struct dflash_handle {
   std::vector<RoundGraph> graphs;
   uint64_t graph_clock = 0;
   bool graphs_off = false;
+  bool attn_fp8 = false;        // e4m3 KV cache: attention on kind::f8f6f4 scores
+  uint64_t uid = 0;             // process-unique handle id (static region ownership)
   cudaStream_t cap_stream = nullptr;   // private stream the rounds are captured on
   struct Rec {
     int kind;
@@ -470,7 +508,7 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     else if (sp.e.kind == EPI_RESID) out_b = nt * sp.N * 12;
     else if (sp.e.kind == EPI_SWIGLU) out_b = nt * sp.N / 2 * 4;
     else if (sp.e.kind == EPI_FC) out_b = nt * sp.N * 4;
-    else out_b = nt * sp.N * (g.kvtype == KV_F32 ? 4 : 2);
+    else out_b = nt * sp.N * (g.kvtype == KV_F32 ? 4 : (g.kvtype == KV_FP8 ? 1.0 + 4.0 / g.d : 2));
     const double bytes = (double)sp.N * sp.K * esize_w(g.wtype) + (sp.wscale ? sp.N * 4.0 : 0.0) + x_b + out_b;
     Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
     a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_GEMM, a.p.grid) : nullptr;
@@ -559,7 +597,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
 // The persistent round takes bf16 rounds of up to kMkMaxTok block rows whose
 // projection stage fits at least two ring stages beside the attention buffers.
 bool mk_eligible(dflash_t* h, int n_tok) {
-  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && !h->mk_off && !h->evicted_any && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
+  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && h->cfg.kv_dtype == DFLASH_BF16 && !h->mk_off && !h->evicted_any && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
          round_mk_stages((n_tok + 15) / 16 * 16, h->g.d) >= 2;
 }
 
@@ -797,14 +835,16 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     a.scale_log2 = 1.4426950408889634f / std::sqrt((float)g.d);
     a.err = h->at<int>(h->lo.err);
     a.g = g;
-    const double ekv = g.kvtype == KV_F32 ? 4 : 2;
+    // bytes per cached element (e4m3: the code plus its row's scale share)
+    const double ekv = g.kvtype == KV_F32 ? 4 : (g.kvtype == KV_FP8 ? 1.0 + 4.0 / g.d : 2);
     const double part_b = (double)rd.n_items * g.G * kBlock * (g.d + 2) * 4;
     {
       double kv_b = 0;
       for (int i = 0; i < rd.n_seq; ++i) kv_b += (double)(rd.len[i] + kBlock) * g.Hkv * g.d * 2 * ekv;
       Launch L(h, DFLASH_KERNEL_ATTENTION, kv_b + (double)n_tok * g.Hq * g.d * ekv + part_b, s);
       a.trace = h->attn_tc ? trace_slot(h, DFLASH_KERNEL_ATTENTION, rd.n_items) : nullptr;
-      if (h->attn_tc) launch_attention_tc(a, rd.n_items, &h->qmap, &h->kv->kmap, &h->kv->vmap, s);
+      if (h->attn_fp8) launch_attention_tc8(a, rd.n_items, &h->qmap, &h->kv->kmap, &h->kv->vmap, s);
+      else if (h->attn_tc) launch_attention_tc(a, rd.n_items, &h->qmap, &h->kv->kmap, &h->kv->vmap, s);
       else launch_attention_simt(a, rd.n_items, s);
     }
     ck(cudaGetLastError(), "attention launch");
@@ -1146,6 +1186,14 @@ void release_slot(dflash_t* h, int slot) {
 
 // Makes `r` the region the enqueued kernels use (pools, maps, free list and
 // the device geometry's pages-per-layer) until the scope ends.
+// e4m3 pools: K pages [64 keys][d bytes] in the 128-byte swizzle (the score
+// MMA's B operand as stored), V^T pages [d][64 bytes] unswizzled (threads
+// convert them to f16); the maps cover the codes, not the scales after them.
+void kv_maps_fp8(dflash_handle::KvRegion& r, const void* kpool, const void* vpool, uint64_t rows, int d) {
+  r.kmap = make_map_u8(kpool, rows * kPage, (uint64_t)d, kPage, (uint32_t)d, CU_TENSOR_MAP_SWIZZLE_128B);
+  r.vmap = make_map_u8(vpool, rows * d, kPage, (uint32_t)d, kPage, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 struct RegionScope {
   dflash_t* h;
   dflash_handle::KvRegion* prev;
@@ -1225,6 +1273,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   dflash_t* h = new (std::nothrow) dflash_handle();
   if (!h) return fail(DFLASH_ERR_CAPACITY, "host allocation failed");
   h->cfg = *cfg;
+  {
+    static std::atomic<uint64_t> next_uid{1};
+    h->uid = next_uid.fetch_add(1);
+  }
   h->lo = lo;
   h->ws = static_cast<char*>(workspace);
   h->n_sm = n_sm;
@@ -1315,7 +1367,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     }
     ck(cudaMemcpyAsync(h->ws + lo.inv_freq, inv.data(), inv.size() * 8, cudaMemcpyHostToDevice, s), "rope table");
     h->use_tc = cfg->weight_dtype != DFLASH_F32;
-    h->attn_tc = cfg->kv_dtype == DFLASH_BF16;
+    h->attn_tc = cfg->kv_dtype != DFLASH_F32;
+    h->attn_fp8 = cfg->kv_dtype == DFLASH_FP8_E4M3;
     {
       // "persistent": the whole round in one kernel (round_mk.cu); by default
       // one kernel per step, which measured faster at the 8-layer shape
@@ -1338,11 +1391,15 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       }
     }
     if (h->attn_tc) {
-      h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
-
       const uint64_t pool_rows = (uint64_t)L * cfg->max_pages * Hkv;
-      h->pool.kmap = make_map_bf16(h->ws + lo.kpool, pool_rows * kPage, d, kPage);
-      h->pool.vmap = make_map_bf16(h->ws + lo.vpool, pool_rows * d, kPage, d);
+      if (h->attn_fp8) {
+        h->qmap = make_map_u8_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
+        kv_maps_fp8(h->pool, h->ws + lo.kpool, h->ws + lo.vpool, pool_rows, d);
+      } else {
+        h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
+        h->pool.kmap = make_map_bf16(h->ws + lo.kpool, pool_rows * kPage, d, kPage);
+        h->pool.vmap = make_map_bf16(h->ws + lo.vpool, pool_rows * d, kPage, d);
+      }
     }
     // stale pool rows are read (and masked) by the attention MMA: keep them finite
     ck(cudaMemsetAsync(h->ws + lo.kpool, 0, lo.vpool - lo.kpool, s), "K pool clear");
@@ -1415,17 +1472,21 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
   if (!aligned16(noise_emb) || !aligned16(out) || (ctx > 0 && !aligned16(taps)))
     return fail(DFLASH_ERR_INVALID_ARG, "taps / noise_emb / out must start on a 16-byte boundary");
   if (ctx + kBlock > h->cfg.max_seq_len) return fail(DFLASH_ERR_CAPACITY, "ctx exceeds max_seq_len");
-  // one page of K (or V^T) for every layer
-  const size_t page_bytes = (size_t)h->g.L * h->g.Hkv * kPage * h->g.d * esize_kv(h->cfg.kv_dtype);
+  // one page of K (or V^T) for every layer, with its row scales for e4m3
+  const size_t page_bytes = (size_t)h->g.L * h->g.Hkv * kPage *
+                            ((size_t)h->g.d * esize_kv(h->cfg.kv_dtype) + (h->attn_fp8 ? 4 : 0));
   const int fixed_pages = (int)(kFixedKvBytes / (2 * page_bytes));
   const int need = (ctx + kBlock + kPage - 1) / kPage;
   if (need > fixed_pages)
     return fail(DFLASH_ERR_CAPACITY, "ctx %d exceeds the static KV region (at most %d context rows for this drafter)",
                 ctx, std::max(0, fixed_pages * kPage - kBlock));
-  if (!h->fixed.kpool) {
-    void* base = nullptr;
-    const cudaError_t e = fixed_kv_region(&base);
+  void* base = nullptr;
+  bool fresh = false;
+  {
+    const cudaError_t e = fixed_kv_region(&base, h->uid, &fresh);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "static KV region lookup: %s", cudaGetErrorString(e));
+  }
+  if (!h->fixed.kpool) {
     const int rc = guarded([&]() -> int {
       dflash_handle::KvRegion r;
       r.kpool = static_cast<char*>(base);
@@ -1433,8 +1494,12 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
       r.max_pages = fixed_pages;
       if (h->attn_tc) {
         const uint64_t rows = (uint64_t)h->g.L * fixed_pages * h->g.Hkv;
-        r.kmap = make_map_bf16(r.kpool, rows * kPage, h->g.d, kPage);
-        r.vmap = make_map_bf16(r.vpool, rows * h->g.d, kPage, h->g.d);
+        if (h->attn_fp8) {
+          kv_maps_fp8(r, r.kpool, r.vpool, rows, h->g.d);
+        } else {
+          r.kmap = make_map_bf16(r.kpool, rows * kPage, h->g.d, kPage);
+          r.vmap = make_map_bf16(r.vpool, rows * h->g.d, kPage, h->g.d);
+        }
       }
       h->fixed = std::move(r);
       return DFLASH_OK;
@@ -1442,6 +1507,11 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
     if (rc != DFLASH_OK) return rc;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (fresh) {
+    // another handle wrote the region last: clear this drafter's K and V areas
+    const cudaError_t e = cudaMemsetAsync(h->fixed.kpool, 0, 2 * (size_t)fixed_pages * page_bytes, s);
+    if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "static KV region clear: %s", cudaGetErrorString(e));
+  }
   release_slot(h, h->cfg.max_seqs);   // pool pages, if any were left
   h->fixed.free_pages.resize(h->fixed.max_pages);
   for (int i = 0; i < h->fixed.max_pages; ++i) h->fixed.free_pages[i] = h->fixed.max_pages - 1 - i;

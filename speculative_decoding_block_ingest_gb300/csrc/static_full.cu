@@ -13,21 +13,25 @@
 
 namespace dfl {
 
-// Zero when the library's device code is loaded.  Calls write only finite
-// values into it; rows past a call's last key in its last page are read by
-// the attention (and masked), so they must stay finite -- zero or an earlier
-// call's finite K/V.
+// Zero when the library's device code is loaded.  Rows past a call's last
+// key in its last page are read by the attention (and masked), so they must
+// stay finite: zero or an earlier call's K/V in the same format.  Another
+// handle's rows (another drafter, maybe another element format: bf16 or f32
+// bytes read as e4m3 can be NaN codes) are not, so a handle's first call
+// after another handle's clears the region.
 static __device__ __align__(256) unsigned char g_fixed_kv[kFixedKvBytes];
 
 // Device address of the region on the current device.  The first call on a
-// device (with that device current) looks it up once.
-cudaError_t fixed_kv_region(void** base) {
+// device (with that device current) looks it up once.  *fresh: the region
+// was last used by a handle other than `user` (the caller clears it).
+cudaError_t fixed_kv_region(void** base, uint64_t user, bool* fresh) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kFixedMaxDevices) return cudaErrorInvalidDevice;
   static std::mutex mu;
   static void* addr[kFixedMaxDevices] = {};
+  static uint64_t last_user[kFixedMaxDevices] = {};
   std::lock_guard<std::mutex> lock(mu);
   if (!addr[dev]) {
     void* p = nullptr;
@@ -36,6 +40,8 @@ cudaError_t fixed_kv_region(void** base) {
     addr[dev] = p;
   }
   *base = addr[dev];
+  *fresh = last_user[dev] != user;
+  last_user[dev] = user;
   return cudaSuccess;
 }
 

@@ -65,7 +65,7 @@ class DraftConfig:
     yarn_beta_fast: float = 32.0
     yarn_beta_slow: float = 1.0
     weight_dtype: str = "bf16"        # "f32" | "bf16" | "fp8"
-    kv_dtype: str = "bf16"            # "f32" | "bf16"
+    kv_dtype: str = "bf16"            # "f32" | "bf16" | "fp8" (e4m3 codes + per-row scales)
     page_size: int = 64
 
     def shape(self, name: str):
@@ -116,6 +116,7 @@ QWEN3_5L_YARN = DraftConfig(n_layers=5, hidden=4096, n_heads=32, n_kv_heads=8, h
 QWEN3_8L = DraftConfig(n_layers=8, hidden=2048, n_heads=32, n_kv_heads=4, head_dim=128,
                        intermediate=6144, n_taps=5)
 QWEN3_8L_FP8 = dataclasses.replace(QWEN3_8L, weight_dtype="fp8")
+QWEN3_8L_FP8_KV8 = dataclasses.replace(QWEN3_8L_FP8, kv_dtype="fp8")
 
 WORKLOADS: Dict[str, Workload] = {
     "tiny_f32": Workload("tiny_f32", TINY_F32, batch=1, ctx=64),
@@ -127,6 +128,9 @@ WORKLOADS: Dict[str, Workload] = {
                                    ctx_lo=1024, ctx_hi=16384),
     "qwen3_8l_fp8_b8_ctx65536": Workload("qwen3_8l_fp8_b8_ctx65536", QWEN3_8L_FP8, batch=8,
                                          ctx=65536, ingest_lo=16, ingest_hi=16, rounds=32),
+    # the same rounds over an e4m3 KV cache (half the cache bytes)
+    "qwen3_8l_fp8_kv8_b8_ctx65536": Workload("qwen3_8l_fp8_kv8_b8_ctx65536", QWEN3_8L_FP8_KV8, batch=8,
+                                             ctx=65536, ingest_lo=16, ingest_hi=16, rounds=32),
 }
 
 

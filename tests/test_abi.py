@@ -99,3 +99,17 @@ def test_draft_token_calls_reject_null_handle(lib):
     assert lib.dflash_lm_head_bytes(None, 128, ctypes.byref(n)) == -1
     assert lib.dflash_pack_lm_head(None, None, 128, None, 0, None) == -1
     assert lib.dflash_draft_tokens(None, 1, None, None, 128, None, None) == -1
+
+
+def test_fp8_kv_cache_config(lib):
+    """An e4m3 cache needs tensor-core weights and head_dim 128; its pools
+    hold one byte per element plus a 4-byte scale per (row, kv head)."""
+    rc, n8 = _ws(_cfg(kv_dtype=dflash.FP8))
+    assert rc == 0
+    _, n16 = _ws(_cfg())
+    cfg = synth.QWEN3_8L
+    per_pool_16 = cfg.n_layers * 64 * 4 * 64 * 128 * 2
+    per_pool_8 = cfg.n_layers * 64 * 4 * 64 * (128 + 4)
+    assert abs((n16 - n8) - 2 * (per_pool_16 - per_pool_8)) <= 4096
+    assert _ws(_cfg(kv_dtype=dflash.FP8, head_dim=64))[0] == dflash.ERR_UNSUPPORTED
+    assert _ws(_cfg(kv_dtype=dflash.FP8, weight_dtype=dflash.F32))[0] == dflash.ERR_UNSUPPORTED

@@ -53,7 +53,7 @@ def _run(wl, n_rounds):
                         max_ingest_rows=GPU_CHUNK, device=DEV)
     D = O.Drafter(cfg, oracle_weights(W))
     del W
-    kv = O.DraftKV(D)
+    kv = O.DraftKV(D, kv_fp8=cfg.kv_dtype == "fp8")
     # cache build: every sequence on the GPU, the sampled ones in the oracle
     for s in range(B):
         for r0 in range(0, lens[s], GPU_CHUNK):
@@ -125,3 +125,9 @@ def test_fullsize_fp8_batch8_ctx65536():
     """FP8 e4m3 weights with row scales, 8 sequences at ctx 65536,
     ingest 16 rows per sequence then forward_round."""
     _run(synth.WORKLOADS["qwen3_8l_fp8_b8_ctx65536"], n_rounds=1)
+
+
+def test_fullsize_fp8kv_batch8_ctx65536():
+    """The FP8-weight batch-8 ctx-65536 workload over an e4m3 KV cache,
+    against the oracle in the same cache format."""
+    _run(synth.WORKLOADS["qwen3_8l_fp8_kv8_b8_ctx65536"], n_rounds=1)

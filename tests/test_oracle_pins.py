@@ -556,3 +556,93 @@ def test_context_window_equals_first_light_on_the_last_rows():
     a = full.forward_round([0], noise[None], np.arange(ctx, ctx + 16)[None])
     b = wide.forward_round([0], noise[None], np.arange(ctx, ctx + 16)[None])
     assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- FP8 KV cache
+def test_e4m3_round_matches_torch_cast_on_a_dense_sweep():
+    """Round-to-nearest-even onto the E4M3 grid equals torch's float32 ->
+    float8_e4m3fn cast (a library routine) inside the finite range, every
+    exact midpoint between neighbouring codes included."""
+    codes = np.arange(256)
+    vals = np.unique(O.e4m3_to_f64(codes)[np.isfinite(O.e4m3_to_f64(codes))])
+    mids = (vals[1:] + vals[:-1]) / 2
+    sweep = np.linspace(-460.0, 460.0, 400001)
+    x = np.concatenate([vals, mids, sweep, sweep * 1e-3]).astype(np.float32).astype(np.float64)
+    want = torch.tensor(x, dtype=torch.float64).to(torch.float32).to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(O.e4m3_round(x), want)
+
+
+def test_e4m3_round_fixes_codes_ties_to_even_and_saturates():
+    v = O.e4m3_to_f64(np.arange(256))
+    fin = v[np.isfinite(v)]
+    assert np.array_equal(O.e4m3_round(fin), fin)
+    # 1 + 1/16 lies halfway between 1 (mantissa 000) and 1.125 (001): even wins
+    assert O.e4m3_round(np.array([1.0625, 1.1875, -1.0625]))[:].tolist() == [1.0, 1.25, -1.0]
+    # subnormal spacing 2^-9; half of it rounds to zero (even)
+    assert O.e4m3_round(np.array([2.0 ** -10, 3 * 2.0 ** -10])).tolist() == [0.0, 2.0 ** -8]
+    assert O.e4m3_round(np.array([448.0, 470.0, 1e9, -1e9])).tolist() == [448.0, 448.0, 448.0, -448.0]
+
+
+def test_fp8_rows_scale_per_row_and_error_bound():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((5, 3, 128)) * np.exp2(rng.integers(-6, 6, size=(5, 3, 1)))
+    x[1, 2] = 0.0
+    q = O.fp8_rows(x)
+    amax = np.max(np.abs(x), axis=-1, keepdims=True)
+    # the largest magnitude of a row is kept (to float32 rounding of its scale)
+    i = np.argmax(np.abs(x), axis=-1)[..., None]
+    assert np.allclose(np.take_along_axis(q, i, -1), np.take_along_axis(x, i, -1), rtol=2e-7, atol=0)
+    # half a code spacing: 2^-4 relative in the normal range, 2^-10 scale below
+    scale = np.where(amax > 0, amax / 448.0, 1.0)
+    err = np.abs(q - x)
+    assert np.all(err <= np.maximum(np.abs(x) * 2.0 ** -4, scale * 2.0 ** -10) * (1 + 1e-6))
+    assert np.all(q[1, 2] == 0.0)
+    # one scale per row: scaling a row by a power of two scales only it, exactly
+    y = x.copy()
+    y[2, 1] *= 8.0
+    qy = O.fp8_rows(y)
+    assert np.array_equal(qy[2, 1], q[2, 1] * 8.0)
+    mask = np.ones(x.shape[:2], bool)
+    mask[2, 1] = False
+    assert np.array_equal(qy[mask], q[mask])
+
+
+MICRO_KV8 = dataclasses.replace(MICRO_BF16, kv_dtype="fp8")
+
+
+def test_fp8_cache_round_equals_first_light_in_the_cache_format():
+    """With the FP8 cache the cached round still equals the first-light
+    forward that recomputes the context in the same format (the cache only
+    avoids recomputation), and chunked ingest equals one-shot ingest."""
+    cfg = MICRO_KV8
+    D = O.Drafter(cfg, oracle_weights(synth.make_weights(cfg)))
+    taps, noise, pos = _inputs(cfg, 37)
+    full = D.forward_full(taps, noise, pos, kv_fp8=True)
+    kv = O.DraftKV(D, kv_fp8=True)
+    kv.ingest(0, taps[:20], pos[:20])
+    kv.ingest(0, taps[20:], pos[20:37])
+    rnd = kv.forward_round([0], noise[None], np.array([pos[37:]]))[0]
+    assert np.allclose(rnd, full, rtol=0, atol=1e-12)
+    one = O.DraftKV(D, kv_fp8=True)
+    one.ingest(0, taps, pos[:37])
+    for li in range(cfg.n_layers):
+        assert np.array_equal(one.k[0][li], kv.k[0][li]) and np.array_equal(one.v[0][li], kv.v[0][li])
+
+
+def test_fp8_cache_stores_quantised_rows_and_moves_the_output_a_little():
+    """The cached rows are the plain K/V through fp8_rows, and the forward in
+    the cache format stays near the plain forward (each K/V/q element moves
+    by at most 2^-4 of itself) but is not equal to it."""
+    cfg = MICRO_KV8
+    D = O.Drafter(cfg, oracle_weights(synth.make_weights(cfg)))
+    taps, noise, pos = _inputs(cfg, 37)
+    kv = O.DraftKV(D, kv_fp8=True)
+    kv.ingest(0, taps, pos[:37])
+    feats = D.ctx_features(taps)
+    for li in range(cfg.n_layers):
+        k, v = D.ctx_kv(li, feats, pos[:37])
+        assert np.array_equal(kv.k[0][li], O.fp8_rows(k)) and np.array_equal(kv.v[0][li], O.fp8_rows(v))
+    plain = D.forward_full(taps, noise, pos)
+    q8 = D.forward_full(taps, noise, pos, kv_fp8=True)
+    e = rel_err(q8, plain)
+    assert 1e-6 < e < 0.5, e

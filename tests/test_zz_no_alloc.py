@@ -34,7 +34,10 @@ def _inputs(cfg, ctx, rnd=0):
     return taps, noise, list(range(ctx + 16))
 
 
-@pytest.mark.parametrize("cfg", [synth.TINY_F32, SMALL_BF16], ids=["tiny_f32", "small_bf16"])
+SMALL_KV8 = dataclasses.replace(SMALL_BF16, kv_dtype="fp8")
+
+
+@pytest.mark.parametrize("cfg", [synth.TINY_F32, SMALL_BF16, SMALL_KV8], ids=["tiny_f32", "small_bf16", "small_kv8"])
 def test_static_matches_pool_forward_twice_in_a_row(cfg):
     """Two calls in a row of each entry point on the same inputs agree within
     the parity tolerance (ragged ctx: 200 rows = 3 pages + 8 rows)."""
