@@ -41,7 +41,8 @@ enum WType { W_F32 = 0, W_BF16 = 1, W_FP8 = 2 };
 // KV cache element: f32, bf16, or OCP e4m3 codes with one f32 scale per
 // (layer, page row, kv head) for K and for V.
 enum KvType { KV_F32 = 0, KV_BF16 = 1, KV_FP8 = 2 };
-enum EpiKind { EPI_FC = 0, EPI_KV = 1, EPI_QKV = 2, EPI_RESID = 3, EPI_SWIGLU = 4 };
+// Fused tile epilogues of the ingest's projections.
+enum EpiKind { EPI_FC = 0, EPI_KV = 1 };
 enum DevErr { DERR_NONE = 0, DERR_TIMEOUT = 4, DERR_BAD_PAGE = 6 };
 
 // Optional launch trace.  Per CTA, kTraceWords u64: {smid, %globaltimer at
@@ -114,27 +115,22 @@ struct Geo {
 
 // Epilogue arguments of one GEMM call site.
 struct EpiArgs {
-  int kind;
-  int layer;
+  int kind;                   // EpiKind
   int n_tok;                  // token columns of this pass
   int tok_base;               // first token of this pass
   const float* wscale;        // per weight row scale (fp8), or null
-  const float* ss_in;         // per token sum of squares -> rsqrt(ss/H+eps) scale; null = 1
-  float* ss_out;              // per token sum of squares of the epilogue's output
-  const float* gain;          // FC: hidden_norm; RESID: next pre-norm gain (or null)
-  float* h;                   // RESID: residual stream [Mt][H] f32
-  int h_ld;
-  void* op;                   // operand written for the next GEMM (hi/lo bf16 planes or f32)
+  const float* ss_in;         // KV: per token sum of squares -> rsqrt(ss/H+eps) scale; null = 1
+  float* ss_out;              // FC: per token sum of squares of the features
+  const float* gain;          // FC: hidden_norm gain
+  void* op;                   // FC: operand written for the K/V projection (hi/lo bf16 planes or f32)
   int op_ld;
   long op_plane;              // elements between hi and lo planes
   int op_f32;
-  const float* qn;            // QKV: q head-norm gain of this layer
-  const float* kn;            // QKV: k gain of this layer; KV: base of [L][d]
-  void* q_out;                // QKV: q buffer [Mt][Hq][d]
+  const float* kn;            // KV: k head-norm gains [L][d]
   void* kpool;                // K pool base (all layers)
   void* vpool;                // V^T pool base (all layers)
-  const int* dest;            // QKV/KV: per token page*64+offset (descriptor copy)
-  const float2* rope_cs;      // QKV/KV: per token [d/2] (cos, sin), mscale folded in
+  const int* dest;            // KV: per token page*64+offset (descriptor copy)
+  const float2* rope_cs;      // KV: per token [d/2] (cos, sin), mscale folded in
   int* err;
   Geo g;
 };
@@ -312,7 +308,7 @@ __device__ __forceinline__ void acc_add16(float* acc_f, int j0, int n_tok, const
 }
 
 // ------------------------------------------------------------------ epilogue
-// Head-wise epilogue (QKV of a round, K/V of an ingest) on a reduced chunk
+// Head-wise epilogue (K/V of an ingest, every layer) on a reduced chunk
 // red[t][0..127] for tokens tok0 .. tok0+tc-1.  One warp per (token, head);
 // lane l holds PER = d/32 consecutive dims, lanes 0..15 the first half (so a
 // dim's RoPE partner j + d/2 sits in lane l + 16).  Every global load of a
@@ -329,21 +325,15 @@ static __device__ void epi_heads_t(const EpiArgs& e, int tile, const float* red,
     const int t = task / heads_in_tile, sh = task % heads_in_tile;
     const int tok = e.tok_base + tok0 + t;     // global token index
     const int hh = (tile * kTileN) / d + sh;   // head index within the tile's GEMM rows
-    int layer, kind, head;                     // kind 0 q, 1 k, 2 v
-    if (e.kind == EPI_QKV) {
-      layer = e.layer;
-      kind = hh < g.Hq ? 0 : (hh < g.Hq + g.Hkv ? 1 : 2);
-      head = kind == 0 ? hh : (kind == 1 ? hh - g.Hq : hh - g.Hq - g.Hkv);
-    } else {
-      layer = hh / (2 * g.Hkv);
-      const int j = hh % (2 * g.Hkv);
-      kind = j < g.Hkv ? 1 : 2;
-      head = j < g.Hkv ? j : j - g.Hkv;
-    }
+    // the all-layer K/V matrix stacks [k heads; v heads] per layer
+    const int layer = hh / (2 * g.Hkv);
+    const int j = hh % (2 * g.Hkv);
+    const int kind = j < g.Hkv ? 1 : 2;        // 1 k, 2 v
+    const int head = j < g.Hkv ? j : j - g.Hkv;
     // loads first: gains, (cos, sin), destination row
     float gn[PER];
     float2 cs[PER];
-    const float* __restrict__ gsrc = (kind == 0) ? e.qn : (e.kind == EPI_QKV ? e.kn : e.kn + (long)layer * d);
+    const float* __restrict__ gsrc = e.kn + (long)layer * d;
     const float2* __restrict__ csrc = e.rope_cs + (long)tok * half;
     if (kind != 2) {
 #pragma unroll
@@ -352,7 +342,7 @@ static __device__ void epi_heads_t(const EpiArgs& e, int tile, const float* red,
         cs[q] = csrc[(dim0 + q) % half];
       }
     }
-    const int dst = kind != 0 ? e.dest[tok] : 0;
+    const int dst = e.dest[tok];
     const float rs = rsc[t];
     float x[PER];
 #pragma unroll
@@ -371,11 +361,7 @@ static __device__ void epi_heads_t(const EpiArgs& e, int tile, const float* red,
       }
     }
     if (g.kvtype == KV_FP8) {
-      put_row_fp8<PER>(g, x, lane, kind, layer, tok, head, dst, e.q_out, e.kpool, e.vpool);
-    } else if (kind == 0) {
-      const long base = ((long)tok * g.Hq + head) * d + dim0;
-#pragma unroll
-      for (int q = 0; q < PER; ++q) put_kv(e.q_out, base + q, x[q], g.kvtype);
+      put_row_fp8<PER>(g, x, lane, kind, layer, tok, head, dst, nullptr, e.kpool, e.vpool);
     } else {
       const int page = dst >> 6, off = dst & (kPage - 1);
 #pragma unroll
@@ -424,37 +410,14 @@ static __device__ void tile_epilogue(const EpiArgs& e, int tile, float* acc, int
     if (et == 0) trace_mark(tr, cta, 11, c0);   // 11: accumulator read
     epi_sync();
     if (et == 0) trace_mark(tr, cta, 12, c0);   // 12: row scales ready
-    if (e.kind == EPI_QKV || e.kind == EPI_KV) {
+    if (e.kind == EPI_KV) {
       epi_heads(e, tile, red, rsc, tok0, tc, et);
-    } else if (e.kind == EPI_SWIGLU) {
-      // tile rows [0,64) = gate rows, [64,128) = up rows of act columns [64*tile, 64*tile+64)
-      const int j = et & 63;
-      for (int t = et >> 6; t < tc; t += 2) {
-        const int tok = e.tok_base + tok0 + t;
-        const float gv = red[t * (kTileN + 1) + j] * rsc[t];
-        const float uv = red[t * (kTileN + 1) + 64 + j] * rsc[t];
-        const float a = gv / (1.f + __expf(-gv)) * uv;
-        put_operand(e.op, (long)tok * e.op_ld + tile * 64 + j, e.op_plane, a, e.op_f32);
-      }
-    } else {  // EPI_FC, EPI_RESID
+    } else {  // EPI_FC: features c (operand c * hidden_norm gain) and their sums of squares
       const int col = tile * kTileN + f;
       const float gn = e.gain ? e.gain[col] : 1.f;
-      if (e.kind == EPI_RESID) {
-        // all residual loads in flight at once, then the adds (red is a
-        // generic pointer the compiler cannot separate from e.h)
-        float hv[kEpiTokChunk];
-        const float* __restrict__ hcol = e.h + (long)(e.tok_base + tok0) * e.h_ld + col;
-#pragma unroll
-        for (int t = 0; t < kEpiTokChunk; ++t)
-          if (t < tc) hv[t] = __ldcg(hcol + (long)t * e.h_ld);
-#pragma unroll
-        for (int t = 0; t < kEpiTokChunk; ++t)
-          if (t < tc) red[t * (kTileN + 1) + f] += hv[t];
-      }
       for (int t = 0; t < tc; ++t) {
         const int tok = e.tok_base + tok0 + t;
         const float x = red[t * (kTileN + 1) + f];
-        if (e.kind == EPI_RESID) e.h[(long)tok * e.h_ld + col] = x;
         if (e.op) put_operand(e.op, (long)tok * e.op_ld + col, e.op_plane, x * gn, e.op_f32);
       }
       epi_sync();

@@ -505,8 +505,6 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     double x_b = nt * sp.K * 4;
     double out_b;
     if (sp.omode == O_RED) out_b = nt * sp.N * 4;
-    else if (sp.e.kind == EPI_RESID) out_b = nt * sp.N * 12;
-    else if (sp.e.kind == EPI_SWIGLU) out_b = nt * sp.N / 2 * 4;
     else if (sp.e.kind == EPI_FC) out_b = nt * sp.N * 4;
     else out_b = nt * sp.N * (g.kvtype == KV_F32 ? 4 : (g.kvtype == KV_FP8 ? 1.0 + 4.0 / g.d : 2));
     const double bytes = (double)sp.N * sp.K * esize_w(g.wtype) + (sp.wscale ? sp.N * 4.0 : 0.0) + x_b + out_b;
