@@ -197,7 +197,7 @@ def main():
         return
 
     import torch
-    from speculative_decoding_block_ingest_gb300 import dflash
+    from speculative_decoding_block_ingest_gb300 import dflash, replicas
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -278,13 +278,9 @@ def main():
     barrier()
     clocks.mark(False)
     launches = dr.launch_count() - n0
-    ms = ev0.elapsed_time(ev1)
     clk = clocks.stop()
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * K / (ms / 1e3)
+    ms = replicas.slowest_ms(ev0.elapsed_time(ev1), dist, dev)
+    value = replicas.job_throughput(world, K, ms)
 
     # ---- end-to-end pass (pass 1): pinned host inputs, copies inside the timed region
     host_taps = [t.cpu().pin_memory() for t in taps_steps]
@@ -312,11 +308,7 @@ def main():
         step_e2e(k)
     e1.record(stream)
     barrier()
-    ms_e2e = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = replicas.slowest_ms(e0.elapsed_time(e1), dist, dev)
     h2d = sum(sum(c) for c in counts[Wm:]) * width * 4 / K + B * 16 * cfg.hidden * 4
     d2h = B * 16 * cfg.hidden * 4
 
@@ -377,7 +369,7 @@ def main():
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic (seeded N(0,1/fan_in) weights, N(0,1) taps/noise)",
         "config": workload_config(wl), "roofline": roofline, "cpu_baseline": cpu,
-        "e2e": {"value": world * K / (ms_e2e / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": replicas.job_throughput(world, K, ms_e2e), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk, "gpu_launches": launches,
         "drafted_tokens_per_s": 15 * B * value, "block_rows_per_s": 16 * B * value,
