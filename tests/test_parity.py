@@ -230,3 +230,29 @@ def test_context_window_matches_oracle(cfg):
     k, v = dr.kv_read(0, 0, lens[0] - 16, 16)
     torch.cuda.synchronize()
     assert rel_err(_np(k), kv.k[0][0][-16:]) <= tol(cfg)
+
+
+@pytest.mark.parametrize("n_seq", [9, 12, 16])
+def test_wide_batch_rounds_match_oracle(n_seq):
+    """Rounds of 144, 192 and 256 block rows: the projections run as wide
+    passes (unfused hi/lo MMAs of N = 144..256, 128-row plus 16-row operand
+    boxes); every sequence against the oracle."""
+    cfg = SMALL_G8
+    dr, D = _setup(cfg, max_seqs=n_seq, max_pages=4 * n_seq, max_seq_len=512, max_batch=n_seq,
+                   max_ingest_rows=512)
+    kv = O.DraftKV(D)
+    seqs = list(range(n_seq))
+    lens = [17 * s + 5 for s in seqs]
+    taps = [synth.taps_rows(cfg, s, 0, n) for s, n in zip(seqs, lens)]
+    for s in seqs:
+        dr.ingest([s], [lens[s]], list(range(lens[s])), taps[s].to(DEV))
+        kv.ingest(s, taps[s].double().numpy(), list(range(lens[s])))
+    noise = torch.stack([synth.noise_rows(cfg, s, 0) for s in seqs])
+    pos_block = [p for n in lens for p in range(n, n + 16)]
+    got = dr.forward_round(seqs, pos_block, noise.to(DEV))
+    torch.cuda.synchronize()
+    dr.device_status()
+    ref = kv.forward_round(seqs, noise.double().numpy(), np.array(pos_block).reshape(n_seq, 16))
+    for i in range(n_seq):
+        assert rel_err(_np(got[i]), ref[i]) <= tol(cfg), i
+    dr.close()
