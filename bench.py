@@ -125,7 +125,7 @@ def oracle_rounds(wl, steps: int, warmup: int, budget_s: float = None):
     from speculative_decoding_block_ingest_gb300 import synth
     cfg = wl.cfg
     D = O.Drafter(cfg, oracle_weights(synth.make_weights(cfg)))
-    kv = O.DraftKV(D)
+    kv = O.DraftKV(D, kv_fp8=cfg.kv_dtype == "fp8")
     ctx = wl.ctx_lengths()[0]
     for r0 in range(0, ctx, 2048):
         n = min(2048, ctx - r0)
@@ -179,7 +179,7 @@ def workload_config(wl):
             "head_dim": c.head_dim, "intermediate": c.intermediate, "taps": c.n_taps, "block": c.block,
             "batch": wl.batch, "ctx": wl.ctx if wl.ctx_hi == 0 else f"U[{wl.ctx_lo},{wl.ctx_hi}]",
             "ingest_rows": f"U{{{wl.ingest_lo}..{wl.ingest_hi}}}",
-            "weights": c.weight_dtype, "kv": c.kv_dtype, "rope": c.rope_type,
+            "weights": c.weight_dtype, "kv": c.kv_dtype, "rope": c.rope_type, "conv_groups": c.conv_groups,
             "l2": "no flush: every round streams >1 GB of weights and KV, far above the 129 MB L2"}
 
 

@@ -104,6 +104,10 @@ typedef struct dflash_config {
   int32_t max_seq_len;   /* committed rows + 16 a sequence may reach       */
   int32_t max_batch;     /* n_seq per dflash_forward_round, <= 64          */
   int32_t max_ingest_rows; /* sum of t per dflash_ingest_ctx, <= 512       */
+  int32_t conv_groups;   /* DFlash2: channel groups of the grouped dynamic
+                            causal conv around every sublayer (divides H,
+                            H / conv_groups a multiple of 4, at most 256);
+                            0 = DFlash (no conv)                            */
 } dflash_config;
 
 /* One decoder layer's tensors (DflashLayer).  Projections have the dtype
@@ -117,6 +121,16 @@ typedef struct dflash_layer_weights {
   const float *k_norm;    /* [d]  */
   const float *input_ln;  /* [H]  */
   const float *post_ln;   /* [H]  */
+  /* DFlash2 (conv_groups = Gc > 0), sublayer s = 0 attention, 1 MLP
+   * (Dflash2Conv, d2_conv_prepare / d2_conv_finish): conv_base[s] f32
+   * [2][H][2] (half 0 wraps the sublayer input, half 1 its output; tap 0
+   * weighs the previous block row, tap 1 this row); conv_dyn[s] the
+   * dynamic-coefficient projection [4 Gc][H] in weight_dtype, output row
+   * (half * Gc + group) * 2 + tap (+ conv_dyn_scale[s] [4 Gc] for e4m3).
+   * Ignored when conv_groups is 0. */
+  const float *conv_base[2];
+  const void *conv_dyn[2];
+  const float *conv_dyn_scale[2];
 } dflash_layer_weights;
 
 /* Backbone tensors (DflashDraft fields fc, hidden_norm, norm, layers): no fc

@@ -160,6 +160,25 @@ def yarn_divisors(head_dim: int, base: float, factor: float, original_max_pos: i
     return 1.0 / ((1.0 - ramp) + ramp / factor)
 
 
+def dyn_causal_conv(u: np.ndarray, base: np.ndarray, coef: np.ndarray, groups: int) -> np.ndarray:
+    """Grouped dynamic causal 2-tap depthwise conv over the block rows.
+
+    DflashDraft page, ``Dflash2Conv`` (GroupedDynamicCausalConv) and
+    ``d2_conv_prepare`` / ``d2_conv_finish``: a causal 2-tap depthwise conv
+    over the block rows, block-local (row 0's missing predecessor is zero,
+    nothing carries across rounds), whose per-channel kernel is a base kernel
+    plus per-position dynamic coefficients shared by a group of channels.
+    ``u [b, H]``; ``base [H, 2]`` (tap 0 weighs the previous row, tap 1 this
+    row); ``coef [b, groups, 2]``; channel c belongs to group
+    ``c // (H / groups)`` (contiguous groups: the pages give no count or
+    order, this is the plainest grouping).
+    """
+    b, H = u.shape
+    c = np.repeat(np.asarray(coef, dtype=np.float64), H // groups, axis=1)   # [b, H, 2]
+    prev = np.vstack([np.zeros((1, H)), u[:-1]])
+    return (base[None, :, 0] + c[:, :, 0]) * prev + (base[None, :, 1] + c[:, :, 1]) * u
+
+
 def rope_tables(cfg) -> tuple:
     """``(inv_freq[d/2], mscale)`` for plain or YaRN RoPE.
 
@@ -212,7 +231,7 @@ class Drafter:
         for lw in weights["layers"]:
             L = {}
             for k, v in lw.items():
-                if k in ("q", "k", "v", "o", "gate", "up", "down"):
+                if k in ("q", "k", "v", "o", "gate", "up", "down", "conv_attn_dyn", "conv_mlp_dyn"):
                     L[k] = decode_weight(v)
                 else:
                     L[k] = np.asarray(v, dtype=np.float64)
@@ -281,6 +300,13 @@ class Drafter:
         ``[b, H]`` (module summary: qwen3-class; DflashDraft page,
         ``forward_round`` and first-light contract).
 
+        With ``cfg.conv_groups`` > 0 (a DFlash2 drafter: DflashDraft page,
+        ``Dflash2Conv``) each sublayer (attention with its projections; the
+        MLP) is wrapped in the grouped dynamic causal conv: its normed input
+        goes through ``conv_prepare`` (which also projects the dynamic
+        coefficients of both halves from that input) and its output through
+        ``conv_finish`` before the residual add.
+
         ``kv_fp8``: an FP8 KV cache (the FP8 block attention kernel named in
         spark_model::layers::dflash_head): the block rows' K and V pass
         through the cache format like context rows (:func:`fp8_rows`), and so
@@ -291,8 +317,22 @@ class Drafter:
         b = noise.shape[0]
         pos_block = np.asarray(pos_block)
         h = np.asarray(noise, dtype=np.float64).copy()
+        Gc = getattr(cfg, "conv_groups", 0)
+
+        def conv_prepare(x, sub):
+            """Dyn coefficients of both halves from the sublayer input, then
+            the input through base half 0 + dyn half 0 (Dflash2Conv)."""
+            dyn = (x @ L[f"conv_{sub}_dyn"].T).reshape(b, 2, Gc, 2)
+            return dyn_causal_conv(x, L[f"conv_{sub}_base"][0], dyn[:, 0], Gc), dyn
+
+        def conv_finish(y, dyn, sub):
+            """The sublayer output through base half 1 + dyn half 1."""
+            return dyn_causal_conv(y, L[f"conv_{sub}_base"][1], dyn[:, 1], Gc)
+
         for li, L in enumerate(self.layers):
             x = rms_norm(h, L["input_ln"], cfg.rms_eps)
+            if Gc:
+                x, dyn = conv_prepare(x, "attn")
             q = (x @ L["q"].T).reshape(b, cfg.n_heads, cfg.head_dim)
             k = (x @ L["k"].T).reshape(b, cfg.n_kv_heads, cfg.head_dim)
             v = (x @ L["v"].T).reshape(b, cfg.n_kv_heads, cfg.head_dim)
@@ -303,10 +343,18 @@ class Drafter:
             keys = np.concatenate([ctx_k[li], k], axis=0)
             vals = np.concatenate([ctx_v[li], v], axis=0)
             o = self.attention(q, keys, vals)
-            h = h + o @ L["o"].T
+            y = o @ L["o"].T
+            if Gc:
+                y = conv_finish(y, dyn, "attn")
+            h = h + y
             y = rms_norm(h, L["post_ln"], cfg.rms_eps)
+            if Gc:
+                y, dyn = conv_prepare(y, "mlp")
             a = silu(y @ L["gate"].T) * (y @ L["up"].T)
-            h = h + a @ L["down"].T
+            m = a @ L["down"].T
+            if Gc:
+                m = conv_finish(m, dyn, "mlp")
+            h = h + m
         return rms_norm(h, self.norm, cfg.rms_eps)
 
     def forward_full(self, taps: np.ndarray, noise: np.ndarray, pos: Sequence[int],

@@ -30,6 +30,7 @@ constexpr int kTileK = 64;        // K columns per unit
 constexpr int kPassTok = 256;     // token columns per GEMM pass (one MMA N)
 constexpr int kMaxBatch = 64;
 constexpr int kMaxIngestRows = 512;
+constexpr int kMaxConvGroups = 256;   // DFlash2 conv channel groups
 constexpr int kMaxHidden = 8192;  // widest residual row the row kernels hold in registers
 constexpr int kMaxPtUpdates = 160;
 constexpr int kEpiThreads = 128;  // threads running a tile epilogue

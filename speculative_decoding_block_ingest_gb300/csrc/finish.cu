@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kRowThreads) prep_norm_kernel(FinishArgs f) {
     if (4 * i < g.H) {
       const float4 x = rn.out(k);
       const long idx = (long)tok * g.H + 4 * i;
+      if (f.u_out) reinterpret_cast<float4*>(f.u_out + idx)[0] = x;
       put_operand(f.op, idx + 0, f.op_plane, x.x, f.op_f32);
       put_operand(f.op, idx + 1, f.op_plane, x.y, f.op_f32);
       put_operand(f.op, idx + 2, f.op_plane, x.z, f.op_f32);
@@ -263,6 +264,55 @@ const void* final_norm_kernel_entry() { return reinterpret_cast<const void*>(fin
 
 void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s) {
   launch_pdl(final_norm_kernel, dim3(n_tok), dim3(kRowThreads), 0, s, h, gain, out, g.H, g.eps);
+}
+
+// DFlash2 conv (DflashDraft, Dflash2Conv / d2_conv_prepare / d2_conv_finish):
+// out_t[c] = (base[half][c][0] + dyn_t[half][g][0]) * src_{t-1}[c]
+//          + (base[half][c][1] + dyn_t[half][g][1]) * src_t[c],  g = c / (H / groups),
+// src_{t-1} = 0 for the first block row of a sequence.  Four channels per
+// thread; prepare writes the operand planes (and clears the next
+// projections' red.add targets), finish adds into the residual stream.
+__global__ void __launch_bounds__(256) conv_kernel(ConvArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const Geo& g = a.g;
+  const long stride = (long)gridDim.x * blockDim.x;
+  const long t0 = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (a.half == 0) {
+    for (long i = t0; i < a.zero0_n; i += stride) a.zero0[i] = 0.f;
+    for (long i = t0; i < a.zero1_n; i += stride) a.zero1[i] = 0.f;
+  }
+  const int n4 = g.H / 4, gs = g.H / a.groups;
+  const float* b = a.base + (long)a.half * g.H * 2;
+  for (long e = t0; e < (long)a.n_tok * n4; e += stride) {
+    const int t = (int)(e / n4), c = (int)(e % n4) * 4;
+    const float4 cur = __ldcg(reinterpret_cast<const float4*>(a.src + (long)t * g.H + c));
+    const float4 prv = (t % kBlock) ? __ldcg(reinterpret_cast<const float4*>(a.src + (long)(t - 1) * g.H + c))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* dy = a.dyn + (long)t * a.dyn_ld + (long)a.half * a.groups * 2;
+    const float xc[4] = {cur.x, cur.y, cur.z, cur.w}, xp[4] = {prv.x, prv.y, prv.z, prv.w};
+    float o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int ch = c + j, grp = ch / gs;
+      o[j] = (b[2 * ch] + dy[2 * grp]) * xp[j] + (b[2 * ch + 1] + dy[2 * grp + 1]) * xc[j];
+    }
+    const long idx = (long)t * g.H + c;
+    if (a.half == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) put_operand(a.op, idx + j, a.op_plane, o[j], a.op_f32);
+    } else {
+      float4* hp = reinterpret_cast<float4*>(a.h + idx);
+      const float4 hv = *hp;
+      *hp = make_float4(hv.x + o[0], hv.y + o[1], hv.z + o[2], hv.w + o[3]);
+    }
+  }
+}
+
+void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s) {
+  const long n = std::max<long>((long)c.n_tok * c.g.H / 4, std::max(c.zero0_n, c.zero1_n));
+  const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, 4L * n_sm));
+  launch_pdl(conv_kernel, dim3(grid), dim3(256), 0, s, c);
 }
 
 void launch_qk_finish(const FinishArgs& f, cudaStream_t s) {

@@ -49,6 +49,27 @@ struct FinishArgs {
   void* q_out;            // [Mt][Hq][d]
   void* kpool;
   void* vpool;
+  float* u_out;           // prep_norm: also the normed rows in f32 [Mt][H] (DFlash2 conv input), or null
+  Geo g;
+};
+
+// DFlash2 grouped dynamic causal conv of one sublayer over the block rows
+// (16 per sequence, token t = 16 s + i; row i = 0 has no predecessor).
+struct ConvArgs {
+  int n_tok, groups;
+  int half;               // 0: prepare (sublayer input -> operand planes); 1: finish (output -> residual add)
+  const float* src;       // prepare: normed input u [Mt][H]; finish: sublayer output y [Mt][H]
+  const float* base;      // [2][H][2] of this sublayer (tap 0 previous row, tap 1 this row)
+  const float* dyn;       // [Mt][dyn_ld]: coefficients (half, group, tap) of this sublayer
+  int dyn_ld;
+  void* op;               // prepare: operand planes of the sublayer's first projection
+  long op_plane;
+  int op_f32;
+  float* h;               // finish: residual stream [Mt][H]
+  float* zero0;           // prepare: buffers the next projections red.add into, cleared here
+  long zero0_n;
+  float* zero1;
+  long zero1_n;
   Geo g;
 };
 
@@ -179,6 +200,7 @@ void launch_attention_tc8(const AttnArgs& a, int n_items, const void* tmq, const
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s);
 void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);
+void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s);
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s);
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s);
 const void* init_kernel_entry();       // kernel function addresses, to find

@@ -65,6 +65,8 @@ struct Layout {
   size_t h, op_h, op_taps, op_o, op_a, q, qkv_acc, gu_acc, ss;
   size_t gacc, rope_cs, counters, apart_o, apart_ml, rdesc, idesc, err;
   size_t mkcnt;                                         // persistent round: two counter sets
+  size_t cbase, cdyn, s_cdyn, cu, cy, cdyn_a, cdyn_m;   // DFlash2 conv: weights, u / y rows, coefficients
+  int conv_n;                                           // rows of a padded dynamic projection
   size_t total;
   int Mt, pps, max_tiles, grid_max, items_cap, n_sites;
   MkCounters mk;
@@ -137,6 +139,18 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.counters = take((size_t)Lo.n_sites * Lo.max_tiles * 4);
   Lo.apart_o = take((size_t)Lo.items_cap * R * d * 4);
   Lo.apart_ml = take((size_t)Lo.items_cap * R * 2 * 4);
+  // DFlash2 conv: base kernels [L][2 sublayers][2][H][2], dynamic
+  // projections [L][2][conv_n][H] (rows past 4 Gc zero), normed input and
+  // sublayer output rows, coefficients of the two sublayers
+  const size_t Gc = c.conv_groups;
+  Lo.conv_n = Gc ? (int)align_up(4 * Gc, kTileN) : 0;
+  Lo.cbase = take(Gc ? L * 2 * 2 * H * 2 * 4 : 0);
+  Lo.cdyn = take(L * 2 * (size_t)Lo.conv_n * H * ew);
+  Lo.s_cdyn = take(fp8 ? L * 2 * (size_t)Lo.conv_n * 4 : 0);
+  Lo.cu = take(Gc ? Mt * H * 4 : 0);
+  Lo.cy = take(Gc ? Mt * H * 4 : 0);
+  Lo.cdyn_a = take(Mt * (size_t)Lo.conv_n * 4);
+  Lo.cdyn_m = take(Mt * (size_t)Lo.conv_n * 4);
   Lo.rdesc = take(sizeof(RoundDesc));
   Lo.idesc = take(sizeof(IngestDesc));
   Lo.err = take(256);
@@ -197,6 +211,10 @@ int validate_config(const dflash_config* c) {
   if (c->max_batch < 1 || c->max_batch > kMaxBatch) return fail(DFLASH_ERR_INVALID_ARG, "max_batch must be 1..64");
   if (c->max_ingest_rows < 1 || c->max_ingest_rows > kMaxIngestRows)
     return fail(DFLASH_ERR_INVALID_ARG, "max_ingest_rows must be 1..512");
+  if (c->conv_groups < 0 || c->conv_groups > kMaxConvGroups ||
+      (c->conv_groups > 0 && (c->hidden % c->conv_groups || (c->hidden / c->conv_groups) % 4)))
+    return fail(DFLASH_ERR_INVALID_ARG, "conv_groups must be 0, or divide hidden into groups of a multiple of 4 (at most %d)",
+                kMaxConvGroups);
   return DFLASH_OK;
 }
 
@@ -595,7 +613,8 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
 // The persistent round takes bf16 rounds of up to kMkMaxTok block rows whose
 // projection stage fits at least two ring stages beside the attention buffers.
 bool mk_eligible(dflash_t* h, int n_tok) {
-  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && h->cfg.kv_dtype == DFLASH_BF16 && !h->mk_off && !h->evicted_any && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
+  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && h->cfg.kv_dtype == DFLASH_BF16 &&
+         h->cfg.conv_groups == 0 && !h->mk_off && !h->evicted_any && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
          round_mk_stages((n_tok + 15) / 16 * 16, h->g.d) >= 2;
 }
 
@@ -653,6 +672,11 @@ InitArgs round_init_args(dflash_t* h, int n_tok, const float* noise) {
   ia.rope_cs = h->at<float2>(h->lo.rope_cs);
   ia.is_round = 1;
   ia.g = h->g;
+  if (h->cfg.conv_groups > 0) {
+    // the first layer's attention coefficients are red.added from zero
+    ia.zero_ptr = h->at<float>(h->lo.cdyn_a);
+    ia.zero_n = n_tok * h->lo.conv_n;
+  }
   return ia;
 }
 
@@ -777,18 +801,81 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   fb.kpool = h->kv->kpool;
   fb.vpool = h->kv->vpool;
   fb.g = g;
+  // DFlash2: the grouped dynamic causal conv around each sublayer
+  const int Gc = h->cfg.conv_groups, conv_n = h->lo.conv_n;
+  float* cu = Gc ? h->at<float>(h->lo.cu) : nullptr;
+  float* cy = Gc ? h->at<float>(h->lo.cy) : nullptr;
+  float* dyn_sub[2] = {h->at<float>(h->lo.cdyn_a), h->at<float>(h->lo.cdyn_m)};
   auto prep_norm = [&](const float* gain) {
     FinishArgs f = fb;
     f.gain = gain;
     f.op = h->at<void>(h->lo.op_h);
     f.op_plane = (long)Mt * g.H;
-    Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * 8, s);
+    f.u_out = cu;
+    Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * (Gc ? 12 : 8), s);
     launch_prep_norm(f, s);
+  };
+  // prepare: the dynamic coefficients of sublayer `sub` (both halves) from
+  // its normed input, then the input through half 0 into the operand planes;
+  // clears the output rows and the other sublayer's coefficients, which the
+  // next projections red.add into
+  auto conv_prepare = [&](int l, int sub) {
+    const size_t m = (size_t)l * 2 + sub;
+    GemmSpec cd;
+    cd.site = 2 + 4 * l;
+    cd.W = h->at<char>(h->lo.cdyn) + m * conv_n * g.H * ew;
+    cd.wscale = fp8 ? h->at<float>(h->lo.s_cdyn) + m * conv_n : nullptr;
+    cd.N = conv_n;
+    cd.K = g.H;
+    cd.X = h->at<void>(h->lo.op_h);
+    cd.xmap = h->xmap_h;
+    cd.omode = O_RED;
+    cd.dst = dyn_sub[sub];
+    cd.dst_ld = conv_n;
+    cd.e = base_epi(h);
+    cd.e.n_tok = n_tok;
+    run_gemm(h, cd, s);
+    ConvArgs c{};
+    c.n_tok = n_tok;
+    c.groups = Gc;
+    c.half = 0;
+    c.src = cu;
+    c.base = h->at<float>(h->lo.cbase) + m * 2 * g.H * 2;
+    c.dyn = dyn_sub[sub];
+    c.dyn_ld = conv_n;
+    c.op = h->at<void>(h->lo.op_h);
+    c.op_plane = (long)Mt * g.H;
+    c.op_f32 = f32;
+    c.zero0 = cy;
+    c.zero0_n = (long)n_tok * g.H;
+    c.zero1 = dyn_sub[sub ^ 1];
+    c.zero1_n = (long)n_tok * conv_n;
+    c.g = g;
+    Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * 20, s);
+    launch_conv(c, h->n_sm, s);
+    ck(cudaGetLastError(), "conv prepare launch");
+  };
+  // finish: the sublayer output through half 1, added into the residual
+  auto conv_finish = [&](int l, int sub) {
+    ConvArgs c{};
+    c.n_tok = n_tok;
+    c.groups = Gc;
+    c.half = 1;
+    c.src = cy;
+    c.base = h->at<float>(h->lo.cbase) + ((size_t)l * 2 + sub) * 2 * g.H * 2;
+    c.dyn = dyn_sub[sub];
+    c.dyn_ld = conv_n;
+    c.h = hres;
+    c.g = g;
+    Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * 16, s);
+    launch_conv(c, h->n_sm, s);
+    ck(cudaGetLastError(), "conv finish launch");
   };
 
   for (int l = 0; l < g.L; ++l) {
     prep_norm(h->at<float>(h->lo.in_ln) + (size_t)l * g.H);
     ck(cudaGetLastError(), "input norm launch");
+    if (Gc) conv_prepare(l, 0);
 
     GemmSpec q;
     q.site = 2 + 4 * l;
@@ -861,14 +948,16 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     o.X = h->at<void>(h->lo.op_o);
     o.xmap = h->xmap_o;
     o.omode = O_RED;
-    o.dst = hres;
+    o.dst = Gc ? cy : hres;
     o.dst_ld = g.H;
     o.e = base_epi(h);
     o.e.n_tok = n_tok;
     run_gemm(h, o, s);
+    if (Gc) conv_finish(l, 0);
 
     prep_norm(h->at<float>(h->lo.post_ln) + (size_t)l * g.H);
     ck(cudaGetLastError(), "post norm launch");
+    if (Gc) conv_prepare(l, 1);
 
     GemmSpec gu;
     gu.site = 4 + 4 * l;
@@ -904,11 +993,12 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     dn.X = h->at<void>(h->lo.op_a);
     dn.xmap = h->xmap_a;
     dn.omode = O_RED;
-    dn.dst = hres;
+    dn.dst = Gc ? cy : hres;
     dn.dst_ld = g.H;
     dn.e = base_epi(h);
     dn.e.n_tok = n_tok;
     run_gemm(h, dn, s);
+    if (Gc) conv_finish(l, 1);
   }
   {
     Launch L(h, DFLASH_KERNEL_NORM, (double)n_tok * g.H * 8, s);
@@ -1256,6 +1346,13 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       return fail(DFLASH_ERR_INVALID_ARG, "missing tensor in layer %d", l);
     if (fp8 && (!L.q_scale || !L.k_scale || !L.v_scale || !L.o_scale || !L.gate_scale || !L.up_scale || !L.down_scale))
       return fail(DFLASH_ERR_INVALID_ARG, "missing fp8 scale in layer %d", l);
+    if (cfg->conv_groups > 0)
+      for (int sub = 0; sub < 2; ++sub) {
+        if (!L.conv_base[sub] || !L.conv_dyn[sub] || (fp8 && !L.conv_dyn_scale[sub]))
+          return fail(DFLASH_ERR_INVALID_ARG, "missing DFlash2 conv tensor in layer %d", l);
+        if (cfg->weight_dtype != DFLASH_F32 && !aligned16(L.conv_dyn[sub]))
+          return fail(DFLASH_ERR_INVALID_ARG, "conv_dyn must start on a 16-byte boundary");
+      }
     // bf16 and e4m3 matrices are re-blocked with 16- and 8-byte moves
     if (cfg->weight_dtype != DFLASH_F32 &&
         !(aligned16(L.q) && aligned16(L.k) && aligned16(L.v) && aligned16(L.o) && aligned16(L.gate) &&
@@ -1325,6 +1422,11 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
            "interleaved weight copy");
       }
     };
+    if (cfg->conv_groups > 0) {
+      // padding rows of the dynamic projections stay zero
+      ck(cudaMemsetAsync(h->ws + lo.cdyn, 0, lo.s_cdyn - lo.cdyn, s), "conv projection clear");
+      if (fp8) ck(cudaMemsetAsync(h->ws + lo.s_cdyn, 0, lo.cu - lo.s_cdyn, s), "conv scale clear");
+    }
     mat(lo.fc, g.n * H, w->fc, H, H, 0, 0);
     if (fp8) cp(lo.s_fc, w->fc_scale, (size_t)H * 4);
     cp(lo.hn, w->hidden_norm, (size_t)H * 4);
@@ -1339,6 +1441,15 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
       mat(lo.kvall, H, W.k, kr, kr, 0, l * g.kv_n);
       mat(lo.kvall, H, W.v, kr, kr, 0, l * g.kv_n + kr);
       mat(lo.o + (size_t)l * H * Hq * d * ew, Hq * d, W.o, H, H, 0, 0);
+      if (cfg->conv_groups > 0) {
+        const int nd = 4 * cfg->conv_groups;
+        for (int sub = 0; sub < 2; ++sub) {
+          const size_t m = (size_t)l * 2 + sub;
+          cp(lo.cbase + m * 2 * H * 2 * 4, W.conv_base[sub], (size_t)2 * H * 2 * 4);
+          mat(lo.cdyn + m * lo.conv_n * H * ew, H, W.conv_dyn[sub], nd, nd, 0, 0);
+          if (fp8) cp(lo.s_cdyn + m * lo.conv_n * 4, W.conv_dyn_scale[sub], (size_t)nd * 4);
+        }
+      }
       mat(lo.down + (size_t)l * H * I * ew, I, W.down, H, H, 0, 0);
       // gate/up interleaved in blocks of 64 rows: [g0..63, u0..63, g64..127, u64..127, ...]
       const size_t gu0 = lo.gu + (size_t)l * 2 * I * H * ew;
@@ -1409,6 +1520,8 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     ck(cudaMemsetAsync(h->ws + lo.qkv_acc, 0, (size_t)lo.Mt * g.qkv_n * 4, s), "QKV accumulator");
     ck(cudaMemsetAsync(h->ws + lo.gu_acc, 0, (size_t)lo.Mt * 2 * I * 4, s), "gate/up accumulator");
     ck(cudaMemsetAsync(h->ws + lo.err, 0, 256, s), "error word");
+    if (cfg->conv_groups > 0)
+      ck(cudaMemsetAsync(h->ws + lo.cu, 0, lo.rdesc - lo.cu, s), "conv rows and coefficients");
     ck(cudaStreamSynchronize(s), "create sync");
     return DFLASH_OK;
   });

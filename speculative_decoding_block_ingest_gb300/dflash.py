@@ -42,14 +42,17 @@ class Config(ctypes.Structure):
                 ("yarn_beta_slow", ctypes.c_double), ("weight_dtype", ctypes.c_int32),
                 ("kv_dtype", ctypes.c_int32), ("page_size", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
                 ("max_pages", ctypes.c_int32), ("max_seq_len", ctypes.c_int32),
-                ("max_batch", ctypes.c_int32), ("max_ingest_rows", ctypes.c_int32)]
+                ("max_batch", ctypes.c_int32), ("max_ingest_rows", ctypes.c_int32),
+                ("conv_groups", ctypes.c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "o", "gate", "up", "down",
                                                 "q_scale", "k_scale", "v_scale", "o_scale", "gate_scale",
                                                 "up_scale", "down_scale", "q_norm", "k_norm", "input_ln",
-                                                "post_ln")]
+                                                "post_ln")] + [
+        ("conv_base", ctypes.c_void_p * 2), ("conv_dyn", ctypes.c_void_p * 2),
+        ("conv_dyn_scale", ctypes.c_void_p * 2)]
 
 
 class Weights(ctypes.Structure):
@@ -126,7 +129,7 @@ def make_config(cfg: synth.DraftConfig, max_seqs: int, max_pages: int, max_seq_l
                   yarn_beta_fast=cfg.yarn_beta_fast, yarn_beta_slow=cfg.yarn_beta_slow,
                   weight_dtype=_DT[cfg.weight_dtype], kv_dtype=_DT[cfg.kv_dtype], page_size=cfg.page_size,
                   max_seqs=max_seqs, max_pages=max_pages, max_seq_len=max_seq_len, max_batch=max_batch,
-                  max_ingest_rows=max_ingest_rows)
+                  max_ingest_rows=max_ingest_rows, conv_groups=cfg.conv_groups)
 
 
 def workspace_bytes(config: Config) -> int:
@@ -179,6 +182,12 @@ class Drafter:
                     setattr(lw, name + "_scale", s)
                 for name in synth.NORM_TENSORS:
                     setattr(lw, name, dev(L[name].float()))
+                if cfg.conv_groups > 0:
+                    for j, sub in enumerate(synth.CONV_SUBLAYERS):
+                        lw.conv_base[j] = dev(L[f"conv_{sub}_base"].float())
+                        p, sc = proj(L[f"conv_{sub}_dyn"])
+                        lw.conv_dyn[j] = p
+                        lw.conv_dyn_scale[j] = sc
             fc, fc_s = proj(weights["fc"])
             W = Weights(fc=fc, fc_scale=fc_s, hidden_norm=dev(weights["hidden_norm"].float()),
                         norm=dev(weights["norm"].float()), layers=layers)

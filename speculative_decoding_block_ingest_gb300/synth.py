@@ -44,6 +44,12 @@ LAYER_TENSORS = ("q", "k", "v", "o", "q_norm", "k_norm", "input_ln",
                  "post_ln", "gate", "up", "down")
 PROJ_TENSORS = ("q", "k", "v", "o", "gate", "up", "down")
 NORM_TENSORS = ("q_norm", "k_norm", "input_ln", "post_ln")
+# DFlash2 drafters (conv_groups > 0): per layer, a grouped dynamic causal conv
+# around each sublayer: base kernels [2][H][2] f32 and the dynamic-coefficient
+# projection [2 * conv_groups * 2, H]
+CONV_SUBLAYERS = ("attn", "mlp")
+CONV_BASE = tuple(f"conv_{s}_base" for s in CONV_SUBLAYERS)
+CONV_PROJ = tuple(f"conv_{s}_dyn" for s in CONV_SUBLAYERS)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -67,6 +73,7 @@ class DraftConfig:
     weight_dtype: str = "bf16"        # "f32" | "bf16" | "fp8"
     kv_dtype: str = "bf16"            # "f32" | "bf16" | "fp8" (e4m3 codes + per-row scales)
     page_size: int = 64
+    conv_groups: int = 0              # DFlash2 conv channel groups; 0 = no conv (DFlash)
 
     def shape(self, name: str):
         H, d = self.hidden, self.head_dim
@@ -77,6 +84,8 @@ class DraftConfig:
             "gate": (self.intermediate, H), "up": (self.intermediate, H),
             "down": (H, self.intermediate),
             "q_norm": (d,), "k_norm": (d,), "input_ln": (H,), "post_ln": (H,),
+            "conv_attn_dyn": (4 * self.conv_groups, H), "conv_mlp_dyn": (4 * self.conv_groups, H),
+            "conv_attn_base": (2, H, 2), "conv_mlp_base": (2, H, 2),
         }[name]
 
 
@@ -117,6 +126,7 @@ QWEN3_8L = DraftConfig(n_layers=8, hidden=2048, n_heads=32, n_kv_heads=4, head_d
                        intermediate=6144, n_taps=5)
 QWEN3_8L_FP8 = dataclasses.replace(QWEN3_8L, weight_dtype="fp8")
 QWEN3_8L_FP8_KV8 = dataclasses.replace(QWEN3_8L_FP8, kv_dtype="fp8")
+QWEN3_8L_D2 = dataclasses.replace(QWEN3_8L, conv_groups=32)
 
 WORKLOADS: Dict[str, Workload] = {
     "tiny_f32": Workload("tiny_f32", TINY_F32, batch=1, ctx=64),
@@ -128,6 +138,9 @@ WORKLOADS: Dict[str, Workload] = {
                                    ctx_lo=1024, ctx_hi=16384),
     "qwen3_8l_fp8_b8_ctx65536": Workload("qwen3_8l_fp8_b8_ctx65536", QWEN3_8L_FP8, batch=8,
                                          ctx=65536, ingest_lo=16, ingest_hi=16, rounds=32),
+    # the bench shape as a DFlash2 drafter (conv of 32 channel groups around every sublayer)
+    "qwen3_8l_d2_ctx8192": Workload("qwen3_8l_d2_ctx8192", QWEN3_8L_D2, batch=1, ctx=8192,
+                                    ingest_lo=1, ingest_hi=16, rounds=200),
     # the same rounds over an e4m3 KV cache (half the cache bytes)
     "qwen3_8l_fp8_kv8_b8_ctx65536": Workload("qwen3_8l_fp8_kv8_b8_ctx65536", QWEN3_8L_FP8_KV8, batch=8,
                                              ctx=65536, ingest_lo=16, ingest_hi=16, rounds=32),
@@ -180,6 +193,26 @@ def make_weights(cfg: DraftConfig, seed: int = WEIGHT_SEED,
             layer[name] = proj(name) if name in PROJ_TENSORS else gain(name)
         W["layers"].append(layer)
     W["norm"] = gain("norm")
+    if cfg.conv_groups > 0:
+        # drawn from a generator of their own, so the backbone tensors of a
+        # DFlash2 drafter equal those of the same drafter without the conv:
+        # base kernels near the identity (this row 1 + N(0, 0.02), previous
+        # row N(0, 0.1)), dynamic projections N(0, 0.01 / fan_in)
+        gc = torch.Generator().manual_seed(_derive(seed, "conv"))
+        for layer in W["layers"]:
+            for sub in CONV_SUBLAYERS:
+                H = cfg.hidden
+                base = torch.empty(2, H, 2)
+                base[:, :, 0] = 0.1 * torch.randn(2, H, generator=gc)
+                base[:, :, 1] = 1.0 + 0.02 * torch.randn(2, H, generator=gc)
+                layer[f"conv_{sub}_base"] = base
+                w = 0.1 * torch.randn(4 * cfg.conv_groups, H, generator=gc) / math.sqrt(H)
+                if cfg.weight_dtype == "f32":
+                    layer[f"conv_{sub}_dyn"] = w
+                elif cfg.weight_dtype == "bf16":
+                    layer[f"conv_{sub}_dyn"] = w.to(torch.bfloat16)
+                else:
+                    layer[f"conv_{sub}_dyn"] = _to_fp8(w.to(torch.bfloat16))
     return W
 
 

@@ -25,7 +25,7 @@ def oracle_weights(W: dict) -> dict:
     out = {"fc": stored(W["fc"]), "hidden_norm": W["hidden_norm"].double().numpy(),
            "norm": W["norm"].double().numpy(), "layers": []}
     for L in W["layers"]:
-        out["layers"].append({k: (stored(v) if k in synth.PROJ_TENSORS else v.double().numpy())
+        out["layers"].append({k: (stored(v) if k in synth.PROJ_TENSORS + synth.CONV_PROJ else v.double().numpy())
                               for k, v in L.items()})
     return out
 

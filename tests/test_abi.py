@@ -113,3 +113,10 @@ def test_fp8_kv_cache_config(lib):
     assert abs((n16 - n8) - 2 * (per_pool_16 - per_pool_8)) <= 4096
     assert _ws(_cfg(kv_dtype=dflash.FP8, head_dim=64))[0] == dflash.ERR_UNSUPPORTED
     assert _ws(_cfg(kv_dtype=dflash.FP8, weight_dtype=dflash.F32))[0] == dflash.ERR_UNSUPPORTED
+
+
+def test_dflash2_conv_groups_validated(lib):
+    assert _ws(_cfg(conv_groups=16))[0] == 0
+    assert _ws(_cfg(conv_groups=-1))[0] == dflash.ERR_INVALID_ARG
+    assert _ws(_cfg(conv_groups=3))[0] == dflash.ERR_INVALID_ARG       # does not divide 2048
+    assert _ws(_cfg(conv_groups=1024))[0] == dflash.ERR_INVALID_ARG    # groups of 2 channels

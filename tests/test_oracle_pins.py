@@ -646,3 +646,174 @@ def test_fp8_cache_stores_quantised_rows_and_moves_the_output_a_little():
     q8 = D.forward_full(taps, noise, pos, kv_fp8=True)
     e = rel_err(q8, plain)
     assert 1e-6 < e < 0.5, e
+
+
+# ---------------------------------------------------------------- DFlash2 conv
+def _scalar_forward_dflash2(cfg, W, taps, noise, pos, inv, mscale):
+    """Scalar-loop forward of a DFlash2 drafter: every sublayer wrapped in the
+    grouped dynamic causal conv (coefficients of both halves projected from
+    the sublayer's normed input; the input through half 0, the output through
+    half 1; row 0 without a predecessor), written independently of the
+    oracle's array code."""
+    H, d, Hq, Hkv, I = cfg.hidden, cfg.head_dim, cfg.n_heads, cfg.n_kv_heads, cfg.intermediate
+    G, eps, Gc = Hq // Hkv, cfg.rms_eps, cfg.conv_groups
+    gs = H // Gc
+
+    def mat(w):
+        return _torch_weight(w).tolist()
+
+    def lin(Wm, x):
+        return [sum(Wm[o][i] * x[i] for i in range(len(x))) for o in range(len(Wm))]
+
+    def norm(x, g):
+        r = 1.0 / math.sqrt(sum(v * v for v in x) / len(x) + eps)
+        return [g[i] * x[i] * r for i in range(len(x))]
+
+    def rope(x, p):
+        half = d // 2
+        out = [0.0] * d
+        for j in range(half):
+            t = p * inv[j]
+            out[j] = mscale * (x[j] * math.cos(t) - x[j + half] * math.sin(t))
+            out[j + half] = mscale * (x[j + half] * math.cos(t) + x[j] * math.sin(t))
+        return out
+
+    def conv(rows, base, dyn, half):
+        out = []
+        for i, r in enumerate(rows):
+            row = []
+            for c in range(H):
+                g = c // gs
+                k0 = base[half][c][0] + dyn[i][(half * Gc + g) * 2 + 0]
+                k1 = base[half][c][1] + dyn[i][(half * Gc + g) * 2 + 1]
+                row.append(k0 * (rows[i - 1][c] if i > 0 else 0.0) + k1 * r[c])
+            out.append(row)
+        return out
+
+    ctx = len(taps)
+    fc = mat(W["fc"])
+    feats = [norm(lin(fc, list(taps[r])), W["hidden_norm"].tolist()) for r in range(ctx)]
+    hs = [list(noise[i]) for i in range(len(noise))]
+    b = len(hs)
+    for L in W["layers"]:
+        Wq, Wk, Wv, Wo = mat(L["q"]), mat(L["k"]), mat(L["v"]), mat(L["o"])
+        Wg, Wu, Wd = mat(L["gate"]), mat(L["up"]), mat(L["down"])
+        Wda, Wdm = mat(L["conv_attn_dyn"]), mat(L["conv_mlp_dyn"])
+        ba, bm = L["conv_attn_base"].tolist(), L["conv_mlp_base"].tolist()
+        qn, kn = L["q_norm"].tolist(), L["k_norm"].tolist()
+        keys, vals = [], []
+        for r in range(ctx):
+            k, v = lin(Wk, feats[r]), lin(Wv, feats[r])
+            keys.append([rope(norm(k[g * d:(g + 1) * d], kn), pos[r]) for g in range(Hkv)])
+            vals.append([v[g * d:(g + 1) * d] for g in range(Hkv)])
+        xs = [norm(h, L["input_ln"].tolist()) for h in hs]
+        dyn = [lin(Wda, x) for x in xs]
+        xs = conv(xs, ba, dyn, 0)
+        qs = []
+        for i, x in enumerate(xs):
+            q, k, v = lin(Wq, x), lin(Wk, x), lin(Wv, x)
+            qs.append([rope(norm(q[h * d:(h + 1) * d], qn), pos[ctx + i]) for h in range(Hq)])
+            keys.append([rope(norm(k[g * d:(g + 1) * d], kn), pos[ctx + i]) for g in range(Hkv)])
+            vals.append([v[g * d:(g + 1) * d] for g in range(Hkv)])
+        ys = []
+        for i in range(b):
+            o = []
+            for h in range(Hq):
+                g = h // G
+                s = [sum(qs[i][h][j] * keys[n][g][j] for j in range(d)) / math.sqrt(d) for n in range(len(keys))]
+                m = max(s)
+                e = [math.exp(z - m) for z in s]
+                z = sum(e)
+                o += [sum(e[n] / z * vals[n][g][j] for n in range(len(keys))) for j in range(d)]
+            ys.append(lin(Wo, o))
+        ys = conv(ys, ba, dyn, 1)
+        hs = [[a + c for a, c in zip(hs[i], ys[i])] for i in range(b)]
+        y2 = [norm(h, L["post_ln"].tolist()) for h in hs]
+        dyn2 = [lin(Wdm, y) for y in y2]
+        y2 = conv(y2, bm, dyn2, 0)
+        ms = []
+        for y in y2:
+            gg, uu = lin(Wg, y), lin(Wu, y)
+            act = [gg[j] / (1 + math.exp(-gg[j])) * uu[j] for j in range(I)]
+            ms.append(lin(Wd, act))
+        ms = conv(ms, bm, dyn2, 1)
+        hs = [[a + c for a, c in zip(hs[i], ms[i])] for i in range(b)]
+    return np.array([norm(h, W["norm"].tolist()) for h in hs])
+
+
+MICRO_D2 = synth.DraftConfig(n_layers=2, hidden=8, n_heads=2, n_kv_heads=1, head_dim=4, intermediate=8,
+                             n_taps=2, block=3, weight_dtype="f32", kv_dtype="f32", rope_theta=100.0,
+                             conv_groups=2)
+
+
+def _d2_micro():
+    D, W = _drafter(MICRO_D2, seed=9)
+    # the seeded conv weights sit near the identity; make them clearly not
+    g = torch.Generator().manual_seed(5)
+    for L in W["layers"]:
+        for sub in synth.CONV_SUBLAYERS:
+            L[f"conv_{sub}_base"] = torch.randn(2, 8, 2, generator=g)
+            L[f"conv_{sub}_dyn"] = torch.randn(8, 8, generator=g)
+    D = O.Drafter(MICRO_D2, oracle_weights(W))
+    g = torch.Generator().manual_seed(3)
+    taps = torch.randn(2, 16, generator=g, dtype=torch.float64).numpy()
+    noise = torch.randn(3, 8, generator=g, dtype=torch.float64).numpy()
+    return D, W, taps, noise, [0, 1, 2, 3, 4]
+
+
+def test_brute_force_micro_dflash2():
+    D, W, taps, noise, pos = _d2_micro()
+    ref = _scalar_forward_dflash2(MICRO_D2, W, taps, noise, pos, list(D.inv_freq), D.mscale)
+    assert rel_err(D.forward_full(taps, noise, pos), ref) < 1e-12
+
+
+def test_planted_conv_tap_swap_is_caught(monkeypatch):
+    D, W, taps, noise, pos = _d2_micro()
+    ref = _scalar_forward_dflash2(MICRO_D2, W, taps, noise, pos, list(D.inv_freq), D.mscale)
+    good = O.dyn_causal_conv
+    monkeypatch.setattr(O, "dyn_causal_conv", lambda u, b, c, g: good(u, b[:, ::-1], c[..., ::-1], g))
+    assert rel_err(D.forward_full(taps, noise, pos), ref) > 1e-3
+
+
+def test_dyn_causal_conv_shift_identity_and_groups():
+    rng = np.random.default_rng(2)
+    u = rng.standard_normal((5, 12))
+    zero = np.zeros((5, 3, 2))
+    ident = np.tile([0.0, 1.0], (12, 1))
+    shift = np.tile([1.0, 0.0], (12, 1))
+    assert np.array_equal(O.dyn_causal_conv(u, ident, zero, 3), u)
+    sh = O.dyn_causal_conv(u, shift, zero, 3)
+    assert np.array_equal(sh[0], np.zeros(12)) and np.array_equal(sh[1:], u[:-1])
+    # a coefficient of group 1 touches only channels 4..7, rows of its position
+    coef = zero.copy()
+    coef[2, 1, 1] = 0.5
+    diff = O.dyn_causal_conv(u, ident, coef, 3) - u
+    assert np.allclose(diff[2, 4:8], 0.5 * u[2, 4:8]) and np.count_nonzero(diff) == 4
+    # causal: changing row 3 changes only rows 3 and 4
+    base = rng.standard_normal((12, 2))
+    c = rng.standard_normal((5, 3, 2))
+    u2 = u.copy()
+    u2[3] += 1.0
+    d = O.dyn_causal_conv(u2, base, c, 3) - O.dyn_causal_conv(u, base, c, 3)
+    assert np.all(d[:3] == 0) and np.any(d[3] != 0) and np.any(d[4] != 0)
+
+
+def test_identity_conv_reduces_dflash2_to_dflash():
+    """Base kernels (0, 1) and zero dynamic projections: the DFlash2 drafter
+    equals the same backbone without the conv."""
+    cfg2 = dataclasses.replace(MICRO, conv_groups=4)
+    D1, W1 = _drafter(MICRO)
+    W2 = synth.make_weights(cfg2)
+    for L in W2["layers"]:
+        for sub in synth.CONV_SUBLAYERS:
+            base = torch.zeros(2, cfg2.hidden, 2)
+            base[:, :, 1] = 1.0
+            L[f"conv_{sub}_base"] = base
+            L[f"conv_{sub}_dyn"] = torch.zeros(4 * cfg2.conv_groups, cfg2.hidden)
+    D2 = O.Drafter(cfg2, oracle_weights(W2))
+    taps, noise, pos = _inputs(MICRO, 21)
+    assert np.array_equal(D2.forward_full(taps, noise, pos), D1.forward_full(taps, noise, pos))
+    kv = O.DraftKV(D2)
+    kv.ingest(0, taps, pos[:21])
+    rnd = kv.forward_round([0], noise[None], np.array([pos[21:]]))[0]
+    assert np.allclose(rnd, D1.forward_full(taps, noise, pos), rtol=0, atol=1e-12)
