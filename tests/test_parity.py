@@ -1,6 +1,6 @@
 """GPU parity: the CUDA path through the C ABI against the f64 CPU oracle.
 
-Bar (BASELINE tolerances): max|d|/rms(ref) <= 1e-4 for f32 drafters and
+Bar: max|d|/rms(ref) <= 1e-4 for f32 drafters and
 <= 2e-2 for bf16 / fp8-weight drafters; greedy argmax through a seeded
 lm_head agrees on >= 99% of slots.
 """
