@@ -122,7 +122,8 @@ typedef struct dflash_layer_weights {
   const float *input_ln;  /* [H]  */
   const float *post_ln;   /* [H]  */
   /* DFlash2 (conv_groups = Gc > 0), sublayer s = 0 attention, 1 MLP
-   * (Dflash2Conv, d2_conv_prepare / d2_conv_finish): conv_base[s] f32
+   * (memra_engine::dflash Dflash2Conv; DflashDraft d2_conv_prepare /
+   * d2_conv_finish): conv_base[s] f32
    * [2][H][2] (half 0 wraps the sublayer input, half 1 its output; tap 0
    * weighs the previous block row, tap 1 this row); conv_dyn[s] the
    * dynamic-coefficient projection [4 Gc][H] in weight_dtype, output row

@@ -163,7 +163,8 @@ def yarn_divisors(head_dim: int, base: float, factor: float, original_max_pos: i
 def dyn_causal_conv(u: np.ndarray, base: np.ndarray, coef: np.ndarray, groups: int) -> np.ndarray:
     """Grouped dynamic causal 2-tap depthwise conv over the block rows.
 
-    DflashDraft page, ``Dflash2Conv`` (GroupedDynamicCausalConv) and
+    memra_engine::dflash (module index), ``Dflash2Conv``
+    (GroupedDynamicCausalConv), and DflashDraft page,
     ``d2_conv_prepare`` / ``d2_conv_finish``: a causal 2-tap depthwise conv
     over the block rows, block-local (row 0's missing predecessor is zero,
     nothing carries across rounds), whose per-channel kernel is a base kernel
@@ -300,7 +301,7 @@ class Drafter:
         ``[b, H]`` (module summary: qwen3-class; DflashDraft page,
         ``forward_round`` and first-light contract).
 
-        With ``cfg.conv_groups`` > 0 (a DFlash2 drafter: DflashDraft page,
+        With ``cfg.conv_groups`` > 0 (a DFlash2 drafter: memra_engine::dflash,
         ``Dflash2Conv``) each sublayer (attention with its projections; the
         MLP) is wrapped in the grouped dynamic causal conv: its normed input
         goes through ``conv_prepare`` (which also projects the dynamic

@@ -266,7 +266,7 @@ void launch_final_norm(const float* h, const float* gain, float* out, int n_tok,
   launch_pdl(final_norm_kernel, dim3(n_tok), dim3(kRowThreads), 0, s, h, gain, out, g.H, g.eps);
 }
 
-// DFlash2 conv (DflashDraft, Dflash2Conv / d2_conv_prepare / d2_conv_finish):
+// DFlash2 conv (memra_engine::dflash, Dflash2Conv; DflashDraft, d2_conv_prepare / d2_conv_finish):
 // out_t[c] = (base[half][c][0] + dyn_t[half][g][0]) * src_{t-1}[c]
 //          + (base[half][c][1] + dyn_t[half][g][1]) * src_t[c],  g = c / (H / groups),
 // src_{t-1} = 0 for the first block row of a sequence.  Four channels per
