@@ -271,8 +271,16 @@ int dflash_kv_read(dflash_t *h, int32_t seq_id, int32_t layer, int32_t row0, int
                    float *k_out, float *v_out, void *stream);
 
 /* Synchronise the handle's last stream and report the device error word
- * (0 = none; else a DFLASH_ERR_* code a kernel recorded). */
+ * (0 = none; else a DFLASH_ERR_* code a kernel recorded: DFLASH_ERR_TIMEOUT
+ * when a bounded device-side wait gave up).  A reported error is cleared,
+ * so the next call reports only what happens after it. */
 int dflash_device_status(dflash_t *h, void *stream);
+
+/* Failure-path self-test: launch one bounded wait on a device barrier that
+ * nothing arrives on; after limit_ms (1..2000) of device time the kernel
+ * records DFLASH_ERR_TIMEOUT in the error word and returns (no trap, the
+ * context stays usable), which the next dflash_device_status reports. */
+int dflash_selftest_wait_timeout(dflash_t *h, int32_t limit_ms, void *stream);
 
 /* Kernel kinds reported by the measurement calls below. */
 enum dflash_kernel_kind {

@@ -190,6 +190,10 @@ cudaError_t launch_round_mk(const MkArgs& a, int grid, const void* tmxh, const v
 constexpr size_t kFixedKvBytes = size_t(16) << 20;
 constexpr int kFixedMaxDevices = 64;
 cudaError_t fixed_kv_region(void** base, uint64_t user, bool* fresh);
+
+// One bounded wait on a barrier nothing arrives on: records DERR_TIMEOUT in
+// *err after limit_ns (selftest.cu).
+void launch_selftest_wait(int* err, unsigned long long limit_ns, cudaStream_t s);
 void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s);
 void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
                          cudaStream_t s);

@@ -1763,8 +1763,26 @@ int dflash_device_status(dflash_t* h, void* stream) {
     cudaStream_t s = stream ? static_cast<cudaStream_t>(stream) : h->last_stream;
     ck(cudaMemcpyAsync(&err, h->ws + h->lo.err, 4, cudaMemcpyDeviceToHost, s), "error word read");
     ck(cudaStreamSynchronize(s), "status sync");
+    if (err) {
+      // reported once: the word is cleared for the calls that follow
+      ck(cudaMemsetAsync(h->ws + h->lo.err, 0, 4, s), "error word clear");
+      ck(cudaStreamSynchronize(s), "status sync");
+    }
     if (err == DERR_TIMEOUT) return fail(DFLASH_ERR_TIMEOUT, "a device-side wait timed out");
     if (err) return fail(DFLASH_ERR_CUDA, "device error word %d", err);
+    return DFLASH_OK;
+  });
+}
+
+int dflash_selftest_wait_timeout(dflash_t* h, int32_t limit_ms, void* stream) {
+  g_last_error.clear();
+  if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
+  if (limit_ms < 1 || limit_ms > 2000) return fail(DFLASH_ERR_INVALID_ARG, "limit_ms must be 1..2000");
+  return guarded([&]() -> int {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    launch_selftest_wait(h->at<int>(h->lo.err), (unsigned long long)limit_ms * 1000000ull, s);
+    ck(cudaGetLastError(), "self-test launch");
+    h->last_stream = s;
     return DFLASH_OK;
   });
 }

@@ -27,7 +27,8 @@ EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dfla
            "dflash_forward_full", "dflash_forward_full_static", "dflash_lm_head_bytes", "dflash_pack_lm_head",
            "dflash_draft_tokens", "dflash_set_ctx_cap", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
            "dflash_device_status", "dflash_destroy", "dflash_last_error", "dflash_profile_enable",
-           "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches")
+           "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches",
+           "dflash_selftest_wait_timeout")
 TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
 KERNEL_KINDS = ("gemm", "attention", "combine", "init", "norm", "finish", "round")
 
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_seq_len.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64)]
     lib.dflash_kv_read.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp]
     lib.dflash_device_status.argtypes = [vp, vp]
+    lib.dflash_selftest_wait_timeout.argtypes = [vp, i32, vp]
     lib.dflash_profile_enable.argtypes = [vp, i32]
     lib.dflash_profile_read.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_double)]
@@ -283,6 +285,12 @@ class Drafter:
 
     def device_status(self, stream=None):
         _check(self.lib.dflash_device_status(self.handle, _stream_ptr(stream)))
+
+    def selftest_wait_timeout(self, limit_ms: int = 100, stream=None):
+        """Launch one bounded device wait that always expires (the failure
+        path of every pipeline wait); the next device_status raises
+        DflashError(ERR_TIMEOUT)."""
+        _check(self.lib.dflash_selftest_wait_timeout(self.handle, int(limit_ms), _stream_ptr(stream)))
 
     def profile(self, enable: bool):
         _check(self.lib.dflash_profile_enable(self.handle, 1 if enable else 0))

@@ -120,3 +120,7 @@ def test_dflash2_conv_groups_validated(lib):
     assert _ws(_cfg(conv_groups=-1))[0] == dflash.ERR_INVALID_ARG
     assert _ws(_cfg(conv_groups=3))[0] == dflash.ERR_INVALID_ARG       # does not divide 2048
     assert _ws(_cfg(conv_groups=1024))[0] == dflash.ERR_INVALID_ARG    # groups of 2 channels
+
+
+def test_selftest_rejects_null_handle_and_bad_limit(lib):
+    assert lib.dflash_selftest_wait_timeout(None, 100, None) == dflash.ERR_INVALID_ARG
