@@ -1593,9 +1593,21 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
                 ctx, std::max(0, fixed_pages * kPage - kBlock));
   void* base = nullptr;
   bool fresh = false;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
   {
     const cudaError_t e = fixed_kv_region(&base, h->uid, &fresh);
     if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "static KV region lookup: %s", cudaGetErrorString(e));
+  }
+  if (fresh) {
+    // another handle wrote the region last: clear this drafter's K and V
+    // areas before anything else can fail (the lookup already recorded this
+    // handle as the region's user; a failed clear hands the region back)
+    const cudaError_t e = cudaMemsetAsync(base, 0, 2 * (size_t)fixed_pages * page_bytes, s);
+    if (e != cudaSuccess) {
+      bool unused = false;
+      fixed_kv_region(&base, 0, &unused);
+      return fail(DFLASH_ERR_CUDA, "static KV region clear: %s", cudaGetErrorString(e));
+    }
   }
   if (!h->fixed.kpool) {
     const int rc = guarded([&]() -> int {
@@ -1616,12 +1628,6 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
       return DFLASH_OK;
     });
     if (rc != DFLASH_OK) return rc;
-  }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (fresh) {
-    // another handle wrote the region last: clear this drafter's K and V areas
-    const cudaError_t e = cudaMemsetAsync(h->fixed.kpool, 0, 2 * (size_t)fixed_pages * page_bytes, s);
-    if (e != cudaSuccess) return fail(DFLASH_ERR_CUDA, "static KV region clear: %s", cudaGetErrorString(e));
   }
   release_slot(h, h->cfg.max_seqs);   // pool pages, if any were left
   h->fixed.free_pages.resize(h->fixed.max_pages);

@@ -23,7 +23,8 @@ static __device__ __align__(256) unsigned char g_fixed_kv[kFixedKvBytes];
 
 // Device address of the region on the current device.  The first call on a
 // device (with that device current) looks it up once.  *fresh: the region
-// was last used by a handle other than `user` (the caller clears it).
+// was last used by a handle other than `user` (the caller clears it); `user`
+// is recorded as the last user (0, an id no handle has, marks it unclaimed).
 cudaError_t fixed_kv_region(void** base, uint64_t user, bool* fresh) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
