@@ -307,13 +307,19 @@ int dflash_profile_enable(dflash_t *h, int32_t enable);
  * in ms and summed algorithmic bytes (waits for the recorded events). */
 int dflash_profile_read(dflash_t *h, int32_t kind, int64_t *launches, double *ms, double *bytes);
 
-/* Launch trace (measurement).  While a buffer is set, every tensor-core
- * projection and attention launch writes, per CTA, 16 u64 words into the next
- * free region of `device_buffer`: the SM id, the %globaltimer (ns) at entry,
- * then SM clock cycles since entry at fixed points of the kernel (set-up
- * done, launch wait passed, last MMA issued, epilogue steps, exit; unused
- * stamps stay as they were).  Launches that no longer fit are not traced.  NULL stops
- * tracing.  The buffer is the caller's; the library never reads it. */
+/* Launch trace (measurement).  While a buffer is set, every kernel launch of
+ * the handle writes, per CTA, 16 u64 words into the next free region of
+ * `device_buffer`: word 0 the SM id, word 1 the %globaltimer (ns) at entry,
+ * word 15 the %globaltimer at exit; the tensor-core projection and attention
+ * kernels also write words 2..14: SM clock cycles since entry at fixed
+ * points of the kernel (set-up done, launch wait passed, last MMA issued,
+ * epilogue steps, exit) or cycle counts spent waiting (projection points 9,
+ * 11, 12: producer waiting for free stages, first MMA issuer waiting for
+ * loaded stages and for a free accumulator).  Unused words stay as they
+ * were.  Rounds still run as CUDA graphs while tracing, each captured afresh
+ * with its own trace regions.  Launches that no longer fit are not traced.
+ * NULL stops tracing (after a device synchronisation when traced rounds
+ * ran).  The buffer is the caller's; the library never reads it. */
 int dflash_trace_begin(dflash_t *h, void *device_buffer, size_t bytes);
 
 /* Traced launches so far: kernel kind (dflash_kernel_kind), CTA count and the

@@ -47,9 +47,9 @@ enum EpiKind { EPI_FC = 0, EPI_KV = 1 };
 enum DevErr { DERR_NONE = 0, DERR_TIMEOUT = 4, DERR_BAD_PAGE = 6 };
 
 // Optional launch trace.  Per CTA, kTraceWords u64: {smid, %globaltimer at
-// entry (ns), then SM clock64 cycles since entry at fixed points 1..14 of the
-// kernel (see each kernel)}.  Points written by one warp compare exactly;
-// points of different warps only roughly.
+// entry (ns), SM clock64 cycles since entry at fixed points 1..13 of the
+// kernel (see each kernel), %globaltimer at exit}.  Points written by one
+// warp compare exactly; points of different warps only roughly.
 constexpr int kTraceWords = 16;
 __device__ __forceinline__ unsigned long long trace_clock() {
   unsigned long long c;
@@ -72,6 +72,26 @@ __device__ __forceinline__ void trace_mark(unsigned long long* tr, int cta, int 
     const unsigned long long v = trace_clock() - c0;
     asm volatile("st.global.u64 [%0], %1;" ::"l"(tr + (long)cta * kTraceWords + 1 + point), "l"(v) : "memory");
   }
+}
+// A measured quantity (e.g. cycles spent waiting) at point `point`.
+__device__ __forceinline__ void trace_put(unsigned long long* tr, int cta, int point, unsigned long long v) {
+  if (tr) asm volatile("st.global.u64 [%0], %1;" ::"l"(tr + (long)cta * kTraceWords + 1 + point), "l"(v) : "memory");
+}
+// %globaltimer (ns) at the CTA's exit in the last word (after point 13).
+__device__ __forceinline__ void trace_exit(unsigned long long* tr, int cta) {
+  if (tr) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    asm volatile("st.global.u64 [%0], %1;" ::"l"(tr + (long)cta * kTraceWords + kTraceWords - 1), "l"(t) : "memory");
+  }
+}
+// Entry and exit stamps of the element-wise kernels (thread 0 of each CTA).
+__device__ __forceinline__ void trace_cta_entry(unsigned long long* tr) {
+  unsigned long long c0;
+  if (tr && threadIdx.x == 0) trace_entry(tr, blockIdx.x, &c0);
+}
+__device__ __forceinline__ void trace_cta_exit(unsigned long long* tr) {
+  if (tr && threadIdx.x == 0) trace_exit(tr, blockIdx.x);
 }
 
 // Per-call descriptor of a drafting round (device copy lives in the workspace).

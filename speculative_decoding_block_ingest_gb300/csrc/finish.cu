@@ -64,8 +64,9 @@ struct RowNorm {
 };
 
 __global__ void __launch_bounds__(kRowThreads) prep_norm_kernel(FinishArgs f) {
-  pdl_wait();
+  trace_cta_entry(f.trace);
   pdl_launch_dependents();
+  pdl_wait();
   const int tok = blockIdx.x;
   const Geo& g = f.g;
   RowNorm rn;
@@ -83,13 +84,15 @@ __global__ void __launch_bounds__(kRowThreads) prep_norm_kernel(FinishArgs f) {
       put_operand(f.op, idx + 3, f.op_plane, x.w, f.op_f32);
     }
   }
+  trace_cta_exit(f.trace);
 }
 
 // Final RMSNorm of the residual stream into the f32 output rows.
 __global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* h, const float* gain, float* out, int H,
-                                                               float eps) {
-  pdl_wait();
+                                                               float eps, unsigned long long* trace) {
+  trace_cta_entry(trace);
   pdl_launch_dependents();
+  pdl_wait();
   const int tok = blockIdx.x;
   RowNorm rn;
   rn.load(h + (long)tok * H, gain, H, eps);
@@ -99,6 +102,7 @@ __global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* h,
     const int i = threadIdx.x + k * kRowThreads;
     if (4 * i < H) o4[i] = rn.out(k);
   }
+  trace_cta_exit(trace);
 }
 
 // One warp per (token, head) row of the QKV accumulator.
@@ -159,8 +163,9 @@ __device__ void qk_finish_row(const FinishArgs& f, int tok, int hh) {
 }
 
 __global__ void __launch_bounds__(128) qk_finish_kernel(FinishArgs f) {
-  pdl_wait();
+  trace_cta_entry(f.trace);
   pdl_launch_dependents();
+  pdl_wait();
   const Geo& g = f.g;
   const int heads = g.Hq + 2 * g.Hkv;
   const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
@@ -168,11 +173,13 @@ __global__ void __launch_bounds__(128) qk_finish_kernel(FinishArgs f) {
   const int tok = row / heads, hh = row % heads;
   if (g.d == 128) qk_finish_row<4>(f, tok, hh);
   else qk_finish_row<2>(f, tok, hh);
+  trace_cta_exit(f.trace);
 }
 
 __global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
-  pdl_wait();
+  trace_cta_entry(f.trace);
   pdl_launch_dependents();
+  pdl_wait();
   const Geo& g = f.g;
   const long n4 = (long)f.n_tok * g.I / 4;
   for (long k = (long)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (long)gridDim.x * blockDim.x) {
@@ -188,12 +195,13 @@ __global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
     for (int q = 0; q < 4; ++q)
       put_operand(f.op, (long)tok * g.I + j + q, f.op_plane, gg[q] / (1.f + __expf(-gg[q])) * uu[q], f.op_f32);
   }
+  trace_cta_exit(f.trace);
 }
 
 // f32 rows -> hi/lo bf16 operand planes (no norm): the lm_head's operand.
 __global__ void __launch_bounds__(kRowThreads) to_operand_kernel(const float* src, int width, void* op, long plane) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   const int row = blockIdx.x, n4 = width / 4;
   const float4* r4 = reinterpret_cast<const float4*>(src + (long)row * width);
   for (int c = threadIdx.x; c < n4; c += kRowThreads) {
@@ -215,8 +223,8 @@ __device__ __forceinline__ void better(float& bv, int& bi, float v, int i) {
 }
 
 __global__ void __launch_bounds__(kRowThreads) argmax_kernel(const float* logits, int V, int32_t* tokens) {
-  pdl_wait();
   pdl_launch_dependents();
+  pdl_wait();
   const int row = blockIdx.x;
   const float4* l4 = reinterpret_cast<const float4*>(logits + (long)row * V);
   float bv = -INFINITY;
@@ -256,14 +264,17 @@ void launch_argmax(const float* logits, int n_rows, int V, int32_t* tokens, cuda
   launch_pdl(argmax_kernel, dim3(n_rows), dim3(kRowThreads), 0, s, logits, V, tokens);
 }
 
+int prep_norm_grid(const FinishArgs& f) { return f.n_tok; }
+
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s) {
-  launch_pdl(prep_norm_kernel, dim3(f.n_tok), dim3(kRowThreads), 0, s, f);
+  launch_pdl(prep_norm_kernel, dim3(prep_norm_grid(f)), dim3(kRowThreads), 0, s, f);
 }
 
 const void* final_norm_kernel_entry() { return reinterpret_cast<const void*>(final_norm_kernel); }
 
-void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s) {
-  launch_pdl(final_norm_kernel, dim3(n_tok), dim3(kRowThreads), 0, s, h, gain, out, g.H, g.eps);
+void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g,
+                       unsigned long long* trace, cudaStream_t s) {
+  launch_pdl(final_norm_kernel, dim3(n_tok), dim3(kRowThreads), 0, s, h, gain, out, g.H, g.eps, trace);
 }
 
 // DFlash2 conv (memra_engine::dflash, Dflash2Conv; DflashDraft, d2_conv_prepare / d2_conv_finish):
@@ -273,8 +284,9 @@ void launch_final_norm(const float* h, const float* gain, float* out, int n_tok,
 // thread; prepare writes the operand planes (and clears the next
 // projections' red.add targets), finish adds into the residual stream.
 __global__ void __launch_bounds__(256) conv_kernel(ConvArgs a) {
-  pdl_wait();
+  trace_cta_entry(a.trace);
   pdl_launch_dependents();
+  pdl_wait();
   const Geo& g = a.g;
   const long stride = (long)gridDim.x * blockDim.x;
   const long t0 = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -307,23 +319,31 @@ __global__ void __launch_bounds__(256) conv_kernel(ConvArgs a) {
       *hp = make_float4(hv.x + o[0], hv.y + o[1], hv.z + o[2], hv.w + o[3]);
     }
   }
+  trace_cta_exit(a.trace);
+}
+
+int conv_grid(const ConvArgs& c, int n_sm) {
+  const long n = std::max<long>((long)c.n_tok * c.g.H / 4, std::max(c.zero0_n, c.zero1_n));
+  return (int)std::max<long>(1, std::min<long>((n + 255) / 256, 4L * n_sm));
 }
 
 void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s) {
-  const long n = std::max<long>((long)c.n_tok * c.g.H / 4, std::max(c.zero0_n, c.zero1_n));
-  const int grid = (int)std::max<long>(1, std::min<long>((n + 255) / 256, 4L * n_sm));
-  launch_pdl(conv_kernel, dim3(grid), dim3(256), 0, s, c);
+  launch_pdl(conv_kernel, dim3(conv_grid(c, n_sm)), dim3(256), 0, s, c);
 }
 
+int qk_finish_grid(const FinishArgs& f) { return (f.n_tok * (f.g.Hq + 2 * f.g.Hkv) + 3) / 4; }
+
 void launch_qk_finish(const FinishArgs& f, cudaStream_t s) {
-  const int rows = f.n_tok * (f.g.Hq + 2 * f.g.Hkv);
-  launch_pdl(qk_finish_kernel, dim3((rows + 3) / 4), dim3(128), 0, s, f);
+  launch_pdl(qk_finish_kernel, dim3(qk_finish_grid(f)), dim3(128), 0, s, f);
+}
+
+int swiglu_grid(const FinishArgs& f, int n_sm) {
+  const long n4 = (long)f.n_tok * f.g.I / 4;
+  return (int)std::min<long>((n4 + 127) / 128, 4L * n_sm);
 }
 
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s) {
-  const long n4 = (long)f.n_tok * f.g.I / 4;
-  const int grid = (int)std::min<long>((n4 + 127) / 128, 4L * n_sm);
-  launch_pdl(swiglu_kernel, dim3(grid), dim3(128), 0, s, f);
+  launch_pdl(swiglu_kernel, dim3(swiglu_grid(f, n_sm)), dim3(128), 0, s, f);
 }
 
 }  // namespace dfl

@@ -3,17 +3,24 @@
 // Swap-AB: a 128-row weight tile is the MMA's A operand (M = 128 output
 // features) and the token rows are its N side (16 per sequence), so the
 // weight dimension fills the tensor core while the few drafted rows ride
-// along.  Stream-K over units of 64 K-columns spreads every projection over
-// all SMs.  One CTA of six warps per SM (two fit):
+// along.  Stream-K over units of 64 K-columns spreads a projection over the
+// CTAs.  One CTA of nine warps per SM:
 //   warp 0 (one lane)  producer: weight blocks [128 x 64] (one contiguous
 //                      16 KB bulk copy each, stored pre-swizzled) and the
 //                      operand's hi/lo bf16 planes [N x 64] (TMA) into a ring
 //                      of stages (the first stages' weights before the
 //                      programmatic-launch wait, so they stream during the
 //                      previous kernel's tail);
-//   warp 1 (one lane)  MMA issuer: per unit, 4 K-steps x (hi, lo) tcgen05.mma
-//                      into a TMEM accumulator (two buffers);
-//   warps 2..5         drain: move finished accumulators out of TMEM and
+//   warps 1, 2 (one lane each)  MMA issuers: ring slot i goes to issuer
+//                      i % kIss, which runs its 4 K-steps x (hi, lo)
+//                      tcgen05.mma into its own TMEM accumulator (two
+//                      buffers).  At N = 32 one issuing thread moves a 16 KB
+//                      unit in ~290 ns on this GB300 and two overlap to
+//                      ~180 ns, which is also what more issuers reach: the
+//                      tensor-core path tops out near 90 GB/s per SM at 16
+//                      tokens, so a projection needs most SMs to stream HBM
+//                      at full rate;
+//   warps 3..6         drain: add the issuers' finished accumulators out of TMEM and
 //                      red.add them into a token-major destination, or (for
 //                      the ingest's projections) take the stream-K ticket and,
 //                      as the last arriver, run the fused tile epilogue.
@@ -36,7 +43,9 @@ struct TcCfg {
   uint32_t idesc;
 };
 
-constexpr int kTcThreads = 224;   // warps: 0 producer, 1 and 6 MMA issuers, 2..5 drain
+constexpr int kTcThreads = 224;   // warps: 0 producer, 1..2 MMA issuers, 3..6 drain
+constexpr int kDrainTid0 = 96;    // first drain thread (warp 3)
+constexpr int kMaxIss = 2;
 constexpr int kWTileBytes = kTileN * kTileK * 2;   // 16 KB
 constexpr int kXBox = 16;                           // operand rows per short TMA box
 constexpr int kXBoxTall = 128;                      // operand rows per tall TMA box
@@ -53,9 +62,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* ctl = smem + t.stages * t.stage_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ctl);
   uint64_t* empty = full + t.stages;
-  uint64_t* accfull = empty + t.stages;   // [issuer][buffer]
-  uint64_t* accempty = accfull + 4;       // [issuer][buffer]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 4);
+  uint64_t* accfull = empty + t.stages;          // [issuer][buffer]
+  uint64_t* accempty = accfull + 2 * kMaxIss;     // [issuer][buffer]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accempty + 2 * kMaxIss);
   volatile int* flags = reinterpret_cast<volatile int*>(tmem_slot + 4);   // abort, last
   float* red = reinterpret_cast<float*>(ctl + 512);
 
@@ -73,7 +82,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 4; ++b) {
+    for (int b = 0; b < 2 * kMaxIss; ++b) {
       mbar_init(&accfull[b], 1);
       mbar_init(&accempty[b], kEpiThreads);
     }
@@ -137,11 +146,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int i = 0; i < pre; ++i) load_x(smem + i * t.stage_bytes, &full[i]);
       int st = 0;
       uint32_t ph = 0;   // parity of the empty phase the next refill waits for
+      unsigned long long waited = 0;   // traced: cycles spent waiting for a free stage
       for (int i = pre; i < n_units; ++i) {
+        const unsigned long long w0 = a.trace ? trace_clock() : 0;
         if (!mbar_wait(&empty[st], ph, &flags[0])) {
           flags[0] = 1;
           break;
         }
+        if (a.trace) waited += trace_clock() - w0;
         uint8_t* sp = smem + st * t.stage_bytes;
         mbar_arrive_expect_tx(&full[st], bytes);
         bulk_load_hint(sp, wsrc + (size_t)i * kWTileBytes, kWTileBytes, &full[st], pol);
@@ -151,14 +163,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ph ^= 1;
         }
       }
+      trace_put(a.trace, blockIdx.x, 9, waited);            // 9: producer cycles waiting for free stages
     }
-  } else if (warp == 1 || warp == 6) {
+  } else if (warp >= 1 && warp <= kMaxIss) {
     // ---------------------------------------------------------------- MMA issuers
-    // One thread issuing tcgen05.mma at small N is bound by its own issue
-    // latency, so when four accumulators fit in TMEM (N = 2*nt <= 128) two
-    // issuers split every segment's units (even / odd ring slots), each into
-    // its own pair of TMEM accumulators; the drain adds the two.
-    const int j = warp == 1 ? 0 : 1;
+    // kIss issuers split every segment's units (ring slot i to issuer
+    // i % kIss), each into its own pair of TMEM accumulators; the drain adds
+    // them.
+    const int j = warp - 1;
     if (lane == 0 && j < kIss) {
       // descriptor start fields are address >> 4 (14 bits, shared memory
       // < 256 KB), so stage and K-step offsets add without carries
@@ -170,24 +182,29 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int seg = 0, st = j % t.stages;
       uint32_t ph = (uint32_t)(j / t.stages) & 1;
       bool ok = true;
+      unsigned long long wfull = 0, wacc = 0;   // traced: cycles waiting for stages / accumulators
       for (int u = u0; u < u1 && ok; ++seg) {
         const int T = u / p.kb;
         const int seg_end = min(u1, (T + 1) * p.kb);
         const int b = seg & 1, use = seg >> 1;
+        const unsigned long long w1 = a.trace ? trace_clock() : 0;
         if (!mbar_wait(&accempty[2 * j + b], (use & 1) ^ 1, &flags[0])) {
           flags[0] = 1;
           break;
         }
+        if (a.trace) wacc += trace_clock() - w1;
         tc_fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)((2 * j + b) * t.aw);
         // this issuer's units of the segment: ring slots i = u - u0 with i % kIss == j
         int k = 0;
         for (int uu = u + ((j - (u - u0)) % kIss + kIss) % kIss; uu < seg_end; uu += kIss, ++k) {
+          const unsigned long long w2 = a.trace ? trace_clock() : 0;
           if (!mbar_wait(&full[st], ph, &flags[0])) {
             flags[0] = 1;
             ok = false;
             break;
           }
+          if (a.trace) wfull += trace_clock() - w2;
           tc_fence_after();
           const uint64_t dw = d0 + (uint64_t)(st * dstage);
           // 4 K-steps of 16 (32 bytes = 2 descriptor units each)
@@ -210,11 +227,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         u = seg_end;
       }
       if (j == 0) trace_mark(a.trace, blockIdx.x, 3, c0);       // 3: last MMA issued
+      if (j == 0 && a.omode == O_RED) {                          // (O_TILE epilogues use 11..13)
+        trace_put(a.trace, blockIdx.x, 11, wfull);              // 11: issuer 0 cycles waiting for full stages
+        trace_put(a.trace, blockIdx.x, 12, wacc);               // 12: issuer 0 cycles waiting for a free accumulator
+      }
     }
   } else {
     // ------------------------------------------------------------------ drain
     pdl_wait();
-    const int et = threadIdx.x - 64;
+    const int et = threadIdx.x - kDrainTid0;
     const int q = warp & 3;                 // TMEM lane quarter this warp may read
     const int row = 32 * q + lane;          // tile row (output feature) of this thread
     // the thread's row of accumulator buffer b of issuer j, token columns
@@ -238,10 +259,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int b = seg & 1, use = seg >> 1;
       const bool last_seg = seg_end == u1;
       // units of each issuer in this segment (ring slots i = uu - u0, issuer i % kIss)
-      int nu[2] = {seg_end - u, 0};
-      if (kIss == 2) {
-        nu[0] = ((u - u0) & 1) == 0 ? (seg_end - u + 1) / 2 : (seg_end - u) / 2;
-        nu[1] = seg_end - u - nu[0];
+      int nu[kMaxIss];
+#pragma unroll
+      for (int jj = 0; jj < kMaxIss; ++jj) {
+        // slots i in [u - u0, seg_end - u0) with i % kIss == jj
+        const int first = u + ((jj - (u - u0)) % kIss + kIss) % kIss;
+        nu[jj] = jj < kIss && first < seg_end ? (seg_end - 1 - first) / kIss + 1 : 0;
       }
       // a failed wait skips the TMEM read but keeps every barrier arrival, so
       // no thread is left waiting at a named barrier
@@ -293,7 +316,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           __threadfence();
           tile_epilogue(a.e, T, acc_tile, t.nt, red, et, last_seg ? a.trace : nullptr, blockIdx.x, c0);
           if (et == 0) a.counters[T] = 0;
-          if (et == 0) trace_mark(a.trace, blockIdx.x, last_seg ? 10 : 14, c0);   // 10/14: tile epilogue done
+          if (et == 0) trace_mark(a.trace, blockIdx.x, last_seg ? 10 : 8, c0);   // 10/8: tile epilogue done
         }
       }
       u = seg_end;
@@ -303,7 +326,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncwarp();   // role lanes rejoin their warp before the CTA barrier
   __syncthreads();
   if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 5, c0);  // 5: all roles done
-  if (threadIdx.x == 64) trace_mark(a.trace, blockIdx.x, 7, c0);
+  if (threadIdx.x == kDrainTid0) trace_mark(a.trace, blockIdx.x, 7, c0);
+  if (threadIdx.x == 0) trace_exit(a.trace, blockIdx.x);
   if (flags[0] && threadIdx.x == 0) atomicExch(const_cast<int*>(err), DERR_TIMEOUT);
   if (warp == 1) {
     __syncwarp();
@@ -336,13 +360,19 @@ void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s) {
   // the two column halves)
   const bool fused = 2 * t.nt <= 256;
   t.aw = fused ? 2 * t.nt : t.nt;
-  // two issuers when their four accumulators fit in the 512 TMEM columns
+  // two issuers when both have two accumulator buffers in the 512 TMEM columns
   const int iss = fused && 4 * t.aw <= 512 ? 2 : 1;
+  // every stage belongs to one issuer (slot i goes to issuer i % iss and
+  // stage i % stages), so the stage count is a multiple of the issuers:
+  // otherwise a stage alternates between issuers, and one of them could wait
+  // for the stage's next phase while the current one is still open, which
+  // the phase parity cannot tell from the phase before it
+  t.stages -= t.stages % iss;
   t.tmem_cols = pow2_at_least(2 * iss * t.aw);   // [issuer][buffer] accumulators
   // nt <= 256 per pass keeps this within an SM's 512 columns (fused: aw <= 256
-  // and two issuers only at aw <= 128; unfused: aw = nt <= 256); a larger
+  // and more issuers only while they fit; unfused: aw = nt <= 256); a larger
   // request would fault tcgen05.alloc, so it is never launched
-  if (t.tmem_cols > 512) return;
+  if (t.tmem_cols > 512 || t.stages < iss) return;
   t.x_row_lo = a.e.g.Mt;
   t.idesc = idesc_bf16(kTileN, t.aw);
   const size_t smem = gemm_tc_smem_bytes(t.nt, t.stages);

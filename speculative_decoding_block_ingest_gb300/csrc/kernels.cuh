@@ -50,6 +50,7 @@ struct FinishArgs {
   void* kpool;
   void* vpool;
   float* u_out;           // prep_norm: also the normed rows in f32 [Mt][H] (DFlash2 conv input), or null
+  unsigned long long* trace;   // optional per-CTA entry / exit stamps, or null
   Geo g;
 };
 
@@ -70,6 +71,7 @@ struct ConvArgs {
   long zero0_n;
   float* zero1;
   long zero1_n;
+  unsigned long long* trace;   // optional per-CTA entry / exit stamps, or null
   Geo g;
 };
 
@@ -110,6 +112,7 @@ struct InitArgs {
   const double* inv_freq;   // RoPE inverse frequencies [d/2] (f64)
   float2* rope_cs;          // out: per row [d/2] (cos, sin) x mscale
   int is_round;             // positions come from blob.round.pos (else blob.ingest.row_pos)
+  unsigned long long* trace;   // optional per-CTA entry / exit stamps, or null
   Geo g;
 };
 
@@ -206,10 +209,18 @@ void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);
 void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s);
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s);
+// CTAs of the element-wise launches (trace regions are sized by them).
+int prep_norm_grid(const FinishArgs& f);
+int qk_finish_grid(const FinishArgs& f);
+int swiglu_grid(const FinishArgs& f, int n_sm);
+int conv_grid(const ConvArgs& c, int n_sm);
+int attn_combine_grid(const AttnArgs& a, int n_tok);
+int init_grid(const InitArgs& a);
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s);
 const void* init_kernel_entry();       // kernel function addresses, to find
 const void* final_norm_kernel_entry(); // their nodes in a captured graph
-void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g, cudaStream_t s);
+void launch_final_norm(const float* h, const float* gain, float* out, int n_tok, const Geo& g,
+                       unsigned long long* trace, cudaStream_t s);
 void launch_to_operand(const float* src, int n_rows, int width, void* op, long plane, cudaStream_t s);
 void launch_argmax(const float* logits, int n_rows, int V, int32_t* tokens, cudaStream_t s);
 void launch_kv_read(const Geo& g, const void* kpool, const void* vpool, const int* block_table,

@@ -220,8 +220,9 @@ __device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) 
 }
 
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) {
-  pdl_wait();
+  trace_cta_entry(a.trace);
   pdl_launch_dependents();
+  pdl_wait();
   __shared__ float red[kCombThreads / 32];
   __shared__ float4 part[kCombThreads];
   const Geo& g = a.g;
@@ -283,10 +284,13 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) 
     put_operand(a.op, idx + 2, a.op_plane, t.z * inv, a.op_f32);
     put_operand(a.op, idx + 3, a.op_plane, t.w * inv, a.op_f32);
   }
+  trace_cta_exit(a.trace);
 }
 
+int attn_combine_grid(const AttnArgs& a, int n_tok) { return n_tok * a.g.Hq; }
+
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s) {
-  launch_pdl(attn_combine_kernel, dim3(n_tok * a.g.Hq), dim3(kCombThreads), 0, s, a);
+  launch_pdl(attn_combine_kernel, dim3(attn_combine_grid(a, n_tok)), dim3(kCombThreads), 0, s, a);
 }
 
 // ------------------------------------------------------------------ per-call init
@@ -295,8 +299,9 @@ void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s) {
 // accumulators.  Row copies issue four float4 loads per thread before storing.
 constexpr int kInitThreads = 256;
 __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __grid_constant__ InitBlob b) {
-  pdl_wait();
+  trace_cta_entry(a.trace);
   pdl_launch_dependents();
+  pdl_wait();
   const int r = blockIdx.x, tid = threadIdx.x;
   if (r == a.n_rows) {
     const int* src = reinterpret_cast<const int*>(&b);
@@ -305,6 +310,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
       for (int i = tid; i < a.cp_len[q]; i += kInitThreads) dst[a.cp_off[q] + i] = src[a.cp_off[q] + i];
     for (int i = tid; i < b.n_pt; i += kInitThreads) a.block_table[b.pt_idx[i]] = b.pt_page[i];
     for (int i = tid; i < a.zero_n; i += kInitThreads) a.zero_ptr[i] = 0.f;
+    trace_cta_exit(a.trace);
     return;
   }
   // RoPE (cos, sin) of this row's position, mscale folded in
@@ -339,12 +345,15 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
       }
     }
   }
+  trace_cta_exit(a.trace);
 }
 
 const void* init_kernel_entry() { return reinterpret_cast<const void*>(init_kernel); }
 
+int init_grid(const InitArgs& a) { return a.n_rows + 1; }
+
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s) {
-  launch_pdl(init_kernel, dim3(a.n_rows + 1), dim3(kInitThreads), 0, s, a, blob);
+  launch_pdl(init_kernel, dim3(init_grid(a)), dim3(kInitThreads), 0, s, a, blob);
 }
 
 __global__ void kv_read_kernel(Geo g, const void* kpool, const void* vpool, const int* block_table,

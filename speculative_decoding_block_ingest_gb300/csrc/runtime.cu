@@ -389,6 +389,7 @@ struct dflash_handle {
     int64_t offset;
   };
   std::vector<TraceRec> trace_recs;
+  std::vector<cudaGraphExec_t> traced_execs;   // traced rounds' graphs, kept until tracing stops
   template <class T>
   T* at(size_t off) { return reinterpret_cast<T*>(ws + off); }
 };
@@ -465,6 +466,16 @@ void rollback_pages(dflash_t* h, const InitBlob& blob, const std::vector<int>& t
   (void)blob;
 }
 
+// CTAs of a tensor-core projection pass.  At 16 tokens the tensor-core path
+// of one SM moves about 90 GB/s of weights (the MMA issue rate, not memory,
+// bounds it), so a projection takes every SM to stream HBM at full rate.
+#ifndef DFLASH_GEMM_GRID
+#define DFLASH_GEMM_GRID 152
+#endif
+int proj_grid(const dflash_t* h, int n_tok) {
+  return n_tok <= 64 ? std::min(h->n_sm, DFLASH_GEMM_GRID) : h->n_sm;
+}
+
 EpiArgs base_epi(dflash_t* h) {
   EpiArgs e{};
   e.g = h->g;
@@ -511,7 +522,7 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     a.n_tiles = sp.N / kTileN;
     a.p.kb = sp.K / kTileK;
     a.p.units = a.n_tiles * a.p.kb;
-    a.p.grid = std::min(a.p.units, h->use_tc ? h->n_sm : h->lo.grid_max);
+    a.p.grid = std::min(a.p.units, h->use_tc ? proj_grid(h, std::min(kPassTok, n_all - base)) : h->lo.grid_max);
     a.acc = h->at<float>(h->lo.gacc);
     a.counters = h->at<int>(h->lo.counters) + (size_t)sp.site * h->lo.max_tiles;
     a.e = sp.e;
@@ -567,6 +578,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   ia.g = g;
   {
     Launch L(h, DFLASH_KERNEL_INIT, (double)n_rows * width * 8, s);
+    ia.trace = trace_slot(h, DFLASH_KERNEL_INIT, init_grid(ia));
     launch_init(ia, blob, s);
   }
   ck(cudaGetLastError(), "ingest init launch");
@@ -637,7 +649,11 @@ int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int*
   // take the split that minimises waves x (pages per item + a fixed per-item
   // cost of about two chunks); among equals the larger split (fewer partials
   // to merge).
-  const long slots = h->attn_tc ? (long)h->n_sm : 2L * h->n_sm;
+  // (beside a small round's projection, which holds proj_grid SMs, so that
+  // the two kernels can be resident together)
+  const int n_tok = (int)lens.size() * kBlock;
+  const long beside = (long)h->n_sm - proj_grid(h, n_tok);
+  const long slots = h->attn_tc ? (n_tok <= 64 && beside >= 32 ? beside : (long)h->n_sm) : 2L * h->n_sm;
   constexpr long kItemCost = 4;
   long best = 1, best_cost = -1;
   for (long sp = 1; sp <= longest; ++sp) {
@@ -782,6 +798,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   InitArgs ia = round_init_args(h, n_tok, noise);
   {
     Launch L(h, DFLASH_KERNEL_INIT, (double)n_tok * g.H * 8, s);
+    ia.trace = trace_slot(h, DFLASH_KERNEL_INIT, init_grid(ia));
     launch_init(ia, blob, s);
   }
   ck(cudaGetLastError(), "round init launch");
@@ -813,6 +830,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     f.op_plane = (long)Mt * g.H;
     f.u_out = cu;
     Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * (Gc ? 12 : 8), s);
+    f.trace = trace_slot(h, DFLASH_KERNEL_FINISH, prep_norm_grid(f));
     launch_prep_norm(f, s);
   };
   // prepare: the dynamic coefficients of sublayer `sub` (both halves) from
@@ -852,6 +870,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     c.zero1_n = (long)n_tok * conv_n;
     c.g = g;
     Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * 20, s);
+    c.trace = trace_slot(h, DFLASH_KERNEL_FINISH, conv_grid(c, h->n_sm));
     launch_conv(c, h->n_sm, s);
     ck(cudaGetLastError(), "conv prepare launch");
   };
@@ -868,6 +887,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     c.h = hres;
     c.g = g;
     Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.H * 16, s);
+    c.trace = trace_slot(h, DFLASH_KERNEL_FINISH, conv_grid(c, h->n_sm));
     launch_conv(c, h->n_sm, s);
     ck(cudaGetLastError(), "conv finish launch");
   };
@@ -899,6 +919,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
       f.qn = h->at<float>(h->lo.qn) + (size_t)l * g.d;
       f.kn = h->at<float>(h->lo.kn) + (size_t)l * g.d;
       Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.qkv_n * 6, s);
+      f.trace = trace_slot(h, DFLASH_KERNEL_FINISH, qk_finish_grid(f));
       launch_qk_finish(f, s);
     }
     ck(cudaGetLastError(), "qk finish launch");
@@ -935,6 +956,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     ck(cudaGetLastError(), "attention launch");
     {
       Launch L(h, DFLASH_KERNEL_COMBINE, part_b + (double)n_tok * g.Hq * g.d * 4, s);
+      a.trace = trace_slot(h, DFLASH_KERNEL_COMBINE, attn_combine_grid(a, n_tok));
       launch_attn_combine(a, n_tok, s);
     }
     ck(cudaGetLastError(), "attention combine launch");
@@ -980,6 +1002,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
       f.op = h->at<void>(h->lo.op_a);
       f.op_plane = (long)Mt * g.I;
       Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.I * 16, s);
+      f.trace = trace_slot(h, DFLASH_KERNEL_FINISH, swiglu_grid(f, h->n_sm));
       launch_swiglu(f, h->n_sm, s);
     }
     ck(cudaGetLastError(), "swiglu launch");
@@ -1002,7 +1025,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   }
   {
     Launch L(h, DFLASH_KERNEL_NORM, (double)n_tok * g.H * 8, s);
-    launch_final_norm(hres, h->at<float>(h->lo.fn), out, n_tok, g, s);
+    launch_final_norm(hres, h->at<float>(h->lo.fn), out, n_tok, g, trace_slot(h, DFLASH_KERNEL_NORM, n_tok), s);
   }
   ck(cudaGetLastError(), "final norm launch");
 }
@@ -1119,16 +1142,39 @@ int ingest_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* t_
 // the host about as long as the GPU takes to run them, so they are captured
 // once per (sequences, attention items, KV region) and replayed; a replay
 // changes only the init node (descriptor blob, noise rows) and the final-norm
-// node (output rows).  Off while profiling or tracing, for the persistent
-// kernel, when the caller's stream is itself being captured, and with
-// DFLASH_GRAPHS=0 at create.
+// node (output rows).  Off while profiling, for the persistent kernel, when
+// the caller's stream is itself being captured, and with DFLASH_GRAPHS=0 at
+// create; while tracing, each round is captured afresh with its own trace
+// regions.
 void enqueue_round_graph(dflash_t* h, InitBlob& blob, const float* noise, float* out, cudaStream_t s) {
   const RoundDesc& rd = blob.round;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   ck(cudaStreamIsCapturing(s, &cap), "stream capture query");
   const bool mk = mk_eligible(h, rd.n_tok) && rd.n_items <= h->n_sm;
-  if (h->graphs_off || h->prof_on || h->trace_buf || mk || cap != cudaStreamCaptureStatusNone) {
+  if (h->graphs_off || h->prof_on || mk || cap != cudaStreamCaptureStatusNone) {
     enqueue_round(h, blob, noise, out, s);
+    return;
+  }
+  if (h->trace_buf) {
+    // a traced round runs the same graph as an untraced one, captured afresh
+    // with this round's trace regions and discarded after its launch
+    if (!h->cap_stream) ck(cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking), "capture stream");
+    ck(cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeRelaxed), "traced round capture begin");
+    cudaGraph_t tg = nullptr;
+    try {
+      enqueue_round(h, blob, noise, out, h->cap_stream);
+    } catch (...) {
+      cudaStreamEndCapture(h->cap_stream, &tg);
+      if (tg) cudaGraphDestroy(tg);
+      throw;
+    }
+    ck(cudaStreamEndCapture(h->cap_stream, &tg), "traced round capture end");
+    cudaGraphExec_t te = nullptr;
+    cudaError_t ie = cudaGraphInstantiate(&te, tg, 0);
+    cudaGraphDestroy(tg);
+    ck(ie, "traced round instantiate");
+    h->traced_execs.push_back(te);   // released when tracing stops (after a device sync)
+    ck(cudaGraphLaunch(te, s), "traced round launch");
     return;
   }
   const void* region = h->kv;
@@ -1145,8 +1191,9 @@ void enqueue_round_graph(dflash_t* h, InitBlob& blob, const float* noise, float*
     const float* fn = h->at<float>(h->lo.fn);
     int H = h->g.H;
     float eps = h->g.eps;
+    unsigned long long* no_trace = nullptr;
     cudaKernelNodeParams q = gr->norm_p;
-    void* np[5] = {&hres, &fn, &out, &H, &eps};
+    void* np[6] = {&hres, &fn, &out, &H, &eps, &no_trace};
     q.kernelParams = np;
     ck(cudaGraphExecKernelNodeSetParams(gr->exec, gr->norm_node, &q), "round graph output update");
     ck(cudaGraphLaunch(gr->exec, s), "round graph launch");
@@ -1834,6 +1881,11 @@ int dflash_trace_begin(dflash_t* h, void* device_buffer, size_t bytes) {
   if (!h) return fail(DFLASH_ERR_INVALID_ARG, "handle is null");
   if (device_buffer && reinterpret_cast<uintptr_t>(device_buffer) % 8)
     return fail(DFLASH_ERR_INVALID_ARG, "trace buffer must be 8-byte aligned");
+  if (!h->traced_execs.empty()) {
+    cudaDeviceSynchronize();
+    for (auto e : h->traced_execs) cudaGraphExecDestroy(e);
+    h->traced_execs.clear();
+  }
   h->trace_buf = static_cast<unsigned long long*>(device_buffer);
   h->trace_cap = device_buffer ? bytes / 8 : 0;
   h->trace_used = 0;
@@ -1873,6 +1925,8 @@ void dflash_destroy(dflash_t* h) {
     cudaGraphExecDestroy(gr.exec);
     cudaGraphDestroy(gr.graph);
   }
+  if (!h->traced_execs.empty()) cudaDeviceSynchronize();
+  for (auto e : h->traced_execs) cudaGraphExecDestroy(e);
   if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
   delete h;
 }
