@@ -309,10 +309,11 @@ class Drafter:
         ``conv_finish`` before the residual add.
 
         ``kv_fp8``: an FP8 KV cache (the FP8 block attention kernel named in
-        spark_model::layers::dflash_head): the block rows' K and V pass
-        through the cache format like context rows (:func:`fp8_rows`), and so
-        do the queries, whose scores are taken in e4m3; the given ctx K/V are
-        already in that format.
+        spark_model::layers::dflash_head): a storage format of the cache.
+        The block rows' K and V pass through it like context rows
+        (:func:`fp8_rows`: the block K/V sit in the cache pages during the
+        round); the given ctx K/V are already in it.  The queries are not
+        stored and stay exact.
         """
         cfg = self.cfg
         b = noise.shape[0]
@@ -340,7 +341,7 @@ class Drafter:
             q = rope_neox(rms_norm(q, L["q_norm"], cfg.rms_eps), pos_block, self.inv_freq, self.mscale)
             k = rope_neox(rms_norm(k, L["k_norm"], cfg.rms_eps), pos_block, self.inv_freq, self.mscale)
             if kv_fp8:
-                q, k, v = fp8_rows(q), fp8_rows(k), fp8_rows(v)
+                k, v = fp8_rows(k), fp8_rows(v)
             keys = np.concatenate([ctx_k[li], k], axis=0)
             vals = np.concatenate([ctx_v[li], v], axis=0)
             o = self.attention(q, keys, vals)
@@ -364,7 +365,7 @@ class Drafter:
 
         ``pos`` holds the ctx rows' positions then the block rows'
         (DflashDraft page, first-light contract under ``ctx_features``).
-        ``kv_fp8``: K/V (and queries) in the FP8 cache format.
+        ``kv_fp8``: K/V in the FP8 cache format (queries exact).
         """
         pos = list(pos)
         ctx = taps.shape[0]

@@ -206,8 +206,7 @@ __device__ __forceinline__ long pool_layer_elems(const Geo& g) {
 
 // FP8 cache: each pool holds its e4m3 codes ([L][page][Hkv][64][d] for K,
 // [L][page][Hkv][d][64] for V^T, one byte each) followed by its scales
-// [L][page][Hkv][64] f32; the query buffer holds codes [Mt][Hq][d] followed
-// by scales [Mt][Hq].
+// [L][page][Hkv][64] f32.
 __host__ __device__ __forceinline__ long fp8_pool_codes(const Geo& g) {
   return (long)g.L * g.max_pages * g.Hkv * kPage * g.d;
 }
@@ -220,7 +219,6 @@ __host__ __device__ __forceinline__ float* fp8_pool_scales(const Geo& g, void* p
 __host__ __device__ __forceinline__ const float* fp8_pool_scales(const Geo& g, const void* pool) {
   return reinterpret_cast<const float*>(static_cast<const char*>(pool) + fp8_pool_codes(g));
 }
-__host__ __device__ __forceinline__ long fp8_q_codes(const Geo& g) { return (long)g.Mt * g.Hq * g.d; }
 
 // e4m3 scale of one head row from its absolute maximum: the largest value
 // maps to the largest finite code (448); an all-zero row takes scale 1.
@@ -241,11 +239,12 @@ __device__ __forceinline__ long v_index(const Geo& g, int layer, int page, int h
   return layer * pool_layer_elems(g) + (((long)page * g.Hkv + head) * g.d + dim) * kPage + off;
 }
 
-// Store one head row (PER dims per lane of a warp, lane l holds dims
-// l*PER ..) of q (kind 0), K (1) or V (2) in e4m3 with its scale.
+// Store one K (kind 1) or V (kind 2) head row of the cache in e4m3 with its
+// scale (PER dims per lane of a warp, lane l holds dims l*PER ..).
 template <int PER>
 __device__ __forceinline__ void put_row_fp8(const Geo& g, const float* x, int lane, int kind, int layer, int tok,
-                                            int head, int dst, void* q, void* kpool, void* vpool) {
+                                            int head, int dst, void* kpool, void* vpool) {
+  (void)tok;
   float am = 0.f;
 #pragma unroll
   for (int i = 0; i < PER; ++i) am = fmaxf(am, fabsf(x[i]));
@@ -257,15 +256,7 @@ __device__ __forceinline__ void put_row_fp8(const Geo& g, const float* x, int la
     c[i] = (uint8_t)(w & 0xFF);
     c[i + 1] = (uint8_t)(w >> 8);
   }
-  constexpr int d = 32 * PER;
   const int dim0 = lane * PER;
-  if (kind == 0) {
-    uint8_t* row = static_cast<uint8_t*>(q) + ((long)tok * g.Hq + head) * d + dim0;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) row[i] = c[i];
-    if (lane == 0) reinterpret_cast<float*>(static_cast<char*>(q) + fp8_q_codes(g))[(long)tok * g.Hq + head] = sc;
-    return;
-  }
   const int page = dst >> 6, off = dst & (kPage - 1);
   if (kind == 1) {
     uint8_t* row = static_cast<uint8_t*>(kpool) + k_index(g, layer, page, head, off, dim0);
@@ -382,7 +373,7 @@ static __device__ void epi_heads_t(const EpiArgs& e, int tile, const float* red,
       }
     }
     if (g.kvtype == KV_FP8) {
-      put_row_fp8<PER>(g, x, lane, kind, layer, tok, head, dst, nullptr, e.kpool, e.vpool);
+      put_row_fp8<PER>(g, x, lane, kind, layer, tok, head, dst, e.kpool, e.vpool);
     } else {
       const int page = dst >> 6, off = dst & (kPage - 1);
 #pragma unroll

@@ -16,6 +16,8 @@
 #include <algorithm>
 #include <cmath>
 
+#include <cuda_fp16.h>
+
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -146,8 +148,13 @@ __device__ void qk_finish_row(const FinishArgs& f, int tok, int hh) {
       x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
     }
   }
-  if (g.kvtype == KV_FP8) {
-    put_row_fp8<PER>(g, x, lane, kind, f.layer, tok, head, dst, f.q_out, f.kpool, f.vpool);
+  if (g.kvtype == KV_FP8 && kind == 0) {
+    // an e4m3 cache stores K and V only: its queries stay f16
+    __half* qrow = static_cast<__half*>(f.q_out) + ((long)tok * g.Hq + head) * d + dim0;
+#pragma unroll
+    for (int q = 0; q < PER; ++q) qrow[q] = __float2half_rn(x[q]);
+  } else if (g.kvtype == KV_FP8) {
+    put_row_fp8<PER>(g, x, lane, kind, f.layer, tok, head, dst, f.kpool, f.vpool);
   } else if (kind == 0) {
     const long base = ((long)tok * g.Hq + head) * d + dim0;
 #pragma unroll

@@ -300,21 +300,6 @@ CUtensorMap make_map_u8(const void* base, uint64_t rows, uint64_t cols, uint32_t
   return m;
 }
 
-// 3-D byte map over [d2][d1][d0], box {d0, b1, b2} in the 128-byte swizzle
-// (d0 = 128: one swizzle row per (d2, d1) index).
-CUtensorMap make_map_u8_3d(const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, uint32_t b2) {
-  CUtensorMap m;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {d0, d0 * d1};
-  cuuint32_t box[3] = {(cuuint32_t)d0, b1, b2};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = tensor_map_encoder()(&m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
-                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) throw CudaError{"cuTensorMapEncodeTiled (u8 3-D) failed (" + std::to_string((int)r) + ")"};
-  return m;
-}
-
 }  // namespace
 
 struct dflash_handle {
@@ -1548,11 +1533,12 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     }
     if (h->attn_tc) {
       const uint64_t pool_rows = (uint64_t)L * cfg->max_pages * Hkv;
+      // queries: bf16 beside a bf16 cache, f16 beside an e4m3 one (2-byte
+      // elements either way; the copy does not convert)
+      h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
       if (h->attn_fp8) {
-        h->qmap = make_map_u8_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
         kv_maps_fp8(h->pool, h->ws + lo.kpool, h->ws + lo.vpool, pool_rows, d);
       } else {
-        h->qmap = make_map_bf16_3d(h->ws + lo.q, d, Hq, lo.Mt, Hq / Hkv, kBlock);
         h->pool.kmap = make_map_bf16(h->ws + lo.kpool, pool_rows * kPage, d, kPage);
         h->pool.vmap = make_map_bf16(h->ws + lo.vpool, pool_rows * d, kPage, d);
       }

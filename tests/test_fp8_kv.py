@@ -1,5 +1,6 @@
 """GPU parity of the e4m3 (FP8) KV cache against the oracle in the same cache
-format (``kv_fp8``: K/V rows and queries through per-row e4m3 scales).
+format (``kv_fp8``: the cached and block K/V rows stored as e4m3 codes with
+per-row scales; the queries exact).
 
 Bars: max|d|/rms(oracle) <= 2e-2 and greedy argmax agreement >= 99% against
 the FP8-format oracle; read-back rows equal the oracle's quantised rows

@@ -63,8 +63,10 @@ def _rope_complex(x, pos, inv_freq, mscale):
     return mscale * torch.cat([z.real, z.imag], dim=-1)
 
 
-def torch_forward(cfg, W, taps, noise, pos, inv_freq, mscale):
-    """The drafter forward expressed with torch.nn.functional routines."""
+def torch_forward(cfg, W, taps, noise, pos, inv_freq, mscale, kv_store=None, q_store=None):
+    """The drafter forward expressed with torch.nn.functional routines.
+    ``kv_store``: a function the cached and block K/V rows pass through (the
+    cache's storage format), or None; ``q_store`` likewise for the queries."""
     H, d, eps = cfg.hidden, cfg.head_dim, cfg.rms_eps
     G = cfg.n_heads // cfg.n_kv_heads
     taps = torch.as_tensor(taps, dtype=torch.float64)
@@ -83,6 +85,10 @@ def torch_forward(cfg, W, taps, noise, pos, inv_freq, mscale):
         kb = _rope_complex(F.rms_norm(F.linear(x, w["k"]).view(b, -1, d), (d,), w["k_norm"], eps),
                            pos[ctx:], inv_freq, mscale)
         vb = F.linear(x, w["v"]).view(b, -1, d)
+        if kv_store is not None:
+            kc, vc, kb, vb = kv_store(kc), kv_store(vc), kv_store(kb), kv_store(vb)
+        if q_store is not None:
+            q = q_store(q)
         K = torch.cat([kc, kb]).repeat_interleave(G, dim=1)
         V = torch.cat([vc, vb]).repeat_interleave(G, dim=1)
         o = F.scaled_dot_product_attention(q.transpose(0, 1)[None], K.transpose(0, 1)[None],
@@ -629,9 +635,38 @@ def test_fp8_cache_round_equals_first_light_in_the_cache_format():
         assert np.array_equal(one.k[0][li], kv.k[0][li]) and np.array_equal(one.v[0][li], kv.v[0][li])
 
 
+def _torch_e4m3_rows(x):
+    """Per-row e4m3 storage through torch's float8_e4m3fn cast: scale
+    amax/448 in float32 (1 for a zero row), codes of x/scale (clamped to the
+    finite range), decoded times the scale."""
+    x32 = x.to(torch.float32)
+    amax = x32.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax))
+    codes = (x32 / scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return codes.to(torch.float64) * scale.to(torch.float64)
+
+
+def test_fp8_cache_is_a_storage_format_of_k_and_v_only():
+    """The FP8-cache forward equals the torch.nn.functional restatement in
+    which the cached and block K/V rows, and nothing else, go through
+    torch's e4m3 cast with per-row scales: the queries stay exact."""
+    cfg = MICRO_KV8
+    D, W = _drafter(cfg)
+    taps, noise, pos = _inputs(cfg, 29)
+    got = D.forward_full(taps, noise, pos, kv_fp8=True)
+    ref = torch_forward(cfg, W, taps, noise, pos, D.inv_freq, D.mscale, kv_store=_torch_e4m3_rows)
+    assert rel_err(got, ref) < 1e-12
+    # the pin tells the reading apart: quantising the queries too, or not
+    # quantising at all, are different functions
+    q8 = torch_forward(cfg, W, taps, noise, pos, D.inv_freq, D.mscale, kv_store=_torch_e4m3_rows,
+                       q_store=_torch_e4m3_rows)
+    assert rel_err(got, q8) > 1e-6
+    assert rel_err(got, torch_forward(cfg, W, taps, noise, pos, D.inv_freq, D.mscale)) > 1e-6
+
+
 def test_fp8_cache_stores_quantised_rows_and_moves_the_output_a_little():
     """The cached rows are the plain K/V through fp8_rows, and the forward in
-    the cache format stays near the plain forward (each K/V/q element moves
+    the cache format stays near the plain forward (each K/V element moves
     by at most 2^-4 of itself) but is not equal to it."""
     cfg = MICRO_KV8
     D = O.Drafter(cfg, oracle_weights(synth.make_weights(cfg)))
