@@ -54,6 +54,25 @@ struct FinishArgs {
   Geo g;
 };
 
+// A projection whose CTAs own whole 128-row tiles over the full K
+// (proj_fused.cu): operand RMSNorm(h) x gain built in the kernel, the
+// element-wise step after the projection in its epilogue.
+enum OwnEpi { OWN_SWIGLU = 0 };
+struct OwnArgs {
+  const uint8_t* W;       // 16 KB weight blocks [tile][kb]
+  int n_tiles, kb;        // tiles (one CTA each), 64-column units per tile
+  int n_tok;
+  const float* gain;      // RMSNorm gain [K]
+  const float* wscale;    // per weight row scale (fp8), or null
+  int epi;                // OwnEpi
+  void* out;              // OWN_SWIGLU: the down projection's hi/lo bf16 operand planes
+  int out_ld;
+  long out_plane;
+  unsigned long long* trace;
+  int* err;
+  Geo g;
+};
+
 // DFlash2 grouped dynamic causal conv of one sublayer over the block rows
 // (16 per sequence, token t = 16 s + i; row i = 0 has no predecessor).
 struct ConvArgs {
@@ -136,6 +155,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 void launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
+// tmap_h: the residual stream h [Mt][H] f32 with boxes of [nt rows][64 cols]
+// (nt = the call's tokens rounded up to 16; 16 or 32).
+cudaError_t launch_proj_own(const OwnArgs& a, const void* tmap_h, cudaStream_t s);
 // Tensor-core projection: a.W is the weight in 16 KB blocks (see weights.cu).
 void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s);
 void launch_repack(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base, cudaStream_t s);
@@ -205,6 +227,7 @@ void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const 
 void launch_attention_tc8(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
                           cudaStream_t s);
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s);
+void launch_relay(unsigned long long* trace, cudaStream_t s);
 void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);
 void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s);

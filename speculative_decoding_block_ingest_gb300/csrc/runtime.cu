@@ -271,6 +271,20 @@ CUtensorMap make_map_bf16(const void* base, uint64_t rows, uint64_t cols, uint32
   return m;
 }
 
+// 2-D f32 map over a row-major [rows][cols] matrix, box [box_rows][64], no swizzle.
+CUtensorMap make_map_f32(const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  CUtensorMap m;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = tensor_map_encoder()(&m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+                                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) throw CudaError{"cuTensorMapEncodeTiled (f32) failed (" + std::to_string((int)r) + ")"};
+  return m;
+}
+
 // 3-D bf16 map over [d2][d1][d0] (d0 innermost), box {64, b1, b2}, 128-byte swizzle.
 CUtensorMap make_map_bf16_3d(const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b1, uint32_t b2) {
   CUtensorMap m;
@@ -333,6 +347,7 @@ struct dflash_handle {
   // tensor maps of the tensor-core projections' operands (per buffer)
   // operand maps: [0] boxes of 16 rows, [1] boxes of 128 rows (passes of >= 128 tokens)
   CUtensorMap xmap_taps[2], xmap_h[2], xmap_o[2], xmap_a[2];
+  CUtensorMap hmap[2];                          // residual stream h (f32), boxes of 16 / 32 rows x 64 columns
   CUtensorMap qmap;                             // attention: q buffer (3-D)
   bool use_tc = false;    // tensor-core projections (bf16 weights)
   bool attn_tc = false;   // tensor-core attention (bf16 KV, any weights)
@@ -484,6 +499,7 @@ struct GemmSpec {
   int omode = O_TILE;
   float* dst = nullptr;         // O_RED destination [tok][dst_ld]
   int dst_ld = 0;
+  int grid = 0;                 // CTAs of a tensor-core pass (0: proj_grid)
   EpiArgs e;
 };
 
@@ -507,7 +523,8 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     a.n_tiles = sp.N / kTileN;
     a.p.kb = sp.K / kTileK;
     a.p.units = a.n_tiles * a.p.kb;
-    a.p.grid = std::min(a.p.units, h->use_tc ? proj_grid(h, std::min(kPassTok, n_all - base)) : h->lo.grid_max);
+    a.p.grid = std::min(a.p.units, !h->use_tc ? h->lo.grid_max
+                                              : sp.grid > 0 ? sp.grid : proj_grid(h, std::min(kPassTok, n_all - base)));
     a.acc = h->at<float>(h->lo.gacc);
     a.counters = h->at<int>(h->lo.counters) + (size_t)sp.site * h->lo.max_tiles;
     a.e = sp.e;
@@ -808,6 +825,10 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   float* cu = Gc ? h->at<float>(h->lo.cu) : nullptr;
   float* cy = Gc ? h->at<float>(h->lo.cy) : nullptr;
   float* dyn_sub[2] = {h->at<float>(h->lo.cdyn_a), h->at<float>(h->lo.cdyn_m)};
+  // the MLP's norm, gate/up and SwiGLU as one tile-owning projection: tensor
+  // cores, no DFlash2 conv around the sublayer, up to 32 block rows, a tile
+  // per SM
+  const bool fused_mlp = h->use_tc && !Gc && n_tok <= 32 && 2 * g.I / kTileN <= h->n_sm;
   auto prep_norm = [&](const float* gain) {
     FinishArgs f = fb;
     f.gain = gain;
@@ -962,6 +983,27 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     run_gemm(h, o, s);
     if (Gc) conv_finish(l, 0);
 
+    if (fused_mlp) {
+      // post-attention RMSNorm, gate/up and SwiGLU in one tile-owning launch
+      OwnArgs oa{};
+      oa.W = h->at<uint8_t>(h->lo.gu) + (size_t)l * 2 * g.I * g.H * ew;
+      oa.n_tiles = 2 * g.I / kTileN;
+      oa.kb = g.H / kTileK;
+      oa.n_tok = n_tok;
+      oa.gain = h->at<float>(h->lo.post_ln) + (size_t)l * g.H;
+      oa.wscale = fp8 ? h->at<float>(h->lo.s_gu) + (size_t)l * 2 * g.I : nullptr;
+      oa.epi = OWN_SWIGLU;
+      oa.out = h->at<void>(h->lo.op_a);
+      oa.out_ld = g.I;
+      oa.out_plane = (long)Mt * g.I;
+      oa.err = h->at<int>(h->lo.err);
+      oa.g = g;
+      const double bytes = (double)2 * g.I * g.H * ew + (fp8 ? 2.0 * g.I * 4 : 0.0) +
+                           (double)oa.n_tiles * n_tok * g.H * 4 + (double)n_tok * g.I * 4;
+      Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
+      oa.trace = trace_slot(h, DFLASH_KERNEL_GEMM, oa.n_tiles);
+      ck(launch_proj_own(oa, &h->hmap[n_tok > 16 ? 1 : 0], s), "fused gate/up launch");
+    } else {
     prep_norm(h->at<float>(h->lo.post_ln) + (size_t)l * g.H);
     ck(cudaGetLastError(), "post norm launch");
     if (Gc) conv_prepare(l, 1);
@@ -991,6 +1033,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
       launch_swiglu(f, h->n_sm, s);
     }
     ck(cudaGetLastError(), "swiglu launch");
+    }
 
     GemmSpec dn;
     dn.site = 5 + 4 * l;
@@ -1530,6 +1573,7 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
         h->xmap_o[b] = make_map_bf16(h->ws + lo.op_o, Mt2, (uint64_t)Hq * d, box);
         h->xmap_a[b] = make_map_bf16(h->ws + lo.op_a, Mt2, I, box);
       }
+      for (int b = 0; b < 2; ++b) h->hmap[b] = make_map_f32(h->ws + lo.h, (uint64_t)lo.Mt, H, b ? 32u : 16u);
     }
     if (h->attn_tc) {
       const uint64_t pool_rows = (uint64_t)L * cfg->max_pages * Hkv;
