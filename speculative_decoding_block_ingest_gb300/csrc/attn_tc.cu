@@ -151,9 +151,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       bool ok = true;
       int deferred[2 * kMaxAttnStages];
       int nd = 0;
-      // the first chunk stages are free: announce them and fetch their
-      // context-only pages before the launch wait
-      const int pre = min(n_chunks, t.stages);
+      // the first chunk stage is free: announce it and fetch its
+      // context-only pages before the launch wait (one stage only: the
+      // query tile, loaded after the wait, queues behind what is in flight)
+      const int pre = min(n_chunks, 1);
       for (int c = 0; c < pre; ++c) {
         mbar_arrive_expect_tx(&kvfull[c], chunk_bytes(c));
         for (int w = 0; w < pages_in(c); ++w) {
