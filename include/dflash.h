@@ -29,10 +29,6 @@
  *    boundary (rows are moved as float4); a misaligned one is rejected with
  *    DFLASH_ERR_INVALID_ARG.  So do bf16 weight matrices (re-blocked at
  *    dflash_create with 16-byte moves).
- *  - DFLASH_ROUND_PATH=persistent in the environment at dflash_create runs
- *    each bf16 round of up to 4 sequences as one persistent kernel (device
- *    counters between its steps); by default every step is its own kernel.
- *    Both give the same results within the parity tolerances.
  *  - The library never allocates device memory: the caller allocates the
  *    workspace (dflash_workspace_bytes) and owns every buffer.
  *  - Every call validates all of its arguments before it launches anything.
@@ -291,9 +287,7 @@ enum dflash_kernel_kind {
   DFLASH_KERNEL_NORM = 4,       /* final RMSNorm                                                  */
   DFLASH_KERNEL_FINISH = 5,     /* element-wise steps between projections (norm operands, q/k
                                    head-norm + RoPE and block K/V rows, SwiGLU)                   */
-  DFLASH_KERNEL_ROUND = 6,      /* persistent round: every layer of forward_round in one kernel
-                                   (bf16 weights, up to 4 sequences)                              */
-  DFLASH_KERNEL_KINDS = 7
+  DFLASH_KERNEL_KINDS = 6
 };
 
 /* Measurement (not needed to draft).  While enabled, every kernel launch

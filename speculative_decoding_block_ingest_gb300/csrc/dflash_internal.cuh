@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace dfl {
@@ -36,6 +37,10 @@ constexpr int kMaxPtUpdates = 160;
 constexpr int kEpiThreads = 128;  // threads running a tile epilogue
 constexpr int kEpiTokChunk = 32;  // tokens per epilogue pass
 constexpr int kEpiBar = 1;        // named barrier id used by the epilogue
+// e4m3 weights reach the tensor cores as f16 values scaled by 2^-8 (the
+// projection widens the codes with integer operations); the row scales,
+// multiplied by this, undo it exactly.
+constexpr float kW8Unscale = 256.f;
 constexpr int kRedFloats = kEpiTokChunk * (kTileN + 1) + kEpiTokChunk;   // epilogue shared scratch
 
 enum WType { W_F32 = 0, W_BF16 = 1, W_FP8 = 2 };
@@ -139,14 +144,14 @@ struct EpiArgs {
   int kind;                   // EpiKind
   int n_tok;                  // token columns of this pass
   int tok_base;               // first token of this pass
-  const float* wscale;        // per weight row scale (fp8), or null
+  const float* wscale;        // per weight row scale of e4m3 weights (times kW8Unscale), or null
   const float* ss_in;         // KV: per token sum of squares -> rsqrt(ss/H+eps) scale; null = 1
   float* ss_out;              // FC: per token sum of squares of the features
   const float* gain;          // FC: hidden_norm gain
   void* op;                   // FC: operand written for the K/V projection (hi/lo bf16 planes or f32)
   int op_ld;
   long op_plane;              // elements between hi and lo planes
-  int op_f32;
+  int op_kind;                 // operand kind (OpKind)
   const float* kn;            // KV: k head-norm gains [L][d]
   void* kpool;                // K pool base (all layers)
   void* vpool;                // V^T pool base (all layers)
@@ -184,9 +189,19 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("barrier.sync %0, %1;" ::"r"(kEpiBar), "r"(kEpiThreads) : "memory");
 }
 
-__device__ __forceinline__ void put_operand(void* op, long idx, long plane, float v, int f32) {
-  if (f32) {
+// Operand element types of the projections: hi/lo bf16 planes beside bf16
+// weights, f32 for the f32 drafter, hi/lo f16 planes beside e4m3 weights
+// (widened to f16 for the tensor cores, which take one type for both sides).
+enum OpKind { OPK_BF16 = 0, OPK_F32 = 1, OPK_F16 = 2 };
+
+__device__ __forceinline__ void put_operand(void* op, long idx, long plane, float v, int kind) {
+  if (kind == OPK_F32) {
     reinterpret_cast<float*>(op)[idx] = v;
+  } else if (kind == OPK_F16) {
+    const __half hi = __float2half_rn(v);
+    const __half lo = __float2half_rn(v - __half2float(hi));
+    reinterpret_cast<__half*>(op)[idx] = hi;
+    reinterpret_cast<__half*>(op)[idx + plane] = lo;
   } else {
     __nv_bfloat16 hi = __float2bfloat16_rn(v);
     __nv_bfloat16 lo = __float2bfloat16_rn(v - __bfloat162float(hi));
@@ -399,7 +414,7 @@ static __device__ void tile_epilogue(const EpiArgs& e, int tile, float* acc, int
   const Geo& g = e.g;
   float* rsc = red + kEpiTokChunk * (kTileN + 1);   // per-token input-norm scale
   const int f = et;                                 // feature within the tile
-  const float wsc = e.wscale ? e.wscale[tile * kTileN + f] : 1.f;
+  const float wsc = e.wscale ? kW8Unscale * e.wscale[tile * kTileN + f] : 1.f;
   float* acc_f = acc + (long)f * nt;
   for (int tok0 = 0; tok0 < e.n_tok; tok0 += kEpiTokChunk) {
     const int tc = min(kEpiTokChunk, e.n_tok - tok0);
@@ -430,7 +445,7 @@ static __device__ void tile_epilogue(const EpiArgs& e, int tile, float* acc, int
       for (int t = 0; t < tc; ++t) {
         const int tok = e.tok_base + tok0 + t;
         const float x = red[t * (kTileN + 1) + f];
-        if (e.op) put_operand(e.op, (long)tok * e.op_ld + col, e.op_plane, x * gn, e.op_f32);
+        if (e.op) put_operand(e.op, (long)tok * e.op_ld + col, e.op_plane, x * gn, e.op_kind);
       }
       epi_sync();
       if (e.ss_out) {

@@ -80,10 +80,10 @@ __global__ void __launch_bounds__(kRowThreads) prep_norm_kernel(FinishArgs f) {
       const float4 x = rn.out(k);
       const long idx = (long)tok * g.H + 4 * i;
       if (f.u_out) reinterpret_cast<float4*>(f.u_out + idx)[0] = x;
-      put_operand(f.op, idx + 0, f.op_plane, x.x, f.op_f32);
-      put_operand(f.op, idx + 1, f.op_plane, x.y, f.op_f32);
-      put_operand(f.op, idx + 2, f.op_plane, x.z, f.op_f32);
-      put_operand(f.op, idx + 3, f.op_plane, x.w, f.op_f32);
+      put_operand(f.op, idx + 0, f.op_plane, x.x, f.op_kind);
+      put_operand(f.op, idx + 1, f.op_plane, x.y, f.op_kind);
+      put_operand(f.op, idx + 2, f.op_plane, x.z, f.op_kind);
+      put_operand(f.op, idx + 3, f.op_plane, x.w, f.op_kind);
     }
   }
   trace_cta_exit(f.trace);
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
     const float gg[4] = {gv.x, gv.y, gv.z, gv.w}, uu[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      put_operand(f.op, (long)tok * g.I + j + q, f.op_plane, gg[q] / (1.f + __expf(-gg[q])) * uu[q], f.op_f32);
+      put_operand(f.op, (long)tok * g.I + j + q, f.op_plane, gg[q] / (1.f + __expf(-gg[q])) * uu[q], f.op_kind);
   }
   trace_cta_exit(f.trace);
 }
@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(256) conv_kernel(ConvArgs a) {
     const long idx = (long)t * g.H + c;
     if (a.half == 0) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) put_operand(a.op, idx + j, a.op_plane, o[j], a.op_f32);
+      for (int j = 0; j < 4; ++j) put_operand(a.op, idx + j, a.op_plane, o[j], a.op_kind);
     } else {
       float4* hp = reinterpret_cast<float4*>(a.h + idx);
       const float4 hv = *hp;

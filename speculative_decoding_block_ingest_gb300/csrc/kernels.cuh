@@ -15,7 +15,8 @@ enum OMode {
 // One weight-streaming projection: Y[tok][N] = X[tok][K] * W[N][K]^T
 // (swap-AB: W rows are tile rows, tokens are columns).
 struct GemmArgs {
-  const void* W;      // [N][K] in Geo::wtype (bf16 tensor-core path: 16 KB blocks)
+  const void* W;      // [N][K]: f32 rows, 16 KB bf16 blocks, or 8 KB e4m3 units (w8)
+  int w8;             // tensor-core path: W is e4m3 codes (per-row scales in e.wscale)
   int N, K;
   const void* X;      // operand [tok][K]: f32, or bf16 hi plane (+ lo plane at x_plane)
   int x_ld;
@@ -41,7 +42,7 @@ struct FinishArgs {
   float* acc;             // qk_finish: QKV accumulator [Mt][qkv_n]; swiglu: gate/up [Mt][2I]
   void* op;               // prep_norm / swiglu: operand planes
   long op_plane;
-  int op_f32;
+  int op_kind;             // operand kind (OpKind)
   const float* qn;        // qk_finish: head-norm gains of this layer
   const float* kn;
   const float2* rope_cs;  // per token [d/2] (cos, sin) x mscale
@@ -84,7 +85,7 @@ struct ConvArgs {
   int dyn_ld;
   void* op;               // prepare: operand planes of the sublayer's first projection
   long op_plane;
-  int op_f32;
+  int op_kind;             // operand kind (OpKind)
   float* h;               // finish: residual stream [Mt][H]
   float* zero0;           // prepare: buffers the next projections red.add into, cleared here
   long zero0_n;
@@ -107,7 +108,7 @@ struct AttnArgs {
   void* op;             // output operand [Mt][Hq*d] (hi/lo bf16 or f32)
   int op_ld;
   long op_plane;
-  int op_f32;
+  int op_kind;             // operand kind (OpKind)
   float scale_log2;     // log2(e)/sqrt(d): scores and the saved max are in log2 units
   unsigned long long* trace;   // optional per-CTA timestamps [items][kTraceWords], or null
   int* err;
@@ -121,7 +122,7 @@ struct InitArgs {
   void* op;             // ingest: operand output
   int op_ld;
   long op_plane;
-  int op_f32;
+  int op_kind;             // operand kind (OpKind)
   float* zero_ptr;      // floats to clear
   int zero_n;
   void* desc_dst;       // device descriptor
@@ -163,53 +164,6 @@ void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s);
 void launch_repack(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base, cudaStream_t s);
 void launch_repack_e4m3(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base,
                         cudaStream_t s);
-
-// Persistent round (round_mk.cu).  Counter offsets (u32 words) within one
-// layer's block of a counter set.
-struct MkCounters {
-  int per_layer;
-  int x_h;        // rows of norm(h) ready for QKV            (target n_tok)
-  int qkv_t;      // [qkv tiles] CTAs done with the tile       (target: contributors)
-  int head;       // [Hkv] q/k/v rows finished per kv group    (target n_tok*(G+2))
-  int att;        // [seq*Hkv] attention splits done           (target nsplit)
-  int comb;       // combined (token, q head) rows              (target n_tok*Hq)
-  int o_done;     // CTAs done with the O projection           (target grid)
-  int x2;         // rows of norm(h) ready for gate/up         (target n_tok)
-  int gu_t;       // [gate/up tiles] CTAs done with the tile   (target: contributors)
-  int act;        // [I/64] activation blocks ready            (target 1)
-  int down_done;  // CTAs done with the down projection        (target grid)
-};
-
-constexpr int kMkMaxTok = 64;   // block rows a persistent round takes (4 sequences)
-
-struct MkArgs {
-  Geo g;
-  int n_tok, nt, aw, stages, stage_bytes, n_items, datoms, kv_stage_bytes, x_lo_row;
-  Part pq, po, pg, pd;                        // stream-K partitions over the grid
-  const uint8_t *wq, *wo, *wg, *wd;           // layer-0 weight blocks
-  size_t wq_l, wo_l, wg_l, wd_l;              // bytes per layer
-  const float *in_ln, *post_ln, *qn, *kn, *fn;
-  float *h, *qkv_acc, *gu_acc, *out;
-  void *op_h, *op_o, *op_a;                   // bf16 hi planes
-  long plane_h, plane_o, plane_a;             // elements from hi to lo plane
-  void *q, *kpool, *vpool;
-  const int* btab;
-  const RoundDesc* rd;
-  const float2* rope_cs;
-  float *part_o, *part_ml;
-  unsigned *cnt, *cnt_next;                   // this round's counter set; the next one (zeroed here)
-  int cnt_words;
-  MkCounters c;
-  int* err;
-  float scale_log2;
-  uint32_t idesc_g, idesc_s, idesc_o;
-  unsigned long long* trace;                  // optional: kMkTraceWords per CTA
-};
-constexpr int kMkTraceWords = 128;   // {smid, entry globaltimer, per layer < 8: 14 stamps}
-size_t round_mk_smem_bytes(int nt, int stages, int d);
-int round_mk_stages(int nt, int d);
-cudaError_t launch_round_mk(const MkArgs& a, int grid, const void* tmxh, const void* tmxo, const void* tmxa,
-                            const void* tmq, const void* tmk, const void* tmv, cudaStream_t s);
 
 // Fixed device region of dflash_forward_full_static (static_full.cu).
 constexpr size_t kFixedKvBytes = size_t(16) << 20;

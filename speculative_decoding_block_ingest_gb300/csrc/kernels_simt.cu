@@ -279,10 +279,10 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) 
     }
     const float inv = 1.f / den;
     const long idx = (long)tok * a.op_ld + h * g.d + 4 * threadIdx.x;
-    put_operand(a.op, idx + 0, a.op_plane, t.x * inv, a.op_f32);
-    put_operand(a.op, idx + 1, a.op_plane, t.y * inv, a.op_f32);
-    put_operand(a.op, idx + 2, a.op_plane, t.z * inv, a.op_f32);
-    put_operand(a.op, idx + 3, a.op_plane, t.w * inv, a.op_f32);
+    put_operand(a.op, idx + 0, a.op_plane, t.x * inv, a.op_kind);
+    put_operand(a.op, idx + 1, a.op_plane, t.y * inv, a.op_kind);
+    put_operand(a.op, idx + 2, a.op_plane, t.z * inv, a.op_kind);
+    put_operand(a.op, idx + 3, a.op_plane, t.w * inv, a.op_kind);
   }
   trace_cta_exit(a.trace);
 }
@@ -338,10 +338,10 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
         reinterpret_cast<float4*>(a.h + (long)r * a.width)[c] = v[k];
       } else {
         const long idx = (long)r * a.op_ld + 4 * c;
-        put_operand(a.op, idx + 0, a.op_plane, v[k].x, a.op_f32);
-        put_operand(a.op, idx + 1, a.op_plane, v[k].y, a.op_f32);
-        put_operand(a.op, idx + 2, a.op_plane, v[k].z, a.op_f32);
-        put_operand(a.op, idx + 3, a.op_plane, v[k].w, a.op_f32);
+        put_operand(a.op, idx + 0, a.op_plane, v[k].x, a.op_kind);
+        put_operand(a.op, idx + 1, a.op_plane, v[k].y, a.op_kind);
+        put_operand(a.op, idx + 2, a.op_plane, v[k].z, a.op_kind);
+        put_operand(a.op, idx + 3, a.op_plane, v[k].w, a.op_kind);
       }
     }
   }

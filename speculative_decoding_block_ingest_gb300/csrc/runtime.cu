@@ -51,9 +51,12 @@ void ck(cudaError_t e, const char* what) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Bytes per stored weight element: f32 stays f32; bf16 and e4m3 weights are
-// stored as bf16 blocks for the tensor cores (e4m3 expands exactly).
-int esize_w(int wtype) { return wtype == DFLASH_F32 ? 4 : 2; }
+// Bytes per stored weight element: f32 rows, bf16 blocks of 16 KB, e4m3
+// units of 8 KB (widened to f16 in shared memory by the projection).
+int esize_w(int wtype) { return wtype == DFLASH_F32 ? 4 : (wtype == DFLASH_FP8_E4M3 ? 1 : 2); }
+
+// Element type of the projections' operand planes for these weights.
+int op_kind_of(int wtype) { return wtype == DFLASH_F32 ? OPK_F32 : (wtype == DFLASH_FP8_E4M3 ? OPK_F16 : OPK_BF16); }
 int esize_kv(int kvtype) { return kvtype == DFLASH_F32 ? 4 : (kvtype == DFLASH_FP8_E4M3 ? 1 : 2); }
 
 // Workspace carve-up, computed identically by dflash_workspace_bytes and dflash_create.
@@ -64,13 +67,10 @@ struct Layout {
   size_t kpool, vpool, btab, inv_freq;
   size_t h, op_h, op_taps, op_o, op_a, q, qkv_acc, gu_acc, ss;
   size_t gacc, rope_cs, counters, apart_o, apart_ml, rdesc, idesc, err;
-  size_t mkcnt;                                         // persistent round: two counter sets
   size_t cbase, cdyn, s_cdyn, cu, cy, cdyn_a, cdyn_m;   // DFlash2 conv: weights, u / y rows, coefficients
   int conv_n;                                           // rows of a padded dynamic projection
   size_t total;
   int Mt, pps, max_tiles, grid_max, items_cap, n_sites;
-  MkCounters mk;
-  int mk_words, mk_batch;                               // words per counter set; sequences per round
 };
 
 int sm_count() {
@@ -154,24 +154,6 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.rdesc = take(sizeof(RoundDesc));
   Lo.idesc = take(sizeof(IngestDesc));
   Lo.err = take(256);
-  {
-    const int qkv_tiles = (int)(qkv_n / kTileN), gu_tiles = (int)(2 * I / kTileN);
-    Lo.mk_batch = std::min(c.max_batch, kMkMaxTok / kBlock);
-    MkCounters& m = Lo.mk;
-    m.x_h = 0;
-    m.qkv_t = 1;
-    m.head = m.qkv_t + qkv_tiles;
-    m.att = m.head + (int)Hkv;
-    m.comb = m.att + Lo.mk_batch * (int)Hkv;
-    m.o_done = m.comb + 1;
-    m.x2 = m.o_done + 1;
-    m.gu_t = m.x2 + 1;
-    m.act = m.gu_t + gu_tiles;
-    m.down_done = m.act + gu_tiles;
-    m.per_layer = m.down_done + 1;
-    Lo.mk_words = (int)L * m.per_layer;
-    Lo.mkcnt = take((size_t)2 * Lo.mk_words * 4);
-  }
   Lo.total = off;
   return Lo;
 }
@@ -352,10 +334,6 @@ struct dflash_handle {
   bool use_tc = false;    // tensor-core projections (bf16 weights)
   bool attn_tc = false;   // tensor-core attention (bf16 KV, any weights)
   bool prof_on = false;
-  // persistent round kernel: only with DFLASH_ROUND_PATH=persistent at
-  // create; rounds alternate between the two counter sets
-  bool mk_off = false;
-  int mk_parity = 0;
   // replayable rounds: one instantiated graph per (sequences, attention
   // items, KV region); only the per-call init and final-norm nodes change
   struct RoundGraph {
@@ -370,7 +348,6 @@ struct dflash_handle {
   };
   std::vector<RoundGraph> graphs;
   uint64_t graph_clock = 0;
-  bool graphs_off = false;
   bool attn_fp8 = false;        // e4m3 KV cache: attention on kind::f8f6f4 scores
   uint64_t uid = 0;             // process-unique handle id (static region ownership)
   cudaStream_t cap_stream = nullptr;   // private stream the rounds are captured on
@@ -483,7 +460,7 @@ EpiArgs base_epi(dflash_t* h) {
   e.kpool = h->kv->kpool;
   e.vpool = h->kv->vpool;
   e.err = h->at<int>(h->lo.err);
-  e.op_f32 = h->cfg.weight_dtype == DFLASH_F32;
+  e.op_kind = op_kind_of(h->cfg.weight_dtype);
   return e;
 }
 
@@ -492,9 +469,9 @@ EpiArgs base_epi(dflash_t* h) {
 struct GemmSpec {
   int site;                     // weight map and counter block
   const void* W;
-  const float* wscale;
+  const float* wscale;          // per-row scales of e4m3 weights (8 KB units); nullptr: bf16 / f32 weights
   int N, K;
-  const void* X = nullptr;      // operand planes (bf16 hi/lo, or f32)
+  const void* X = nullptr;      // operand planes (bf16 or f16 hi/lo, or f32)
   const CUtensorMap* xmap = nullptr;   // [short, tall] operand maps
   int omode = O_TILE;
   float* dst = nullptr;         // O_RED destination [tok][dst_ld]
@@ -503,14 +480,15 @@ struct GemmSpec {
   EpiArgs e;
 };
 
-// Passes of <= 256 token columns; tensor cores for bf16 and e4m3 weights
-// (stored as bf16 blocks), CUDA cores for f32 weights.
+// Passes of <= 256 token columns; tensor cores for bf16 and e4m3 weights,
+// CUDA cores for f32 weights.
 void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
   const Geo& g = h->g;
   const int n_all = sp.e.n_tok;
   for (int base = 0; base < n_all; base += kPassTok) {
     GemmArgs a{};
     a.W = sp.W;
+    a.w8 = sp.wscale != nullptr;
     a.N = sp.N;
     a.K = sp.K;
     a.X = sp.X;
@@ -538,7 +516,8 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
     if (sp.omode == O_RED) out_b = nt * sp.N * 4;
     else if (sp.e.kind == EPI_FC) out_b = nt * sp.N * 4;
     else out_b = nt * sp.N * (g.kvtype == KV_F32 ? 4 : (g.kvtype == KV_FP8 ? 1.0 + 4.0 / g.d : 2));
-    const double bytes = (double)sp.N * sp.K * esize_w(g.wtype) + (sp.wscale ? sp.N * 4.0 : 0.0) + x_b + out_b;
+    const double ew = a.w8 ? 1.0 : (h->cfg.weight_dtype == DFLASH_F32 ? 4.0 : 2.0);
+    const double bytes = (double)sp.N * sp.K * ew + (sp.wscale ? sp.N * 4.0 : 0.0) + x_b + out_b;
     Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
     a.trace = h->use_tc ? trace_slot(h, DFLASH_KERNEL_GEMM, a.p.grid) : nullptr;
     if (h->use_tc) launch_gemm_tc(a, sp.xmap, s);
@@ -562,7 +541,7 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   ia.op = h->at<void>(h->lo.op_taps);
   ia.op_ld = width;
   ia.op_plane = (long)h->lo.Mt * width;
-  ia.op_f32 = h->cfg.weight_dtype == DFLASH_F32;
+  ia.op_kind = op_kind_of(h->cfg.weight_dtype);
   float* ss_feat = h->at<float>(h->lo.ss) + (size_t)(2 * g.L + 1) * h->lo.Mt;
   ia.zero_ptr = ss_feat;
   ia.zero_n = n_rows;
@@ -624,14 +603,6 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   run_gemm(h, kv, s);
 }
 
-// The persistent round takes bf16 rounds of up to kMkMaxTok block rows whose
-// projection stage fits at least two ring stages beside the attention buffers.
-bool mk_eligible(dflash_t* h, int n_tok) {
-  return h->use_tc && h->cfg.weight_dtype == DFLASH_BF16 && h->cfg.kv_dtype == DFLASH_BF16 &&
-         h->cfg.conv_groups == 0 && !h->mk_off && !h->evicted_any && n_tok <= kMkMaxTok && n_tok / kBlock <= h->lo.mk_batch &&
-         round_mk_stages((n_tok + 15) / 16 * 16, h->g.d) >= 2;
-}
-
 int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int* kstart) {
   std::vector<long> pages(lens.size());
   long units = 0, longest = 1;
@@ -639,13 +610,6 @@ int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int*
     pages[i] = (lens[i] + kBlock + kPage - 1) / kPage - kstart[i] / kPage;
     units += (long)h->g.Hkv * pages[i];
     longest = std::max(longest, pages[i]);
-  }
-  // the persistent round runs one item per CTA: at most n_sm items even after
-  // each (sequence, kv head) rounds its split count up
-  const bool mk = mk_eligible(h, (int)lens.size() * kBlock);
-  if (mk) {
-    const long target = std::max<long>(1, (long)h->n_sm - (long)h->g.Hkv * (long)lens.size());
-    return (int)std::max<long>(1, (units + target - 1) / target);
   }
   // Items run in waves of `slots` CTAs and each walks its pages serially, so
   // take the split that minimises waves x (pages per item + a fixed per-item
@@ -698,85 +662,6 @@ InitArgs round_init_args(dflash_t* h, int n_tok, const float* noise) {
   return ia;
 }
 
-// The whole round (after the per-call init) as one persistent kernel.
-void enqueue_round_mk(dflash_t* h, const RoundDesc& rd, float* out, cudaStream_t s) {
-  const Geo& g = h->g;
-  const Layout& lo = h->lo;
-  const int n_tok = rd.n_tok;
-  MkArgs a{};
-  a.g = g;
-  a.n_tok = n_tok;
-  a.nt = (n_tok + 15) / 16 * 16;
-  a.aw = 2 * a.nt;
-  a.stages = round_mk_stages(a.nt, g.d);
-  a.stage_bytes = kTileN * kTileK * 2 + 2 * a.nt * 128;
-  a.n_items = rd.n_items;
-  a.datoms = g.d / 64;
-  a.kv_stage_bytes = a.datoms * 64 * 128 + g.d * 128;
-  a.x_lo_row = lo.Mt;
-  const int grid = h->n_sm;
-  auto part = [&](int n_rows, int K) {
-    const int kb = K / kTileK;
-    return Part{n_rows / kTileN * kb, grid, kb};
-  };
-  a.pq = part(g.qkv_n, g.H);
-  a.po = part(g.H, g.Hq * g.d);
-  a.pg = part(2 * g.I, g.H);
-  a.pd = part(g.H, g.I);
-  a.wq = h->at<uint8_t>(lo.qkv);
-  a.wo = h->at<uint8_t>(lo.o);
-  a.wg = h->at<uint8_t>(lo.gu);
-  a.wd = h->at<uint8_t>(lo.down);
-  a.wq_l = (size_t)g.qkv_n * g.H * 2;
-  a.wo_l = (size_t)g.H * g.Hq * g.d * 2;
-  a.wg_l = (size_t)2 * g.I * g.H * 2;
-  a.wd_l = (size_t)g.H * g.I * 2;
-  a.in_ln = h->at<float>(lo.in_ln);
-  a.post_ln = h->at<float>(lo.post_ln);
-  a.qn = h->at<float>(lo.qn);
-  a.kn = h->at<float>(lo.kn);
-  a.fn = h->at<float>(lo.fn);
-  a.h = h->at<float>(lo.h);
-  a.qkv_acc = h->at<float>(lo.qkv_acc);
-  a.gu_acc = h->at<float>(lo.gu_acc);
-  a.out = out;
-  a.op_h = h->at<void>(lo.op_h);
-  a.op_o = h->at<void>(lo.op_o);
-  a.op_a = h->at<void>(lo.op_a);
-  a.plane_h = (long)lo.Mt * g.H;
-  a.plane_o = (long)lo.Mt * g.Hq * g.d;
-  a.plane_a = (long)lo.Mt * g.I;
-  a.q = h->at<void>(lo.q);
-  a.kpool = h->kv->kpool;
-  a.vpool = h->kv->vpool;
-  a.btab = h->at<int>(lo.btab);
-  a.rd = h->at<RoundDesc>(lo.rdesc);
-  a.rope_cs = h->at<float2>(lo.rope_cs);
-  a.part_o = h->at<float>(lo.apart_o);
-  a.part_ml = h->at<float>(lo.apart_ml);
-  unsigned* sets = h->at<unsigned>(lo.mkcnt);
-  a.cnt = sets + (size_t)h->mk_parity * lo.mk_words;
-  a.cnt_next = sets + (size_t)(1 - h->mk_parity) * lo.mk_words;
-  a.cnt_words = lo.mk_words;
-  a.c = lo.mk;
-  a.err = h->at<int>(lo.err);
-  a.scale_log2 = 1.4426950408889634f / std::sqrt((float)g.d);
-  // algorithmic bytes: every weight once, every cached K/V row once, the
-  // block rows in and out
-  double bytes = (double)g.L * (a.wq_l + a.wo_l + a.wg_l + a.wd_l);
-  for (int i = 0; i < rd.n_seq; ++i)
-    bytes += (double)(rd.len[i] + kBlock) * g.L * g.Hkv * g.d * 2.0 * esize_kv(g.kvtype);
-  bytes += (double)n_tok * g.H * 8;
-  // a trace record of kMkTraceWords per CTA spans kMkTraceWords / kTraceWords slots
-  a.trace = trace_slot(h, DFLASH_KERNEL_ROUND, grid * (kMkTraceWords / kTraceWords));
-  {
-    Launch L(h, DFLASH_KERNEL_ROUND, bytes, s);
-    ck(launch_round_mk(a, grid, h->xmap_h, h->xmap_o, h->xmap_a, &h->qmap, &h->kv->kmap, &h->kv->vmap, s),
-       "persistent round launch");
-  }
-  h->mk_parity ^= 1;
-}
-
 // The round: per layer
 //   prep_norm(input_ln) -> QKV -> qk_finish -> attention -> combine -> O ->
 //   prep_norm(post_ln) -> gate/up -> swiglu -> down.
@@ -791,7 +676,6 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   const int n_tok = rd.n_tok;
   const size_t Mt = h->lo.Mt;
   const bool fp8 = h->cfg.weight_dtype == DFLASH_FP8_E4M3;
-  const bool f32 = h->cfg.weight_dtype == DFLASH_F32;
   const size_t ew = wbytes(h);
   float* hres = h->at<float>(h->lo.h);
   float* qkv_acc = h->at<float>(h->lo.qkv_acc);
@@ -805,15 +689,10 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   }
   ck(cudaGetLastError(), "round init launch");
 
-  if (mk_eligible(h, n_tok) && rd.n_items <= h->n_sm) {
-    enqueue_round_mk(h, rd, out, s);
-    return;
-  }
-
   FinishArgs fb{};
   fb.n_tok = n_tok;
   fb.h = hres;
-  fb.op_f32 = f32;
+  fb.op_kind = op_kind_of(h->cfg.weight_dtype);
   fb.rope_cs = h->at<float2>(h->lo.rope_cs);
   fb.dest = h->at<RoundDesc>(h->lo.rdesc)->dest;
   fb.q_out = h->at<void>(h->lo.q);
@@ -828,7 +707,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   // the MLP's norm, gate/up and SwiGLU as one tile-owning projection: tensor
   // cores, no DFlash2 conv around the sublayer, up to 32 block rows, a tile
   // per SM
-  const bool fused_mlp = h->use_tc && !Gc && n_tok <= 32 && 2 * g.I / kTileN <= h->n_sm;
+  const bool fused_mlp = h->use_tc && !fp8 && !Gc && n_tok <= 32 && 2 * g.I / kTileN <= h->n_sm;
   auto prep_norm = [&](const float* gain) {
     FinishArgs f = fb;
     f.gain = gain;
@@ -869,7 +748,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     c.dyn_ld = conv_n;
     c.op = h->at<void>(h->lo.op_h);
     c.op_plane = (long)Mt * g.H;
-    c.op_f32 = f32;
+    c.op_kind = op_kind_of(h->cfg.weight_dtype);
     c.zero0 = cy;
     c.zero0_n = (long)n_tok * g.H;
     c.zero1 = dyn_sub[sub ^ 1];
@@ -943,7 +822,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
     a.op = h->at<void>(h->lo.op_o);
     a.op_ld = g.Hq * g.d;
     a.op_plane = (long)Mt * g.Hq * g.d;
-    a.op_f32 = f32;
+    a.op_kind = op_kind_of(h->cfg.weight_dtype);
     a.scale_log2 = 1.4426950408889634f / std::sqrt((float)g.d);
     a.err = h->at<int>(h->lo.err);
     a.g = g;
@@ -1170,16 +1049,14 @@ int ingest_slots(dflash_t* h, int n_seq, const int32_t* slots, const int32_t* t_
 // the host about as long as the GPU takes to run them, so they are captured
 // once per (sequences, attention items, KV region) and replayed; a replay
 // changes only the init node (descriptor blob, noise rows) and the final-norm
-// node (output rows).  Off while profiling, for the persistent kernel, when
-// the caller's stream is itself being captured, and with DFLASH_GRAPHS=0 at
-// create; while tracing, each round is captured afresh with its own trace
-// regions.
+// node (output rows).  Off while profiling and when the caller's stream is
+// itself being captured; while tracing, each round is captured afresh with
+// its own trace regions.
 void enqueue_round_graph(dflash_t* h, InitBlob& blob, const float* noise, float* out, cudaStream_t s) {
   const RoundDesc& rd = blob.round;
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   ck(cudaStreamIsCapturing(s, &cap), "stream capture query");
-  const bool mk = mk_eligible(h, rd.n_tok) && rd.n_items <= h->n_sm;
-  if (h->graphs_off || h->prof_on || mk || cap != cudaStreamCaptureStatusNone) {
+  if (h->prof_on || cap != cudaStreamCaptureStatusNone) {
     enqueue_round(h, blob, noise, out, s);
     return;
   }
@@ -1553,16 +1430,6 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     h->use_tc = cfg->weight_dtype != DFLASH_F32;
     h->attn_tc = cfg->kv_dtype != DFLASH_F32;
     h->attn_fp8 = cfg->kv_dtype == DFLASH_FP8_E4M3;
-    {
-      // "persistent": the whole round in one kernel (round_mk.cu); by default
-      // one kernel per step, which measured faster at the 8-layer shape
-      const char* path = std::getenv("DFLASH_ROUND_PATH");
-      h->mk_off = !(path && std::string(path) == "persistent");
-    }
-    {
-      const char* gs = std::getenv("DFLASH_GRAPHS");   // "0": launch every round's kernels directly
-      h->graphs_off = gs && std::string(gs) == "0";
-    }
     if (h->use_tc) {
       const uint64_t Mt2 = 2ull * lo.Mt;
       const uint32_t tall = Mt2 >= 256 ? 128u : 16u;   // 128-row boxes only where a pass can reach 128 tokens
@@ -1591,7 +1458,6 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
     ck(cudaMemsetAsync(h->ws + lo.kpool, 0, lo.vpool - lo.kpool, s), "K pool clear");
     ck(cudaMemsetAsync(h->ws + lo.vpool, 0, lo.btab - lo.vpool, s), "V pool clear");
     ck(cudaMemsetAsync(h->ws + lo.btab, 0xff, (size_t)(cfg->max_seqs + 1) * lo.pps * 4, s), "block table");
-    ck(cudaMemsetAsync(h->ws + lo.mkcnt, 0, (size_t)2 * lo.mk_words * 4, s), "round counters");
     ck(cudaMemsetAsync(h->ws + lo.counters, 0, (size_t)lo.n_sites * lo.max_tiles * 4, s), "counters");
     ck(cudaMemsetAsync(h->ws + lo.gacc, 0, (size_t)lo.max_tiles * kTileN * kPassTok * 4, s), "tile accumulators");
     ck(cudaMemsetAsync(h->ws + lo.qkv_acc, 0, (size_t)lo.Mt * g.qkv_n * 4, s), "QKV accumulator");

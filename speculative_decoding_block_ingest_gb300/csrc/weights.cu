@@ -31,34 +31,28 @@ __global__ void repack_kernel(uint8_t* dst, int K, const uint16_t* src, int n_ro
   }
 }
 
-// The same blocks from OCP e4m3 bytes: every e4m3 value is exactly a bf16
-// value, so the expansion is exact (the per-row scales are applied where the
-// projections drain their accumulators).
+// e4m3 weights stay one byte each: block (T, kb) of 128 rows x 64 codes is
+// an 8 KB unit at index T * (K/64) + kb, row r at byte r * 64 with its 16-code
+// piece p at piece position p ^ ((r >> 1) & 3), so that eight consecutive rows'
+// pieces fall in eight different shared-memory bank groups when a thread per
+// row reads them.  The projection widens the codes to f16 (exact) in shared
+// memory; the per-row scales multiply the sums as the projection drains.
 __global__ void repack_e4m3_kernel(uint8_t* dst, int K, const uint8_t* src, int n_rows, int chunk, int stride,
                                    int base) {
-  const int cpr = K / 8;   // 8-element chunks per row (16 bytes of bf16)
-  const long n = (long)n_rows * cpr;
+  const int ppr = K / 16;   // 16-code pieces per row
+  const long n = (long)n_rows * ppr;
   for (long idx = (long)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (long)gridDim.x * blockDim.x) {
-    const int i = (int)(idx / cpr), c = (int)(idx % cpr);
+    const int i = (int)(idx / ppr), c = (int)(idx % ppr);
     const int R = base + (i / chunk) * stride + i % chunk;
-    const int T = R / kTileN, r = R % kTileN, kb = c / 8, c16 = c % 8;
-    const size_t off = ((size_t)T * (K / kTileK) + kb) * (kTileN * kTileK * 2) + (size_t)r * 128 + ((c16 ^ (r & 7)) * 16);
-    const uint2 raw = *reinterpret_cast<const uint2*>(src + (size_t)i * K + (size_t)c * 8);
-    const uint8_t* b = reinterpret_cast<const uint8_t*>(&raw);
-    __nv_bfloat16 out[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      __nv_fp8_e4m3 v;
-      v.__x = b[e];
-      out[e] = __float2bfloat16_rn(static_cast<float>(v));
-    }
-    *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(out);
+    const int T = R / kTileN, r = R % kTileN, kb = c / 4, p = c % 4;
+    const size_t off = ((size_t)T * (K / kTileK) + kb) * (kTileN * kTileK) + (size_t)r * 64 + ((p ^ ((r >> 1) & 3)) * 16);
+    *reinterpret_cast<uint4*>(dst + off) = *reinterpret_cast<const uint4*>(src + (size_t)i * K + (size_t)c * 16);
   }
 }
 
 void launch_repack_e4m3(void* dst, int K, const void* src, int n_rows, int chunk, int stride, int base,
                         cudaStream_t s) {
-  const long n = (long)n_rows * (K / 8);
+  const long n = (long)n_rows * (K / 16);
   const int grid = (int)std::min<long>((n + 255) / 256, 8192);
   if (n > 0)
     repack_e4m3_kernel<<<grid, 256, 0, s>>>(static_cast<uint8_t*>(dst), K, static_cast<const uint8_t*>(src), n_rows,

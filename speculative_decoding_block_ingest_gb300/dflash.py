@@ -30,7 +30,7 @@ EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dfla
            "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches",
            "dflash_selftest_wait_timeout")
 TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
-KERNEL_KINDS = ("gemm", "attention", "combine", "init", "norm", "finish", "round")
+KERNEL_KINDS = ("gemm", "attention", "combine", "init", "norm", "finish")
 
 
 class Config(ctypes.Structure):

@@ -138,6 +138,9 @@ WORKLOADS: Dict[str, Workload] = {
                                    ctx_lo=1024, ctx_hi=16384),
     "qwen3_8l_fp8_b8_ctx65536": Workload("qwen3_8l_fp8_b8_ctx65536", QWEN3_8L_FP8, batch=8,
                                          ctx=65536, ingest_lo=16, ingest_hi=16, rounds=32),
+    # the bench shape with e4m3 weights (half the weight bytes per round)
+    "qwen3_8l_fp8w_ctx8192": Workload("qwen3_8l_fp8w_ctx8192", QWEN3_8L_FP8, batch=1, ctx=8192,
+                                      ingest_lo=1, ingest_hi=16, rounds=200),
     # the bench shape as a DFlash2 drafter (conv of 32 channel groups around every sublayer)
     "qwen3_8l_d2_ctx8192": Workload("qwen3_8l_d2_ctx8192", QWEN3_8L_D2, batch=1, ctx=8192,
                                     ingest_lo=1, ingest_hi=16, rounds=200),
