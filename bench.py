@@ -13,7 +13,12 @@ e2e    = rounds/s through the public API with pinned HOST inputs: each step
 roofline = the projection kernel (weight-streaming GEMM, the dominant
          kernel): algorithmic bytes per launch / mean launch time, from CUDA
          event pairs the library records around each launch of a profiled
-         pass of the same steps
+         pass of the same steps; round_frac = the whole step's algorithmic
+         bytes / ms_per_step against the same HBM peak; in_situ = each kernel
+         kind's share of the step on the live (graph) path, from the
+         library's per-CTA entry/exit stamps, with its GB/s there
+repeats = the timed steps split into 5 consecutive windows (events between
+         steps, no synchronisation): rounds/s of each, median and spread
 cpu_baseline = the f64 CPU oracle on this host's cores, a bounded sample of
          the same workload (one-time cache build excluded)
 
@@ -183,6 +188,38 @@ def workload_config(wl):
             "l2": "no flush: every round streams >1 GB of weights and KV, far above the 129 MB L2"}
 
 
+def in_situ_shares(traced, prof, K, T):
+    """Each kernel kind's share of the step on the live (graph) path: per
+    launch, the time by which its last CTA's exit extends the step past every
+    earlier launch's end (its first CTA's entry if later), from the per-CTA
+    entry/exit stamps; per kind summed and divided by the T traced steps.
+    GB/s = the kind's algorithmic bytes per step (profiled pass) / that time."""
+    from speculative_decoding_block_ingest_gb300 import dflash
+    spans = []
+    for kind, grid, t in traced:
+        ent, ext = t[:, 1].double(), t[:, 15].double()
+        ok = (ent > 0) & (ext > 0)
+        if int(ok.sum()) == 0:
+            continue
+        spans.append((dflash.KERNEL_KINDS[kind], ent[ok].min().item(), ext[ok].max().item()))
+    spans.sort(key=lambda x: x[1])
+    excl, end, idle = {}, None, 0.0
+    for name, s0, e in spans:
+        if end is None:
+            end = s0
+        if s0 > end:
+            idle += s0 - end
+        add = max(0.0, e - max(s0, end))
+        excl[name] = excl.get(name, 0.0) + add
+        end = max(end, e)
+    out = {"steps": T, "idle_ms_per_step": idle / 1e6 / T, "kinds": {}}
+    for name, ns in excl.items():
+        ms_step = ns / 1e6 / T
+        b = prof.get(name, (0, 0.0, 0.0))[2] / K
+        out["kinds"][name] = {"ms_per_step": ms_step, "GB/s": (b / 1e9) / (ms_step / 1e3) if ms_step > 0 and b else None}
+    return out
+
+
 # ---------------------------------------------------------------- GPU leg
 def main():
     args = parse()
@@ -208,7 +245,8 @@ def main():
     cfg = wl.cfg
     B = wl.batch
     K, Wm = args.steps, args.warmup
-    counts = wl.ingest_counts(Wm + K)          # [step][sequence]
+    T = min(K, 8)                                # traced steps (in-situ shares)
+    counts = wl.ingest_counts(Wm + K + T)      # [step][sequence]
     lens0 = wl.ctx_lengths()
     SLOTS = 3                                    # device-timed, e2e, profiled passes
     grow = [sum(c[i] for c in counts) for i in range(B)]
@@ -237,7 +275,7 @@ def main():
     # per-step inputs, resident in HBM
     taps_steps, noise_steps, lens = [], [], []
     cur = list(lens0)
-    for k in range(Wm + K):
+    for k in range(Wm + K + T):
         taps_steps.append(torch.cat([taps_for(i, cur[i], counts[k][i]) for i in range(B)]))
         noise_steps.append(torch.stack([synth.noise_rows(cfg, i, k) for i in range(B)]).to(dev))
         lens.append(list(cur))
@@ -270,10 +308,17 @@ def main():
     barrier()
     n0 = dr.launch_count()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # window boundaries: events between steps, recorded without synchronising
+    R = min(5, K)
+    bounds = [Wm + (K * r) // R for r in range(R + 1)]
+    wev = [torch.cuda.Event(enable_timing=True) for _ in range(R + 1)]
     clocks.mark(True)
     ev0.record(stream)
     for k in range(Wm, Wm + K):
+        if k in bounds:
+            wev[bounds.index(k)].record(stream)
         step(0, k)
+    wev[R].record(stream)
     ev1.record(stream)
     barrier()
     clocks.mark(False)
@@ -281,6 +326,11 @@ def main():
     clk = clocks.stop()
     ms = replicas.slowest_ms(ev0.elapsed_time(ev1), dist, dev)
     value = replicas.job_throughput(world, K, ms)
+    win = [(bounds[r + 1] - bounds[r]) / (wev[r].elapsed_time(wev[r + 1]) / 1e3) for r in range(R)]
+    repeats = {"n": R, "steps_each": [bounds[r + 1] - bounds[r] for r in range(R)],
+               "rounds_per_s": [round(w, 1) for w in win], "median": statistics.median(win),
+               "spread_pct": 100.0 * (max(win) - min(win)) / statistics.median(win),
+               "note": "rank-local windows of the timed region"}
 
     # ---- end-to-end pass (pass 1): pinned host inputs, copies inside the timed region
     host_taps = [t.cpu().pin_memory() for t in taps_steps]
@@ -309,7 +359,7 @@ def main():
     e1.record(stream)
     barrier()
     ms_e2e = replicas.slowest_ms(e0.elapsed_time(e1), dist, dev)
-    h2d = sum(sum(c) for c in counts[Wm:]) * width * 4 / K + B * 16 * cfg.hidden * 4
+    h2d = sum(sum(c) for c in counts[Wm:Wm + K]) * width * 4 / K + B * 16 * cfg.hidden * 4
     d2h = B * 16 * cfg.hidden * 4
 
     # ---- greedy draft tokens through a seeded target lm_head (vocab 32768)
@@ -343,12 +393,26 @@ def main():
     prof = dr.profile_read()
     dr.profile(False)
     dr.device_status()
+    # in-situ shares: T more steps of pass 2 on the graph path, traced (a
+    # traced round runs the graph of an untraced one, captured afresh)
+    dr.trace_begin(16 << 20)
+    for k in range(Wm + K, Wm + K + T):
+        step(2, k)
+    barrier()
+    traced = dr.trace_end()
+    in_situ = in_situ_shares(traced, prof, K, T)
     g_n, g_ms, g_b = prof["gemm"]
     peak, peak_kind = peaks()
     achieved = (g_b / 1e9) / (g_ms / 1e3) if g_ms > 0 else 0.0
+    step_bytes = sum(b for (_, _, b) in prof.values()) / K
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": gemm_traffic(wl.name), "kernel": "gemm_swapab (all projections)",
-                "launches": g_n, "bytes_per_launch": g_b / max(g_n, 1), "peak_source": peak_kind}
+                "launches": g_n, "bytes_per_launch": g_b / max(g_n, 1), "peak_source": peak_kind,
+                "round_bytes_per_step": step_bytes,
+                "round_frac": (step_bytes / 1e9) / (ms / K / 1e3) / peak}
+    for v in in_situ["kinds"].values():
+        if v.get("GB/s") is not None:
+            v["frac"] = v["GB/s"] / peak
     breakdown = {k: {"launches": n, "ms_per_step": m / K, "GB/s": (b / 1e9) / (m / 1e3) if m else None}
                  for k, (n, m, b) in prof.items()}
 
@@ -367,13 +431,14 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "rounds/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded N(0,1/fan_in) weights, N(0,1) taps/noise)",
+        "dtype": {"bf16": "bf16", "fp8": "e4m3", "f32": "f32"}[cfg.weight_dtype],
+        "data": "synthetic (seeded N(0,1/fan_in) weights, N(0,1) taps/noise)",
         "config": workload_config(wl), "roofline": roofline, "cpu_baseline": cpu,
         "e2e": {"value": replicas.job_throughput(world, K, ms_e2e), "unit": "rounds/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "clocks": clk, "gpu_launches": launches,
         "drafted_tokens_per_s": 15 * B * value, "block_rows_per_s": 16 * B * value,
-        "kernel_breakdown": breakdown, "lm_head": lm_line,
+        "kernel_breakdown": breakdown, "in_situ": in_situ, "repeats": repeats, "lm_head": lm_line,
     }
     print(json.dumps(line))
     if dist is not None:

@@ -27,8 +27,8 @@
  *    issued on one stream, or ordered by the caller.
  *  - Device f32 row buffers (taps, noise_emb, out) start on a 16-byte
  *    boundary (rows are moved as float4); a misaligned one is rejected with
- *    DFLASH_ERR_INVALID_ARG.  So do bf16 weight matrices (re-blocked at
- *    dflash_create with 16-byte moves).
+ *    DFLASH_ERR_INVALID_ARG.  So do bf16 and e4m3 weight matrices
+ *    (re-blocked at dflash_create with 16-byte moves).
  *  - The library never allocates device memory: the caller allocates the
  *    workspace (dflash_workspace_bytes) and owns every buffer.
  *  - Every call validates all of its arguments before it launches anything.
@@ -141,17 +141,29 @@ typedef struct dflash_weights {
 } dflash_weights;
 
 /* Bytes of device workspace the handle needs for this config (256-byte
- * aligned start required).  Holds the repacked weights, the paged KV pools,
- * page tables, activations and reduction scratch.  bf16 and e4m3 weights are
- * stored as bf16 blocks for the tensor cores (e4m3 values expand exactly;
- * their per-row scales are applied to the projections' sums), f32 weights
- * as given. */
+ * aligned start required).  It is the one allocation behind three items of
+ * the pages: the per-layer draft KV cache (memra_engine::dflash, struct
+ * DflashKv; paged with one block table shared by the layers as in
+ * spark_model::layers::dflash_head, struct DflashProposerState), the
+ * per-step scratch of the block forward (dflash_head, struct DflashScratch)
+ * and the weights.  It holds the repacked weights, the paged KV pools, page
+ * tables, activations and reduction scratch.  bf16 weights are stored as
+ * 16 KB blocks for the tensor cores, e4m3 weights as 8 KB units of one byte
+ * per weight (widened to f16 inside the projections; their per-row scales
+ * are applied to the projections' sums), f32 weights as given.  A config
+ * that dflash_create would reject fails here with the same code
+ * (DFLASH_ERR_INVALID_ARG or DFLASH_ERR_UNSUPPORTED). */
 int dflash_workspace_bytes(const dflash_config *cfg, size_t *bytes);
 
 /* Validate cfg, carve the caller's workspace, copy and repack the weights
  * into it (the caller may free its weight buffers once the stream has
  * passed this call), resolve every kernel once and build the RoPE table.
- * Returns a handle in *out. */
+ * Resolving the kernels once here, so that every later call only launches,
+ * is the dflash_head page's struct DflashKernels (handles resolved once at
+ * from_weights, each propose() only launches).  The workspace stays owned
+ * by the caller and must outlive the handle; the handle itself is host
+ * memory freed by dflash_destroy.  Returns a handle in *out; on error *out
+ * is left untouched and nothing was launched. */
 int dflash_create(const dflash_config *cfg, const dflash_weights *w, void *workspace,
                   size_t workspace_bytes, void *stream, dflash_t **out);
 
@@ -200,10 +212,14 @@ int dflash_forward_full(dflash_t *h, int32_t ctx, const float *taps, const float
  * Arguments, layouts and results are those of dflash_forward_full; no
  * sequence state changes.
  *
- * Limit: ctx + 16 rows must fit floor(16 MiB / (2 * L * Hkv * 64 * d *
- * kv_bytes)) pages of 64 rows -- 1008 context rows for the 8-layer,
- * 4-kv-head, head_dim-128 bf16-KV drafter; a larger ctx is rejected with
- * DFLASH_ERR_CAPACITY before anything is launched.
+ * Limit: ctx + 16 rows must fit floor(16 MiB / (2 * L * Hkv * 64 * row))
+ * pages of 64 rows, row = d * kv_bytes + (e4m3 KV ? 4 : 0) bytes (an e4m3
+ * row carries its f32 scale) -- 16 pages, 1008 context rows, for the
+ * 8-layer, 4-kv-head, head_dim-128 drafter with a bf16 KV cache; 31 pages,
+ * 1968 rows, with an e4m3 one.  A larger ctx is rejected with
+ * DFLASH_ERR_CAPACITY before anything is launched.  The current device must
+ * be the handle's (the one current at dflash_create), else
+ * DFLASH_ERR_INVALID_ARG.
  *
  * Set-up: the first call on a device (with that device current) looks the
  * region's address up once (cudaGetSymbolAddress; a failure returns
@@ -253,10 +269,19 @@ int dflash_draft_tokens(dflash_t *h, int32_t n_seq, const float *hidden, const v
  * windowed (the first-light forward attends to its whole context). */
 int dflash_set_ctx_cap(dflash_t *h, int32_t cap);
 
-/* Drop a sequence's cache (len = 0, pages back to the pool). */
+/* Drop a sequence's cache (len = 0, pages back to the pool): a fresh
+ * DflashKv (memra_engine::dflash, struct DflashKv) for slot seq_id, whose
+ * pages return to the shared pool of the dflash_head page's
+ * DflashProposerState.  Host-side bookkeeping only (no launch, no stream);
+ * a null handle or an id out of [0, max_seqs) fails with
+ * DFLASH_ERR_INVALID_ARG. */
 int dflash_seq_reset(dflash_t *h, int32_t seq_id);
 
-/* Committed rows of a sequence. */
+/* Committed rows of a sequence: the append-only len of its DflashKv
+ * (memra_engine::dflash, struct DflashKv: block rows land transiently at
+ * [len, len + 16) each round and are never committed, so len counts only
+ * ingested context rows).  Written to *len on the host; a null argument or
+ * an id out of [0, max_seqs) fails with DFLASH_ERR_INVALID_ARG. */
 int dflash_seq_len(dflash_t *h, int32_t seq_id, int64_t *len);
 
 /* Copy cached rows row0 .. row0+nrows-1 of one layer of a sequence out of

@@ -350,6 +350,7 @@ struct dflash_handle {
   uint64_t graph_clock = 0;
   bool attn_fp8 = false;        // e4m3 KV cache: attention on kind::f8f6f4 scores
   uint64_t uid = 0;             // process-unique handle id (static region ownership)
+  int device = -1;              // the device current at create (its workspace, weights and static region)
   cudaStream_t cap_stream = nullptr;   // private stream the rounds are captured on
   struct Rec {
     int kind;
@@ -1327,6 +1328,10 @@ int dflash_create(const dflash_config* cfg, const dflash_weights* w, void* works
   h->lo = lo;
   h->ws = static_cast<char*>(workspace);
   h->n_sm = n_sm;
+  if (cudaGetDevice(&h->device) != cudaSuccess) {
+    delete h;
+    return fail(DFLASH_ERR_CUDA, "device query failed");
+  }
   const int L = cfg->n_layers, H = cfg->hidden, d = cfg->head_dim, Hq = cfg->n_heads, Hkv = cfg->n_kv_heads;
   const int I = cfg->intermediate;
   Geo& g = h->g;
@@ -1526,6 +1531,13 @@ int dflash_forward_full_static(dflash_t* h, int32_t ctx, const float* taps, cons
   if (!aligned16(noise_emb) || !aligned16(out) || (ctx > 0 && !aligned16(taps)))
     return fail(DFLASH_ERR_INVALID_ARG, "taps / noise_emb / out must start on a 16-byte boundary");
   if (ctx + kBlock > h->cfg.max_seq_len) return fail(DFLASH_ERR_CAPACITY, "ctx exceeds max_seq_len");
+  {
+    // the static region is looked up on the current device and bound to the
+    // handle at its first use: only the handle's own device may call
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev != h->device)
+      return fail(DFLASH_ERR_INVALID_ARG, "the current device (%d) is not the handle's device (%d)", dev, h->device);
+  }
   // one page of K (or V^T) for every layer, with its row scales for e4m3
   const size_t page_bytes = (size_t)h->g.L * h->g.Hkv * kPage *
                             ((size_t)h->g.d * esize_kv(h->cfg.kv_dtype) + (h->attn_fp8 ? 4 : 0));

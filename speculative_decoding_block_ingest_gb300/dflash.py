@@ -310,7 +310,7 @@ class Drafter:
         _check(self.lib.dflash_trace_begin(self.handle, ctypes.c_void_p(self._trace.data_ptr()), words * 8))
 
     def trace_end(self):
-        """Stop tracing; returns [(kind, grid, tensor[grid, 8])] per traced launch."""
+        """Stop tracing; returns [(kind, grid, tensor[grid, TRACE_WORDS])] per traced launch."""
         n = ctypes.c_int32(0)
         _check(self.lib.dflash_trace_launches(self.handle, 0, None, None, None, ctypes.byref(n)))
         k = (ctypes.c_int32 * max(1, n.value))()

@@ -12,7 +12,7 @@ import torch
 
 from oracle import dflash_oracle as O
 from speculative_decoding_block_ingest_gb300 import synth
-from _common import oracle_weights, rel_err
+from _common import bf16_readback_stats, oracle_weights, rel_err
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -99,8 +99,18 @@ def test_batched_ragged_rounds_match_oracle(cfg):
         for li in range(cfg.n_layers):
             k, v = dr.kv_read(s, li, 0, lens[s])
             torch.cuda.synchronize()
-            assert rel_err(_np(k), kv.k[s][li]) <= tol(cfg)
-            assert rel_err(_np(v), kv.v[s][li]) <= tol(cfg)
+            if cfg.kv_dtype == "bf16":
+                # the cached rows are f32 results rounded to nearest bf16:
+                # every element within one bf16 spacing of the oracle's f64
+                # value (spacing floored at that of rms/8), and at least 99%
+                # equal to the oracle's value rounded to bf16 (a truncating
+                # store would match about half)
+                for got, ref in ((k, kv.k[s][li]), (v, kv.v[s][li])):
+                    ulps, same = bf16_readback_stats(_np(got), ref)
+                    assert ulps <= 1.0 and same >= 0.99, (s, li, ulps, same)
+            else:
+                assert rel_err(_np(k), kv.k[s][li]) <= tol(cfg)
+                assert rel_err(_np(v), kv.v[s][li]) <= tol(cfg)
 
 
 def test_round_equals_forward_full_on_gpu():
