@@ -200,31 +200,21 @@ void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s) {
 }
 
 // Merge the split-KV partials of one (token, q head) row into the O-proj
-// operand.  All loads of a pass are issued before their use: the (m, l) pairs
-// one split per thread, then the partial rows (d/4 lanes per split, a warp
-// covering 32/(d/4) splits, eight warps, four splits deep per thread).
+// operand.  One pass: warp w takes splits w, w + 8, ..., eight deep per
+// thread, every (m, l) pair and partial-row load of a pass issued before the
+// first use (d/4 lanes per split row); each thread merges its splits online
+// against its own running maximum, and one exchange through shared memory
+// merges the eight warps -- a single L2 round trip per pass.
 constexpr int kCombThreads = 256;
-__device__ __forceinline__ float block_reduce(float v, bool is_max, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float u = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? fmaxf(v, u) : v + u;
-  }
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = red[0];
-#pragma unroll
-  for (int w = 1; w < kCombThreads / 32; ++w) t = is_max ? fmaxf(t, red[w]) : t + red[w];
-  __syncthreads();
-  return t;
-}
+constexpr int kCombWarps = kCombThreads / 32;
+constexpr int kCombDepth = 8;
 
 __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) {
   trace_cta_entry(a.trace);
   pdl_launch_dependents();
   pdl_wait();
-  __shared__ float red[kCombThreads / 32];
-  __shared__ float4 part[kCombThreads];
+  __shared__ float4 wacc[kCombWarps][32];
+  __shared__ float wm[kCombWarps], wl[kCombWarps];
   const Geo& g = a.g;
   const int row = blockIdx.x;               // tok * Hq + h
   const int tok = row / g.Hq, h = row % g.Hq;
@@ -235,49 +225,83 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) 
   const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / g.Hkv;
   const int it0 = rd->item0[s] + kvh * nsplit;
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
-  float M = -INFINITY;
-  for (int sp = threadIdx.x; sp < nsplit; sp += kCombThreads) M = fmaxf(M, __ldcg(ml + (long)(it0 + sp) * R + r).x);
-  M = block_reduce(M, true, red);
-
-  const int lpp = g.d / 4, spw = 32 / lpp, step = (kCombThreads / 32) * spw;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane / lpp, d4 = lane % lpp;
   const float4* po = reinterpret_cast<const float4*>(a.part_o);
+  const int lpp = g.d / 4;                  // float4 lanes of a row (16 or 32)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int spw = 32 / lpp;                 // split rows a warp covers at once (1 or 2)
+  const int sub = lane / lpp, d4 = lane % lpp;
+  const int stride = kCombWarps * spw;      // splits per depth step
+  float m_t = -INFINITY, den = 0.f;         // this thread's running max and weighted sum of l
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-  for (int base = warp * spw + sub; base < nsplit; base += 4 * step) {
-    float4 o[4];
-    float2 m[4];
+  for (int base = warp * spw + sub; base < nsplit; base += kCombDepth * stride) {
+    float4 o[kCombDepth];
+    float2 m[kCombDepth];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int sp = base + k * step;
+    for (int k = 0; k < kCombDepth; ++k) {
+      const int sp = base + k * stride;
       const long pr = (long)(it0 + sp) * R + r;
       o[k] = sp < nsplit ? __ldcg(po + pr * lpp + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
       m[k] = sp < nsplit ? __ldcg(ml + pr) : make_float2(-INFINITY, 0.f);
     }
+    float mx = m_t;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float w = exp2f(m[k].x - M);
+    for (int k = 0; k < kCombDepth; ++k) mx = fmaxf(mx, m[k].x);
+    if (mx == -INFINITY) continue;
+    const float sc = exp2f(m_t - mx);       // 0 while m_t is still -inf
+    acc.x *= sc;
+    acc.y *= sc;
+    acc.z *= sc;
+    acc.w *= sc;
+    den *= sc;
+#pragma unroll
+    for (int k = 0; k < kCombDepth; ++k) {
+      const float w = exp2f(m[k].x - mx);   // 0 for a missing split
       acc.x += w * o[k].x;
       acc.y += w * o[k].y;
       acc.z += w * o[k].z;
       acc.w += w * o[k].w;
-      if (d4 == 0) den += w * m[k].y;
+      den += w * m[k].y;
     }
+    m_t = mx;
   }
-  den = block_reduce(den, false, red);
-  part[threadIdx.x] = acc;
+  // merge the sub-rows of a warp (spw = 2: lanes l and l + 16), then the warps
+  if (spw == 2) {
+    const float mo = __shfl_xor_sync(0xffffffffu, m_t, 16);
+    const float mx = fmaxf(m_t, mo);
+    const float sa = mx == -INFINITY ? 0.f : exp2f(m_t - mx), sb = mx == -INFINITY ? 0.f : exp2f(mo - mx);
+    float4 ob;
+    ob.x = __shfl_xor_sync(0xffffffffu, acc.x, 16);
+    ob.y = __shfl_xor_sync(0xffffffffu, acc.y, 16);
+    ob.z = __shfl_xor_sync(0xffffffffu, acc.z, 16);
+    ob.w = __shfl_xor_sync(0xffffffffu, acc.w, 16);
+    const float db = __shfl_xor_sync(0xffffffffu, den, 16);
+    acc = make_float4(sa * acc.x + sb * ob.x, sa * acc.y + sb * ob.y, sa * acc.z + sb * ob.z, sa * acc.w + sb * ob.w);
+    den = sa * den + sb * db;
+    m_t = mx;
+  }
+  if (lane < lpp) wacc[warp][lane] = acc;
+  if (lane == 0) {
+    wm[warp] = m_t;
+    wl[warp] = den;
+  }
   __syncthreads();
   if (threadIdx.x < lpp) {
-    float4 t = part[threadIdx.x];
-    for (int j = 1; j < step; ++j) {
-      const float4 u = part[j * lpp + threadIdx.x];
-      t.x += u.x;
-      t.y += u.y;
-      t.z += u.z;
-      t.w += u.w;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kCombWarps; ++w) M = fmaxf(M, wm[w]);
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombWarps; ++w) {
+      const float sc = wm[w] == -INFINITY ? 0.f : exp2f(wm[w] - M);
+      const float4 u = wacc[w][threadIdx.x];
+      t.x += sc * u.x;
+      t.y += sc * u.y;
+      t.z += sc * u.z;
+      t.w += sc * u.w;
+      l += sc * wl[w];
     }
-    const float inv = 1.f / den;
+    const float inv = 1.f / l;
     const long idx = (long)tok * a.op_ld + h * g.d + 4 * threadIdx.x;
     put_operand(a.op, idx + 0, a.op_plane, t.x * inv, a.op_kind);
     put_operand(a.op, idx + 1, a.op_plane, t.y * inv, a.op_kind);
