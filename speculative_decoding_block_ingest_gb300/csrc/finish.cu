@@ -183,13 +183,19 @@ __global__ void __launch_bounds__(128) qk_finish_kernel(FinishArgs f) {
   trace_cta_exit(f.trace);
 }
 
+// One float4 of act per thread: a single round trip, no loop.
 __global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
   trace_cta_entry(f.trace);
   pdl_launch_dependents();
   pdl_wait();
   const Geo& g = f.g;
   const long n4 = (long)f.n_tok * g.I / 4;
-  for (long k = (long)blockIdx.x * blockDim.x + threadIdx.x; k < n4; k += (long)gridDim.x * blockDim.x) {
+  {
+    const long k = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= n4) {
+      trace_cta_exit(f.trace);
+      return;
+    }
     const long e = k * 4;
     const int tok = (int)(e / g.I), j = (int)(e % g.I);
     float* gp = f.acc + (long)tok * 2 * g.I + (j / 64) * 128 + (j % 64);
@@ -360,8 +366,9 @@ void launch_qk_finish(const FinishArgs& f, cudaStream_t s) {
 }
 
 int swiglu_grid(const FinishArgs& f, int n_sm) {
+  (void)n_sm;
   const long n4 = (long)f.n_tok * f.g.I / 4;
-  return (int)std::min<long>((n4 + 127) / 128, 4L * n_sm);
+  return (int)((n4 + 127) / 128);
 }
 
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s) {

@@ -110,6 +110,7 @@ struct AttnArgs {
   long op_plane;
   int op_kind;             // operand kind (OpKind)
   float scale_log2;     // log2(e)/sqrt(d): scores and the saved max are in log2 units
+  int comb_wpr;         // merge: warps per merged row (attn_combine_wpr of the largest split count)
   unsigned long long* trace;   // optional per-CTA timestamps [items][kTraceWords], or null
   int* err;
   Geo g;
@@ -192,6 +193,7 @@ int qk_finish_grid(const FinishArgs& f);
 int swiglu_grid(const FinishArgs& f, int n_sm);
 int conv_grid(const ConvArgs& c, int n_sm);
 int attn_combine_grid(const AttnArgs& a, int n_tok);
+int attn_combine_wpr(int max_split);
 int init_grid(const InitArgs& a);
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s);
 const void* init_kernel_entry();       // kernel function addresses, to find

@@ -199,73 +199,80 @@ void launch_attention_simt(const AttnArgs& a, int n_items, cudaStream_t s) {
   launch_pdl(attn_simt_kernel, dim3(n_items), dim3(128), smem, s, a);
 }
 
-// Merge the split-KV partials of one (token, q head) row into the O-proj
-// operand.  One pass: warp w takes splits w, w + 8, ..., eight deep per
-// thread, every (m, l) pair and partial-row load of a pass issued before the
-// first use (d/4 lanes per split row); each thread merges its splits online
-// against its own running maximum, and one exchange through shared memory
-// merges the eight warps -- a single L2 round trip per pass.
+// Merge the split-KV partials of (token, q head) rows into the O-proj
+// operand.  Each row gets comb_wpr warps (1, 2, 4 or 8: enough for its
+// splits) and a CTA of eight warps takes 8 / comb_wpr rows.  One pass: warp w
+// of a row takes splits w, w + comb_wpr, ..., eight deep per thread, every
+// (m, l) pair and partial-row load of a pass issued before the first use
+// (d/4 lanes per split row); each thread merges its splits online against its
+// own running maximum, and one exchange through shared memory merges the
+// row's warps -- a single L2 round trip per pass.
 constexpr int kCombThreads = 256;
 constexpr int kCombWarps = kCombThreads / 32;
 constexpr int kCombDepth = 8;
 
-__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) {
+__global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a, int n_rows) {
   trace_cta_entry(a.trace);
   pdl_launch_dependents();
   pdl_wait();
   __shared__ float4 wacc[kCombWarps][32];
   __shared__ float wm[kCombWarps], wl[kCombWarps];
   const Geo& g = a.g;
-  const int row = blockIdx.x;               // tok * Hq + h
-  const int tok = row / g.Hq, h = row % g.Hq;
-  const int s = tok / kBlock, i = tok % kBlock;
-  const int kvh = h / g.G, hl = h % g.G;
-  const int R = g.G * kBlock, r = i * g.G + hl;
-  const RoundDesc* rd = a.rd;
-  const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / g.Hkv;
-  const int it0 = rd->item0[s] + kvh * nsplit;
-  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
-  const float4* po = reinterpret_cast<const float4*>(a.part_o);
-  const int lpp = g.d / 4;                  // float4 lanes of a row (16 or 32)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int spw = 32 / lpp;                 // split rows a warp covers at once (1 or 2)
-  const int sub = lane / lpp, d4 = lane % lpp;
-  const int stride = kCombWarps * spw;      // splits per depth step
+  const int wpr = a.comb_wpr, rpc = kCombWarps / wpr;
+  const int row = blockIdx.x * rpc + warp / wpr, wr = warp % wpr;   // tok * Hq + h; warp of the row
+  const int lpp = g.d / 4;                  // float4 lanes of a row (16 or 32)
   float m_t = -INFINITY, den = 0.f;         // this thread's running max and weighted sum of l
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = warp * spw + sub; base < nsplit; base += kCombDepth * stride) {
-    float4 o[kCombDepth];
-    float2 m[kCombDepth];
+  int tok = 0, h = 0;
+  if (row < n_rows) {
+    tok = row / g.Hq;
+    h = row % g.Hq;
+    const int s = tok / kBlock, i = tok % kBlock;
+    const int kvh = h / g.G, hl = h % g.G;
+    const int R = g.G * kBlock, r = i * g.G + hl;
+    const RoundDesc* rd = a.rd;
+    const int nsplit = (rd->item0[s + 1] - rd->item0[s]) / g.Hkv;
+    const int it0 = rd->item0[s] + kvh * nsplit;
+    const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
+    const float4* po = reinterpret_cast<const float4*>(a.part_o);
+    const int spw = 32 / lpp;               // split rows a warp covers at once (1 or 2)
+    const int sub = lane / lpp, d4 = lane % lpp;
+    const int stride = wpr * spw;           // splits per depth step
+    for (int base = wr * spw + sub; base < nsplit; base += kCombDepth * stride) {
+      float4 o[kCombDepth];
+      float2 m[kCombDepth];
 #pragma unroll
-    for (int k = 0; k < kCombDepth; ++k) {
-      const int sp = base + k * stride;
-      const long pr = (long)(it0 + sp) * R + r;
-      o[k] = sp < nsplit ? __ldcg(po + pr * lpp + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
-      m[k] = sp < nsplit ? __ldcg(ml + pr) : make_float2(-INFINITY, 0.f);
+      for (int k = 0; k < kCombDepth; ++k) {
+        const int sp = base + k * stride;
+        const long pr = (long)(it0 + sp) * R + r;
+        o[k] = sp < nsplit ? __ldcg(po + pr * lpp + d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        m[k] = sp < nsplit ? __ldcg(ml + pr) : make_float2(-INFINITY, 0.f);
+      }
+      float mx = m_t;
+#pragma unroll
+      for (int k = 0; k < kCombDepth; ++k) mx = fmaxf(mx, m[k].x);
+      if (mx == -INFINITY) continue;
+      const float sc = exp2f(m_t - mx);     // 0 while m_t is still -inf
+      acc.x *= sc;
+      acc.y *= sc;
+      acc.z *= sc;
+      acc.w *= sc;
+      den *= sc;
+#pragma unroll
+      for (int k = 0; k < kCombDepth; ++k) {
+        const float w = exp2f(m[k].x - mx);   // 0 for a missing split
+        acc.x += w * o[k].x;
+        acc.y += w * o[k].y;
+        acc.z += w * o[k].z;
+        acc.w += w * o[k].w;
+        den += w * m[k].y;
+      }
+      m_t = mx;
     }
-    float mx = m_t;
-#pragma unroll
-    for (int k = 0; k < kCombDepth; ++k) mx = fmaxf(mx, m[k].x);
-    if (mx == -INFINITY) continue;
-    const float sc = exp2f(m_t - mx);       // 0 while m_t is still -inf
-    acc.x *= sc;
-    acc.y *= sc;
-    acc.z *= sc;
-    acc.w *= sc;
-    den *= sc;
-#pragma unroll
-    for (int k = 0; k < kCombDepth; ++k) {
-      const float w = exp2f(m[k].x - mx);   // 0 for a missing split
-      acc.x += w * o[k].x;
-      acc.y += w * o[k].y;
-      acc.z += w * o[k].z;
-      acc.w += w * o[k].w;
-      den += w * m[k].y;
-    }
-    m_t = mx;
   }
-  // merge the sub-rows of a warp (spw = 2: lanes l and l + 16), then the warps
-  if (spw == 2) {
+  // merge the sub-rows of a warp (d = 64: lanes l and l + 16), then the row's warps
+  if (lpp == 16) {
     const float mo = __shfl_xor_sync(0xffffffffu, m_t, 16);
     const float mx = fmaxf(m_t, mo);
     const float sa = mx == -INFINITY ? 0.f : exp2f(m_t - mx), sb = mx == -INFINITY ? 0.f : exp2f(mo - mx);
@@ -285,16 +292,14 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) 
     wl[warp] = den;
   }
   __syncthreads();
-  if (threadIdx.x < lpp) {
+  if (row < n_rows && wr == 0 && lane < lpp) {
     float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kCombWarps; ++w) M = fmaxf(M, wm[w]);
+    for (int w = warp; w < warp + wpr; ++w) M = fmaxf(M, wm[w]);
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCombWarps; ++w) {
+    for (int w = warp; w < warp + wpr; ++w) {
       const float sc = wm[w] == -INFINITY ? 0.f : exp2f(wm[w] - M);
-      const float4 u = wacc[w][threadIdx.x];
+      const float4 u = wacc[w][lane];
       t.x += sc * u.x;
       t.y += sc * u.y;
       t.z += sc * u.z;
@@ -302,7 +307,7 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) 
       l += sc * wl[w];
     }
     const float inv = 1.f / l;
-    const long idx = (long)tok * a.op_ld + h * g.d + 4 * threadIdx.x;
+    const long idx = (long)tok * a.op_ld + h * g.d + 4 * lane;
     put_operand(a.op, idx + 0, a.op_plane, t.x * inv, a.op_kind);
     put_operand(a.op, idx + 1, a.op_plane, t.y * inv, a.op_kind);
     put_operand(a.op, idx + 2, a.op_plane, t.z * inv, a.op_kind);
@@ -311,10 +316,21 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a) 
   trace_cta_exit(a.trace);
 }
 
-int attn_combine_grid(const AttnArgs& a, int n_tok) { return n_tok * a.g.Hq; }
+// Warps per merged row for splits of up to max_split partials each: one warp
+// covers eight splits a pass (d = 128; sixteen at d = 64).
+int attn_combine_wpr(int max_split) {
+  int w = 1;
+  while (w < kCombWarps && 8 * w < max_split) w *= 2;
+  return w;
+}
+
+int attn_combine_grid(const AttnArgs& a, int n_tok) {
+  const int rpc = kCombWarps / a.comb_wpr;
+  return (n_tok * a.g.Hq + rpc - 1) / rpc;
+}
 
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s) {
-  launch_pdl(attn_combine_kernel, dim3(attn_combine_grid(a, n_tok)), dim3(kCombThreads), 0, s, a);
+  launch_pdl(attn_combine_kernel, dim3(attn_combine_grid(a, n_tok)), dim3(kCombThreads), 0, s, a, n_tok * a.g.Hq);
 }
 
 // ------------------------------------------------------------------ per-call init
