@@ -1,0 +1,249 @@
+// gemm_tt.cu -- token-tiled projection for rounds of many block rows.
+//
+// The weight-streaming projection (gemm_tc.cu) puts the weights on the MMA's
+// M side and the few drafted rows on N; past 64 rows its operand planes
+// outweigh the weights four to one per unit and the stages no longer fit
+// shared memory deeply enough to stream.  Here the roles follow the data: a
+// tile is 128 token rows (M, the operand's hi and lo bf16 planes as two A
+// operands, loaded by TMA) by 256 output features (N, the two stacked 16 KB
+// weight blocks of two 128-row tiles as B), accumulated over K in TMEM.
+// Stream-K runs over units (token tile, feature tile, 64-column K step), K
+// innermost, feature tile outermost, so that CTAs working on the same
+// feature tile at once share its weights through L2 and every weight byte
+// comes from HBM once per projection.  One CTA of six warps per SM:
+//   warp 0 (one lane)  producer: per unit the two weight blocks (bulk copies,
+//                      the first stages before the programmatic-launch wait)
+//                      and the unit's 128 x 64 hi and lo operand boxes (TMA);
+//   warp 1 (one lane)  MMA issuer: 4 K-steps x (hi, lo) tcgen05.mma of
+//                      M = 128, N = 256 into one of two TMEM accumulators
+//                      (256 columns each);
+//   warps 2..5         drain: each warp reads its 32 token rows out of TMEM
+//                      32 features at a time, turns the 32 x 32 block through
+//                      shared memory and red.adds it a row at a time, so
+//                      every warp-wide red.add covers 128 contiguous bytes
+//                      (one L2 line) instead of 32 rows' scattered words.
+#include <algorithm>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace dfl {
+
+namespace {
+
+constexpr int kTtThreads = 192;          // warps: 0 producer, 1 issuer, 2..5 drain
+constexpr int kTtM = 128;                // token rows per tile
+constexpr int kTtN = 2 * kTileN;         // output features per tile
+constexpr int kTtABytes = kTtM * kTileK * 2;            // one operand plane box: 16 KB
+constexpr int kTtBBytes = 2 * kTileN * kTileK * 2;      // two weight blocks: 32 KB
+constexpr int kTtStageBytes = 2 * kTtABytes + kTtBBytes;   // 64 KB
+constexpr int kTtStages = 3;
+constexpr int kTtCtlBytes = 512;
+constexpr int kTtTurnFloats = 32 * 33;   // a drain warp's 32 x 32 block, rows padded against bank conflicts
+
+struct TtCfg {
+  int n_tt, n_ft;      // token tiles, feature tiles
+  uint32_t idesc;
+};
+
+__global__ void __launch_bounds__(kTtThreads, 1)
+    gemm_tt_kernel(const __grid_constant__ CUtensorMap tmX, GemmArgs a, TtCfg t) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ctl = smem + kTtStages * kTtStageBytes;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl);
+  volatile int* flags = reinterpret_cast<volatile int*>(ctl + 16);   // abort
+  uint64_t* full = reinterpret_cast<uint64_t*>(ctl + 32);
+  uint64_t* empty = full + kTtStages;
+  uint64_t* accfull = empty + kTtStages;    // [2]
+  uint64_t* accempty = accfull + 2;         // [2]
+  float* turn = reinterpret_cast<float*>(ctl + kTtCtlBytes);   // [4 drain warps][kTtTurnFloats]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned long long c0 = 0;
+  if (threadIdx.x == 0) trace_entry(a.trace, blockIdx.x, &c0);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTtStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accfull[b], 1);
+      mbar_init(&accempty[b], kEpiThreads);
+    }
+    flags[0] = 0;
+    fence_barrier_init();
+    tma_prefetch_map(&tmX);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncwarp();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const Part p = a.p;          // p.kb K steps per tile; tiles ordered (feature tile, token tile)
+  const int u0 = p.start(blockIdx.x), u1 = p.start(blockIdx.x + 1);
+  const int n_units = u1 - u0;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- producer
+      const uint8_t* W = static_cast<const uint8_t*>(a.W);
+      auto load_w = [&](int u, uint8_t* st, uint64_t* bar) {
+        const int tile = u / p.kb, k = u % p.kb, ft = tile / t.n_tt;
+        const size_t blk = (size_t)(2 * ft) * p.kb + k;   // block (2 ft, k), then (2 ft + 1, k)
+        bulk_load(st + 2 * kTtABytes, W + blk * (kTtBBytes / 2), kTtBBytes / 2, bar);
+        bulk_load(st + 2 * kTtABytes + kTtBBytes / 2, W + (blk + p.kb) * (kTtBBytes / 2), kTtBBytes / 2, bar);
+      };
+      auto load_x = [&](int u, uint8_t* st, uint64_t* bar) {
+        const int tile = u / p.kb, k = u % p.kb, tt = tile % t.n_tt;
+        const int y = a.e.tok_base + tt * kTtM;
+        tma_load_2d(st, &tmX, bar, k * kTileK, y);                          // hi plane rows
+        tma_load_2d(st + kTtABytes, &tmX, bar, k * kTileK, a.e.g.Mt + y);   // lo plane rows
+      };
+      const int pre = min(n_units, kTtStages);
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], kTtStageBytes);
+        load_w(u0 + i, smem + i * kTtStageBytes, &full[i]);
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      trace_mark(a.trace, blockIdx.x, 2, c0);               // 2: producer past the launch wait
+      for (int i = 0; i < pre; ++i) load_x(u0 + i, smem + i * kTtStageBytes, &full[i]);
+      int st = 0;
+      uint32_t ph = 0;
+      for (int i = pre; i < n_units; ++i) {
+        if (!mbar_wait(&empty[st], ph, &flags[0])) {
+          flags[0] = 1;
+          break;
+        }
+        uint8_t* sp = smem + st * kTtStageBytes;
+        mbar_arrive_expect_tx(&full[st], kTtStageBytes);
+        load_w(u0 + i, sp, &full[st]);
+        load_x(u0 + i, sp, &full[st]);
+        if (++st == kTtStages) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------------------------------------------------------- MMA issuer
+      const uint64_t d0 = desc_sw128(smem_u32(smem));
+      constexpr uint32_t dstage = (uint32_t)kTtStageBytes >> 4;
+      constexpr uint32_t lo = (uint32_t)kTtABytes >> 4;
+      constexpr uint32_t wo = (uint32_t)(2 * kTtABytes) >> 4;
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      int seg = 0;
+      for (int u = u0; u < u1 && ok; ++seg) {
+        const int seg_end = min(u1, (u / p.kb + 1) * p.kb);
+        const int b = seg & 1, use = seg >> 1;
+        if (!mbar_wait(&accempty[b], (use & 1) ^ 1, &flags[0])) {
+          flags[0] = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(b * kTtN);
+        for (int k = 0; u < seg_end; ++u, ++k) {
+          if (!mbar_wait(&full[st], ph, &flags[0])) {
+            flags[0] = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ds = d0 + (uint64_t)(st * dstage);
+#pragma unroll
+          for (uint32_t kk = 0; kk < 8; kk += 2) {
+            mma_bf16(d_tmem, ds + kk, ds + wo + kk, t.idesc, (k > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(d_tmem, ds + lo + kk, ds + wo + kk, t.idesc, 1u);
+          }
+          mma_commit(&empty[st]);
+          if (++st == kTtStages) {
+            st = 0;
+            ph ^= 1;
+          }
+        }
+        if (ok) mma_commit(&accfull[b]);
+      }
+      trace_mark(a.trace, blockIdx.x, 3, c0);                   // 3: last MMA issued
+    }
+  } else {
+    // ------------------------------------------------------------------ drain
+    pdl_wait();
+    const int q = warp & 3;                 // TMEM lane quarter this warp may read
+    int seg = 0;
+    for (int u = u0; u < u1; ++seg) {
+      const int tile = u / p.kb;
+      const int seg_end = min(u1, (tile + 1) * p.kb);
+      const int b = seg & 1, use = seg >> 1;
+      const int ft = tile / t.n_tt, tt = tile % t.n_tt;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(&accfull[b], use & 1, &flags[0]));
+      if (!got) flags[0] = 1;
+      __syncwarp();
+      tc_fence_after();
+      if (got) {
+        const uint32_t base = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * kTtN);
+        float* tb = turn + (warp - 2) * kTtTurnFloats;
+        const int tok0 = tt * kTtM + 32 * q;                 // the warp's first token row (within the pass)
+        const int rows = min(32, a.e.n_tok - tok0);          // its rows that exist
+        float* dst0 = a.dst + (long)(a.e.tok_base + tok0) * a.dst_ld + ft * kTtN + lane;
+        for (int j0 = 0; j0 < kTtN; j0 += 32) {
+          float v[32];
+          tmem_ld32(base + (uint32_t)j0, v);                 // warp-wide: lane = row, v = 32 features
+#pragma unroll
+          for (int j = 0; j < 32; ++j) tb[lane * 33 + j] = v[j];
+          __syncwarp();
+          for (int r = 0; r < rows; ++r)                     // lane = feature j0 + lane of row r
+            asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst0 + (long)r * a.dst_ld + j0), "f"(tb[r * 33 + lane])
+                         : "memory");
+          __syncwarp();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&accempty[b]);
+      u = seg_end;
+    }
+  }
+  __syncwarp();
+  __syncthreads();
+  if (threadIdx.x == 0) trace_exit(a.trace, blockIdx.x);
+  if (flags[0] && threadIdx.x == 0) atomicExch(a.e.err, DERR_TIMEOUT);
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+
+bool gemm_tt_fits(const GemmArgs& a) {
+  return !a.w8 && a.omode == O_RED && a.N % kTtN == 0 && a.K % kTileK == 0 && a.e.n_tok > 64;
+}
+
+int gemm_tt_units(const GemmArgs& a) {
+  const int n_tt = (a.e.n_tok + kTtM - 1) / kTtM;
+  return n_tt * (a.N / kTtN) * (a.K / kTileK);
+}
+
+void launch_gemm_tt(const GemmArgs& a, const void* tmap_x_tall, cudaStream_t s) {
+  TtCfg t{};
+  t.n_tt = (a.e.n_tok + kTtM - 1) / kTtM;
+  t.n_ft = a.N / kTtN;
+  t.idesc = idesc_bf16(kTtM, kTtN);
+  const size_t smem = (size_t)kTtStages * kTtStageBytes + kTtCtlBytes + 4 * kTtTurnFloats * 4 + 1024;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(gemm_tt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return;   // the launch below is skipped; the caller's cudaGetLastError reports it
+    attr = true;
+  }
+  launch_pdl(gemm_tt_kernel, dim3(a.p.grid), dim3(kTtThreads), smem, s, *static_cast<const CUtensorMap*>(tmap_x_tall),
+             a, t);
+}
+
+}  // namespace dfl

@@ -486,6 +486,34 @@ struct GemmSpec {
 void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
   const Geo& g = h->g;
   const int n_all = sp.e.n_tok;
+  if (h->use_tc && 2 * h->lo.Mt >= 256) {
+    // more than 64 rows into a red.add destination: one token-tiled launch
+    // over every row (weights streamed once)
+    GemmArgs a{};
+    a.W = sp.W;
+    a.w8 = sp.wscale != nullptr;
+    a.N = sp.N;
+    a.K = sp.K;
+    a.omode = sp.omode;
+    a.dst = sp.dst;
+    a.dst_ld = sp.dst_ld;
+    a.e = sp.e;
+    a.e.wscale = sp.wscale;
+    a.e.tok_base = 0;
+    a.e.n_tok = n_all;
+    if (gemm_tt_fits(a)) {
+      a.n_tiles = sp.N / kTileN;
+      a.p.kb = sp.K / kTileK;
+      a.p.units = gemm_tt_units(a);
+      a.p.grid = std::min(a.p.units, h->n_sm);
+      const double bytes = (double)sp.N * sp.K * 2 + (double)n_all * sp.K * 4 + (double)n_all * sp.N * 4;
+      Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
+      a.trace = trace_slot(h, DFLASH_KERNEL_GEMM, a.p.grid);
+      launch_gemm_tt(a, &sp.xmap[1], s);
+      ck(cudaGetLastError(), "token-tiled gemm launch");
+      return;
+    }
+  }
   for (int base = 0; base < n_all; base += kPassTok) {
     GemmArgs a{};
     a.W = sp.W;
