@@ -19,9 +19,9 @@
 //                      (256 columns each);
 //   warps 2..5         drain: each warp reads its 32 token rows out of TMEM
 //                      32 features at a time, turns the 32 x 32 block through
-//                      shared memory and red.adds it a row at a time, so
-//                      every warp-wide red.add covers 128 contiguous bytes
-//                      (one L2 line) instead of 32 rows' scattered words.
+//                      shared memory and red.adds it as 16-byte vectors, four
+//                      rows' 128 contiguous bytes per warp instruction
+//                      instead of 32 rows' scattered words.
 #include <algorithm>
 
 #include "kernels.cuh"
@@ -190,16 +190,22 @@ __global__ void __launch_bounds__(kTtThreads, 1)
         float* tb = turn + (warp - 2) * kTtTurnFloats;
         const int tok0 = tt * kTtM + 32 * q;                 // the warp's first token row (within the pass)
         const int rows = min(32, a.e.n_tok - tok0);          // its rows that exist
-        float* dst0 = a.dst + (long)(a.e.tok_base + tok0) * a.dst_ld + ft * kTtN + lane;
+        // lane l adds features 4 (l % 8) .. + 3 of row r + l / 8 as one
+        // 16-byte red.add: a warp instruction covers four rows' 128 bytes
+        const int rl = lane >> 3, c4 = 4 * (lane & 7);
+        float* dst0 = a.dst + (long)(a.e.tok_base + tok0 + rl) * a.dst_ld + ft * kTtN + c4;
         for (int j0 = 0; j0 < kTtN; j0 += 32) {
           float v[32];
           tmem_ld32(base + (uint32_t)j0, v);                 // warp-wide: lane = row, v = 32 features
 #pragma unroll
           for (int j = 0; j < 32; ++j) tb[lane * 33 + j] = v[j];
           __syncwarp();
-          for (int r = 0; r < rows; ++r)                     // lane = feature j0 + lane of row r
-            asm volatile("red.global.add.f32 [%0], %1;" ::"l"(dst0 + (long)r * a.dst_ld + j0), "f"(tb[r * 33 + lane])
+          for (int r = 0; r + rl < rows; r += 4) {
+            const float* src = tb + (r + rl) * 33 + c4;
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst0 + (long)r * a.dst_ld + j0),
+                         "f"(src[0]), "f"(src[1]), "f"(src[2]), "f"(src[3])
                          : "memory");
+          }
           __syncwarp();
         }
       }
