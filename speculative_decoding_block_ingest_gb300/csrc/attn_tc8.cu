@@ -13,8 +13,8 @@
 //                      [d x 64 B] and the page's K and V scales into a ring
 //                      of raw chunk stages (the first ones before the
 //                      programmatic-launch wait);
-//   warps 10, 11       converters, per chunk: K codes -> f16 (exact: every
-//                      e4m3 value is an f16 value) into the chunk's K
+//   warps 10, 11       converters, per chunk: K codes -> f16 times 2^-8
+//                      (exact, by integer operations) into the chunk's K
 //                      operand, the chunk's K scales into one of three small
 //                      buffers;
 //   warp 1 (one lane)  tcgen05.mma: S = Q K^T into one of two TMEM buffers,
@@ -64,12 +64,12 @@ constexpr int kA8Ksc = 2 * kPage * 4;      // K scales of one chunk (bytes)
 constexpr int kA8Chunk = 2 * kPage;
 constexpr float kA8RescaleLog2 = 8.f;
 
-// Two e4m3 codes (low byte first) times their scales, each product in f32
-// (exact: 4 + 24 significant bits) rounded once to f16.
-__device__ __forceinline__ uint32_t scaled_f16x2(uint32_t codes, float s0, float s1) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)codes, __NV_E4M3);
-  const float2 f = __half22float2(__half2(h));
-  const __half2 r = __floats2half2_rn(f.x * s0, f.y * s1);
+// Two codes widened to f16 times 2^-8 (e4m3x2_to_f16x2_scaled, integer
+// operations) times their scales times 2^8, each product in f32 (exact: 4 +
+// 24 significant bits; the powers of two cancel exactly) rounded once to f16.
+__device__ __forceinline__ uint32_t scaled_f16x2(uint32_t widened, float s0x256, float s1x256) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&widened));
+  const __half2 r = __floats2half2_rn(f.x * s0x256, f.y * s1x256);
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
@@ -241,8 +241,10 @@ __global__ void __launch_bounds__(kA8Threads, 1)
       // (page w, key rr, 16-code piece j): K operand row r = 64 w + rr, atom
       // j / 4, f16 pieces 2 (j % 4), +1.
       if (ok) {
+        // (the K operand holds the codes' values times 2^-8: the scales
+        // carry 2^8, exactly)
         float* ksc = sKsc + (c % 3) * (2 * kPage);
-        for (int i = ct; i < 2 * kPage; i += kA8CvThreads) ksc[i] = ssc[i];
+        for (int i = ct; i < 2 * kPage; i += kA8CvThreads) ksc[i] = ssc[i] * kW8Unscale;
         // four items in flight per thread (their loads and conversions
         // overlap; one at a time the chain is latency-bound)
 #pragma unroll 4
@@ -253,10 +255,9 @@ __global__ void __launch_bounds__(kA8Threads, 1)
           uint32_t hv[8];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(sw[i] & 0xFFFFu), __NV_E4M3);
-            const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(sw[i] >> 16), __NV_E4M3);
-            hv[2 * i] = (uint32_t)lo.x | ((uint32_t)lo.y << 16);
-            hv[2 * i + 1] = (uint32_t)hi.x | ((uint32_t)hi.y << 16);
+            const uint2 f4 = e4m3x4_to_f16x4_scaled(sw[i]);   // exact, times 2^-8
+            hv[2 * i] = f4.x;
+            hv[2 * i + 1] = f4.y;
           }
           const int r = w * kPage + rr, cc = 2 * (j & 3);
           uint8_t* drow = sK16 + (j >> 2) * kA8Atom + r * 128;
@@ -367,8 +368,9 @@ __global__ void __launch_bounds__(kA8Threads, 1)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const float4 sv4 = svp[i];   // scales of keys 4i .. 4i+3 of the piece
-              hv[2 * i] = scaled_f16x2(sw[i] & 0xFFFFu, sv4.x, sv4.y);
-              hv[2 * i + 1] = scaled_f16x2(sw[i] >> 16, sv4.z, sv4.w);
+              const uint2 f4 = e4m3x4_to_f16x4_scaled(sw[i]);
+              hv[2 * i] = scaled_f16x2(f4.x, sv4.x * kW8Unscale, sv4.y * kW8Unscale);
+              hv[2 * i + 1] = scaled_f16x2(f4.y, sv4.z * kW8Unscale, sv4.w * kW8Unscale);
             }
             uint8_t* drow = vdst + w * kA8V16Page + row * 128;
             *reinterpret_cast<uint4*>(drow + (((2 * pc) ^ (row & 7)) << 4)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);

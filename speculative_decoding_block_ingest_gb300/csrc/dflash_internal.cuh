@@ -37,9 +37,27 @@ constexpr int kMaxPtUpdates = 160;
 constexpr int kEpiThreads = 128;  // threads running a tile epilogue
 constexpr int kEpiTokChunk = 32;  // tokens per epilogue pass
 constexpr int kEpiBar = 1;        // named barrier id used by the epilogue
-// e4m3 weights reach the tensor cores as f16 values scaled by 2^-8 (the
-// projection widens the codes with integer operations); the row scales,
-// multiplied by this, undo it exactly.
+// Two e4m3 codes, in bytes 0 and 2 of t (bytes 1 and 3 zero), as two f16
+// values scaled by 2^-8 (low half first).  For a code b = s eeee mmm the f16
+// pattern s 0 eeee mmm 0000000 (b << 7 with the sign moved up one bit, i.e.
+// (b + (b & 0x80)) << 7) has exponent field e against f16's bias 15 instead
+// of e4m3's 7 and the same mantissa, so it is the value times 2^-8 for the
+// normal codes, and for the subnormal ones (e = 0) both formats scale the
+// mantissa alike.  Exact for every finite code (neither the weights nor the
+// cache ever hold a NaN code).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t t) {
+  return (t + (t & 0x00800080u)) << 7;
+}
+
+// Codes (b0 b1 b2 b3) of a word as the f16 pairs (b0, b1) and (b2, b3),
+// scaled by 2^-8 (integer operations only).
+__device__ __forceinline__ uint2 e4m3x4_to_f16x4_scaled(uint32_t w) {
+  return make_uint2(e4m3x2_to_f16x2_scaled(__byte_perm(w, 0u, 0x4140)), e4m3x2_to_f16x2_scaled(__byte_perm(w, 0u, 0x4342)));
+}
+
+// e4m3 weights and cached K/V reach the tensor cores as f16 values scaled by
+// 2^-8 (the kernels widen the codes with integer operations); the row
+// scales, multiplied by this, undo it exactly.
 constexpr float kW8Unscale = 256.f;
 constexpr int kRedFloats = kEpiTokChunk * (kTileN + 1) + kEpiTokChunk;   // epilogue shared scratch
 

@@ -57,18 +57,6 @@ struct TcCfg {
   uint32_t idesc;
 };
 
-// Two e4m3 codes, in bytes 0 and 2 of t (bytes 1 and 3 zero), as two f16
-// values scaled by 2^-8 (low half first).  For a code b = s eeee mmm the f16
-// pattern s 0 eeee mmm 0000000 (b << 7 with the sign moved up one bit, i.e.
-// (b + (b & 0x80)) << 7) has exponent field e against f16's bias 15 instead
-// of e4m3's 7 and the same mantissa, so it is the value times 2^-8 for the
-// normal codes, and for the subnormal ones (e = 0) both formats scale the
-// mantissa alike.  Exact for every finite code (the projections' weights have
-// no NaN codes).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t t) {
-  return (t + (t & 0x00800080u)) << 7;
-}
-
 constexpr int kTcThreads = 224;   // warps: 0 producer, 1..2 MMA issuers, 3..6 drain
 constexpr int kDrainTid0 = 96;    // first drain thread (warp 3)
 constexpr int kConvTid0 = 224;    // w8: first converter thread (warps 7..14)
