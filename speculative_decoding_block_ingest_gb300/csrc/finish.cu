@@ -211,21 +211,6 @@ __global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
   trace_cta_exit(f.trace);
 }
 
-// A one-CTA link in the programmatic-launch chain: it lets its dependent
-// launch at once and completes when its own predecessor has.  Placed after a
-// kernel whose CTAs hold most SMs, so that the next kernel's CTAs take SMs as
-// they free instead of queueing on that kernel's completion.
-__global__ void relay_kernel(unsigned long long* trace) {
-  trace_cta_entry(trace);
-  pdl_launch_dependents();
-  pdl_wait();
-  trace_cta_exit(trace);
-}
-
-void launch_relay(unsigned long long* trace, cudaStream_t s) {
-  launch_pdl(relay_kernel, dim3(1), dim3(32), 0, s, trace);
-}
-
 // f32 rows -> hi/lo bf16 operand planes (no norm): the lm_head's operand.
 __global__ void __launch_bounds__(kRowThreads) to_operand_kernel(const float* src, int width, void* op, long plane) {
   pdl_launch_dependents();

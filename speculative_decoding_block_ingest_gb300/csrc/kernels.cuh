@@ -188,7 +188,6 @@ void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const 
 void launch_attention_tc8(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
                           cudaStream_t s);
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s);
-void launch_relay(unsigned long long* trace, cudaStream_t s);
 void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);
 void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s);

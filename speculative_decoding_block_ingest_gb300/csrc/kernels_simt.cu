@@ -334,15 +334,20 @@ void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s) {
 }
 
 // ------------------------------------------------------------------ per-call init
-// CTA r < n_rows: stage row r (residual stream + operand); CTA n_rows: upload
-// the used words of the descriptor, apply page-table entries and clear
-// accumulators.  Row copies issue four float4 loads per thread before storing.
+// The row CTAs stage rows (residual stream or operand), a row's float4s in
+// chunks of kInitChunk4 per CTA; the last CTA uploads the used words of the
+// descriptor, applies page-table entries and clears accumulators.  Row
+// copies issue four float4 loads per thread before storing.
 constexpr int kInitThreads = 256;
+constexpr int kInitChunk4 = 4 * kInitThreads;   // float4 of a row per CTA: four loads per thread
 __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __grid_constant__ InitBlob b) {
   trace_cta_entry(a.trace);
   pdl_launch_dependents();
   pdl_wait();
-  const int r = blockIdx.x, tid = threadIdx.x;
+  // CTA b < n_rows * nch: row b / nch, its float4 chunk b % nch (one load
+  // batch per thread); CTA n_rows * nch: the descriptor
+  const int n4 = a.width / 4, nch = (n4 + kInitChunk4 - 1) / kInitChunk4;
+  const int r = blockIdx.x / nch, ch = blockIdx.x % nch, tid = threadIdx.x;
   if (r == a.n_rows) {
     const int* src = reinterpret_cast<const int*>(&b);
     int* dst = reinterpret_cast<int*>(a.desc_dst);
@@ -354,26 +359,28 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
     return;
   }
   // RoPE (cos, sin) of this row's position, mscale folded in
-  const int pos = a.is_round ? b.round.pos[r] : b.ingest.row_pos[r];
-  const int half = a.g.d / 2;
-  for (int j = tid; j < half; j += kInitThreads) {
-    float sn, cs;
-    rope_sincos(pos, a.inv_freq, j, &sn, &cs);
-    a.rope_cs[(long)r * half + j] = make_float2(cs * a.g.mscale, sn * a.g.mscale);
+  if (ch == 0) {
+    const int pos = a.is_round ? b.round.pos[r] : b.ingest.row_pos[r];
+    const int half = a.g.d / 2;
+    for (int j = tid; j < half; j += kInitThreads) {
+      float sn, cs;
+      rope_sincos(pos, a.inv_freq, j, &sn, &cs);
+      a.rope_cs[(long)r * half + j] = make_float2(cs * a.g.mscale, sn * a.g.mscale);
+    }
   }
-  const int n4 = a.width / 4;
   const float4* src4 = reinterpret_cast<const float4*>(a.src + (long)r * a.width);
-  for (int c0 = tid; c0 < n4; c0 += 4 * kInitThreads) {
+  const int c_end = min(n4, (ch + 1) * kInitChunk4);
+  for (int c0 = ch * kInitChunk4 + tid; c0 < c_end; c0 += 4 * kInitThreads) {
     float4 v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int c = c0 + k * kInitThreads;
-      v[k] = c < n4 ? __ldg(src4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[k] = c < c_end ? __ldg(src4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int c = c0 + k * kInitThreads;
-      if (c >= n4) break;
+      if (c >= c_end) break;
       if (a.h) {
         reinterpret_cast<float4*>(a.h + (long)r * a.width)[c] = v[k];
       } else {
@@ -390,7 +397,10 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
 
 const void* init_kernel_entry() { return reinterpret_cast<const void*>(init_kernel); }
 
-int init_grid(const InitArgs& a) { return a.n_rows + 1; }
+int init_grid(const InitArgs& a) {
+  const int n4 = a.width / 4;
+  return a.n_rows * ((n4 + kInitChunk4 - 1) / kInitChunk4) + 1;
+}
 
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s) {
   launch_pdl(init_kernel, dim3(init_grid(a)), dim3(kInitThreads), 0, s, a, blob);
