@@ -162,8 +162,8 @@ void launch_gemm_simt(const GemmArgs& a, cudaStream_t s);
 cudaError_t launch_proj_own(const OwnArgs& a, const void* tmap_h, cudaStream_t s);
 // Tensor-core projection: a.W is the weight in 16 KB blocks (see weights.cu).
 void launch_gemm_tc(const GemmArgs& a, const void* tmap_x, cudaStream_t s);
-// Token-tiled projection (gemm_tt.cu): bf16 weights, red.add results, more
-// than 64 token rows, N a multiple of 256.  Units = gemm_tt_units; the
+// Token-tiled projection (gemm_tt.cu): bf16 or e4m3 weights, red.add results,
+// more than 64 token rows, N a multiple of 256.  Units = gemm_tt_units; the
 // operand map is the 128-row-box one.
 bool gemm_tt_fits(const GemmArgs& a);
 int gemm_tt_units(const GemmArgs& a);

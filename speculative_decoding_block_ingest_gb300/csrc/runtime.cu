@@ -506,7 +506,8 @@ void run_gemm(dflash_t* h, const GemmSpec& sp, cudaStream_t s) {
       a.p.kb = sp.K / kTileK;
       a.p.units = gemm_tt_units(a);
       a.p.grid = std::min(a.p.units, h->n_sm);
-      const double bytes = (double)sp.N * sp.K * 2 + (double)n_all * sp.K * 4 + (double)n_all * sp.N * 4;
+      const double bytes = (double)sp.N * sp.K * (a.w8 ? 1 : 2) + (a.w8 ? sp.N * 4.0 : 0.0) + (double)n_all * sp.K * 4 +
+                           (double)n_all * sp.N * 4;
       Launch L(h, DFLASH_KERNEL_GEMM, bytes, s);
       a.trace = trace_slot(h, DFLASH_KERNEL_GEMM, a.p.grid);
       launch_gemm_tt(a, &sp.xmap[1], s);

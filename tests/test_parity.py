@@ -234,12 +234,12 @@ def test_context_window_matches_oracle(cfg):
     assert rel_err(_np(k), kv.k[0][0][-16:]) <= tol(cfg)
 
 
-@pytest.mark.parametrize("n_seq", [9, 12, 16])
-def test_wide_batch_rounds_match_oracle(n_seq):
-    """Rounds of 144, 192 and 256 block rows: the projections run as wide
-    passes (unfused hi/lo MMAs of N = 144..256, 128-row plus 16-row operand
-    boxes); every sequence against the oracle."""
-    cfg = SMALL_G8
+@pytest.mark.parametrize("wdt,n_seq", [("bf16", 5), ("bf16", 9), ("bf16", 12), ("bf16", 16), ("fp8", 5), ("fp8", 9)])
+def test_wide_batch_rounds_match_oracle(wdt, n_seq):
+    """Rounds of 80 to 256 block rows: the projections run token-tiled (128
+    token rows x 256 features per tile, a ragged last token tile, bf16 or
+    e4m3 weights widened in the kernel); every sequence against the oracle."""
+    cfg = dataclasses.replace(SMALL_G8, weight_dtype=wdt)
     dr, D = _setup(cfg, max_seqs=n_seq, max_pages=4 * n_seq, max_seq_len=512, max_batch=n_seq,
                    max_ingest_rows=512)
     kv = O.DraftKV(D)
