@@ -289,7 +289,10 @@ __global__ void __launch_bounds__(kW8 ? kTtThreadsW8 : kTtThreads, 1)
         // 16-byte red.add: a warp instruction covers four rows' 128 bytes
         const int rl = lane >> 3, c4 = 4 * (lane & 7);
         float* dst0 = a.dst + (long)(a.e.tok_base + tok0 + rl) * a.dst_ld + ft * kTtN + c4;
-        for (int j0 = 0; j0 < kTtN; j0 += 32) {
+        // the CTAs sharing a tile drain together: each starts at another
+        // 32-feature chunk, so their simultaneous red.adds hit other lines
+        for (int jj = 0; jj < kTtN / 32; ++jj) {
+          const int j0 = ((jj + blockIdx.x) & (kTtN / 32 - 1)) * 32;
           float v[32];
           tmem_ld32(base + (uint32_t)j0, v);                 // warp-wide: lane = row, v = 32 features
 #pragma unroll
