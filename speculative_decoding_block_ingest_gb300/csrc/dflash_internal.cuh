@@ -88,6 +88,7 @@ __device__ __forceinline__ void trace_entry(unsigned long long* tr, int cta, uns
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
     tr[(long)cta * kTraceWords] = smid;
     tr[(long)cta * kTraceWords + 1] = t;
+    tr[(long)cta * kTraceWords + kTraceWords - 1] = 0;   // exit: the warps' maximum (trace_exit_warp)
   }
 }
 __device__ __forceinline__ void trace_mark(unsigned long long* tr, int cta, int point, unsigned long long c0) {
@@ -109,6 +110,19 @@ __device__ __forceinline__ void trace_exit(unsigned long long* tr, int cta) {
   }
 }
 // Entry and exit stamps of the element-wise kernels (thread 0 of each CTA).
+// The CTA's exit as the latest of its warps' finishing times: lane 0 of every
+// warp takes the maximum into the exit word (zeroed by trace_entry before the
+// CTA's set-up barrier).  A single
+// thread's stamp after the final barrier can read early: the role warps of
+// the pipelined kernels reach that barrier converged only in appearance, so
+// the first thread past it is no proof that the others are done.
+__device__ __forceinline__ void trace_exit_warp(unsigned long long* tr, int cta) {
+  if (tr && (threadIdx.x & 31) == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
+    atomicMax(tr + (long)cta * kTraceWords + kTraceWords - 1, t);
+  }
+}
 __device__ __forceinline__ void trace_cta_entry(unsigned long long* tr) {
   unsigned long long c0;
   if (tr && threadIdx.x == 0) trace_entry(tr, blockIdx.x, &c0);

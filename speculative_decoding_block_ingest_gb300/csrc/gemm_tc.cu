@@ -492,7 +492,7 @@ __global__ void __launch_bounds__(kW8 ? kTcThreadsW8 : kTcThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0) trace_mark(a.trace, blockIdx.x, 5, c0);  // 5: all roles done
   if (threadIdx.x == kDrainTid0) trace_mark(a.trace, blockIdx.x, 7, c0);
-  if (threadIdx.x == 0) trace_exit(a.trace, blockIdx.x);
+  trace_exit_warp(a.trace, blockIdx.x);
   if (flags[0] && threadIdx.x == 0) atomicExch(const_cast<int*>(err), DERR_TIMEOUT);
   if (warp == 1) {
     __syncwarp();

@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kOwnThreads, 1)
   }
   __syncwarp();
   __syncthreads();
-  if (threadIdx.x == 0) trace_exit(a.trace, blockIdx.x);
+  trace_exit_warp(a.trace, blockIdx.x);
   if (flags[0] && threadIdx.x == 0) atomicExch(a.err, DERR_TIMEOUT);
   if (warp == 1) {
     __syncwarp();
