@@ -329,7 +329,8 @@ int dflash_profile_read(dflash_t *h, int32_t kind, int64_t *launches, double *ms
 /* Launch trace (measurement).  While a buffer is set, every kernel launch of
  * the handle writes, per CTA, 16 u64 words into the next free region of
  * `device_buffer`: word 0 the SM id, word 1 the %globaltimer (ns) at entry,
- * word 15 the %globaltimer at exit; the tensor-core projection and attention
+ * word 15 the %globaltimer at exit (the latest of the CTA's warps' finishing
+ * stamps, so a warp still draining counts); the tensor-core projection and attention
  * kernels also write words 2..14: SM clock cycles since entry at fixed
  * points of the kernel (set-up done, launch wait passed, last MMA issued,
  * epilogue steps, exit) or cycle counts spent waiting (projection points 9,
