@@ -242,9 +242,55 @@ __device__ __forceinline__ void put_operand(void* op, long idx, long plane, floa
   }
 }
 
+// Four consecutive operand elements [idx, idx + 4) as one vector store per
+// plane (idx and plane multiples of 4); the values put_operand would store.
+__device__ __forceinline__ void put_operand4(void* op, long idx, long plane, float4 v, int kind) {
+  if (kind == OPK_F32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(op) + idx) = v;
+    return;
+  }
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  uint32_t hi[2], lo[2];
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    if (kind == OPK_F16) {
+      const __half h0 = __float2half_rn(x[2 * p]), h1 = __float2half_rn(x[2 * p + 1]);
+      const __half l0 = __float2half_rn(x[2 * p] - __half2float(h0));
+      const __half l1 = __float2half_rn(x[2 * p + 1] - __half2float(h1));
+      hi[p] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+      lo[p] = (uint32_t)__half_as_ushort(l0) | ((uint32_t)__half_as_ushort(l1) << 16);
+    } else {
+      const __nv_bfloat16 h0 = __float2bfloat16_rn(x[2 * p]), h1 = __float2bfloat16_rn(x[2 * p + 1]);
+      const __nv_bfloat16 l0 = __float2bfloat16_rn(x[2 * p] - __bfloat162float(h0));
+      const __nv_bfloat16 l1 = __float2bfloat16_rn(x[2 * p + 1] - __bfloat162float(h1));
+      hi[p] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      lo[p] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+    }
+  }
+  uint16_t* base = reinterpret_cast<uint16_t*>(op);
+  *reinterpret_cast<uint2*>(base + idx) = make_uint2(hi[0], hi[1]);
+  *reinterpret_cast<uint2*>(base + idx + plane) = make_uint2(lo[0], lo[1]);
+}
+
 __device__ __forceinline__ void put_kv(void* base, long idx, float v, int kvtype) {
   if (kvtype == KV_F32) reinterpret_cast<float*>(base)[idx] = v;
   else reinterpret_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+}
+
+// PER consecutive elements of a bf16 or f32 row [idx, idx + PER) (idx a
+// multiple of PER): one vector store at PER = 4, else element by element.
+template <int PER>
+__device__ __forceinline__ void put_kv_row(void* base, long idx, const float* x, int kvtype) {
+  if (PER == 4 && kvtype == KV_F32) {
+    *reinterpret_cast<float4*>(reinterpret_cast<float*>(base) + idx) = make_float4(x[0], x[1], x[2], x[3]);
+  } else if (PER == 4) {
+    const __nv_bfloat162 a = __floats2bfloat162_rn(x[0], x[1]), b = __floats2bfloat162_rn(x[2], x[3]);
+    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(base) + idx) =
+        make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  } else {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) put_kv(base, idx + q, x[q], kvtype);
+  }
 }
 
 __device__ __forceinline__ long pool_layer_elems(const Geo& g) {

@@ -80,10 +80,44 @@ __global__ void __launch_bounds__(kRowThreads) prep_norm_kernel(FinishArgs f) {
       const float4 x = rn.out(k);
       const long idx = (long)tok * g.H + 4 * i;
       if (f.u_out) reinterpret_cast<float4*>(f.u_out + idx)[0] = x;
-      put_operand(f.op, idx + 0, f.op_plane, x.x, f.op_kind);
-      put_operand(f.op, idx + 1, f.op_plane, x.y, f.op_kind);
-      put_operand(f.op, idx + 2, f.op_plane, x.z, f.op_kind);
-      put_operand(f.op, idx + 3, f.op_plane, x.w, f.op_kind);
+      put_operand4(f.op, idx, f.op_plane, x, f.op_kind);
+    }
+  }
+  trace_cta_exit(f.trace);
+}
+
+// Wide passes (more than 64 rows): one warp per token row, the row's VEC
+// float4 per lane (and the gain's) loaded at once and the sum of squares
+// taken by warp shuffles; a CTA of kRowWarps rows, so a pass of 512 rows is
+// 128 CTAs instead of 512.
+constexpr int kRowWarps = 4;
+template <int VEC>
+__global__ void __launch_bounds__(32 * kRowWarps) prep_norm_warp_kernel(FinishArgs f) {
+  trace_cta_entry(f.trace);
+  pdl_launch_dependents();
+  pdl_wait();
+  const Geo& g = f.g;
+  const int lane = threadIdx.x & 31;
+  const int tok = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (tok < f.n_tok) {
+    const float4* r4 = reinterpret_cast<const float4*>(f.h + (long)tok * g.H);
+    const float4* g4 = reinterpret_cast<const float4*>(f.gain);
+    float4 v[VEC], w[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      v[k] = __ldcg(r4 + lane + 32 * k);
+      w[k] = __ldg(g4 + lane + 32 * k);
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    const float r = rsqrtf(warp_sum(ss) / (float)g.H + g.eps);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+      const float4 x = make_float4(v[k].x * w[k].x * r, v[k].y * w[k].y * r, v[k].z * w[k].z * r, v[k].w * w[k].w * r);
+      const long idx = (long)tok * g.H + 4 * (lane + 32 * k);
+      if (f.u_out) reinterpret_cast<float4*>(f.u_out + idx)[0] = x;
+      put_operand4(f.op, idx, f.op_plane, x, f.op_kind);
     }
   }
   trace_cta_exit(f.trace);
@@ -107,106 +141,138 @@ __global__ void __launch_bounds__(kRowThreads) final_norm_kernel(const float* h,
   trace_cta_exit(trace);
 }
 
-// One warp per (token, head) row of the QKV accumulator.
-template <int PER>
-__device__ void qk_finish_row(const FinishArgs& f, int tok, int hh) {
+// One warp per (token, head) row of the QKV accumulator, RPW rows per warp
+// (rows w, w + W, ... for W warps in the grid): the accumulator and RoPE
+// loads of all of a warp's rows are issued before the first row is
+// finished (its stores may alias later rows, so the compiler would not
+// hoist them).
+template <int PER, int RPW>
+__device__ void qk_finish_rows(const FinishArgs& f, int row0, int rstride) {
   const Geo& g = f.g;
   constexpr int d = 32 * PER, half = d / 2;
+  const int heads = g.Hq + 2 * g.Hkv, n_rows = f.n_tok * heads;
   const int lane = threadIdx.x & 31, dim0 = lane * PER;
-  const int kind = hh < g.Hq ? 0 : (hh < g.Hq + g.Hkv ? 1 : 2);
-  const int head = kind == 0 ? hh : (kind == 1 ? hh - g.Hq : hh - g.Hq - g.Hkv);
-  float* src = f.acc + (long)tok * g.qkv_n + hh * d + dim0;
-  float x[PER], gn[PER];
-  float2 cs[PER];
-  if (PER == 4) {
-    const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
-  } else {
-    const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-    x[0] = v.x; x[1] = v.y;
-  }
-  const float* gsrc = kind == 0 ? f.qn : f.kn;
+  float x[RPW][PER];
+  float2 cs[RPW][PER];
 #pragma unroll
-  for (int q = 0; q < PER; ++q) {
-    gn[q] = kind != 2 ? gsrc[dim0 + q] : 1.f;
-    cs[q] = kind != 2 ? f.rope_cs[(long)tok * half + (dim0 + q) % half] : make_float2(1.f, 0.f);
-  }
-  const int dst = kind != 0 ? f.dest[tok] : 0;
-  // clear the accumulator row for the next layer
-  if (PER == 4) *reinterpret_cast<float4*>(src) = make_float4(0.f, 0.f, 0.f, 0.f);
-  else *reinterpret_cast<float2*>(src) = make_float2(0.f, 0.f);
-  if (kind != 2) {
-    float ss = 0.f;
-#pragma unroll
-    for (int q = 0; q < PER; ++q) ss += x[q] * x[q];
-    ss = warp_sum(ss);
-    const float rn = rsqrtf(ss / (float)d + g.eps);
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const float y = x[q] * rn * gn[q];
-      const float partner = __shfl_xor_sync(0xffffffffu, y, 16);   // dims j <-> j + d/2
-      x[q] = lane < 16 ? (y * cs[q].x - partner * cs[q].y) : (y * cs[q].x + partner * cs[q].y);
+  for (int r = 0; r < RPW; ++r) {
+    const int row = row0 + r * rstride;
+    if (row >= n_rows) break;
+    const int tok = row / heads, hh = row % heads;
+    const float* src = f.acc + (long)tok * g.qkv_n + hh * d + dim0;
+    if (PER == 4) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+      x[r][0] = v.x; x[r][1] = v.y; x[r][2] = v.z; x[r][3] = v.w;
+    } else {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+      x[r][0] = v.x; x[r][1] = v.y;
     }
+    const bool roped = hh < g.Hq + g.Hkv;
+#pragma unroll
+    for (int q = 0; q < PER; ++q)
+      cs[r][q] = roped ? f.rope_cs[(long)tok * half + (dim0 + q) % half] : make_float2(1.f, 0.f);
   }
-  if (g.kvtype == KV_FP8 && kind == 0) {
-    // an e4m3 cache stores K and V only: its queries stay f16
-    __half* qrow = static_cast<__half*>(f.q_out) + ((long)tok * g.Hq + head) * d + dim0;
 #pragma unroll
-    for (int q = 0; q < PER; ++q) qrow[q] = __float2half_rn(x[q]);
-  } else if (g.kvtype == KV_FP8) {
-    put_row_fp8<PER>(g, x, lane, kind, f.layer, tok, head, dst, f.kpool, f.vpool);
-  } else if (kind == 0) {
-    const long base = ((long)tok * g.Hq + head) * d + dim0;
+  for (int r = 0; r < RPW; ++r) {
+    const int row = row0 + r * rstride;
+    if (row >= n_rows) break;
+    const int tok = row / heads, hh = row % heads;
+    const int kind = hh < g.Hq ? 0 : (hh < g.Hq + g.Hkv ? 1 : 2);
+    const int head = kind == 0 ? hh : (kind == 1 ? hh - g.Hq : hh - g.Hq - g.Hkv);
+    float* src = f.acc + (long)tok * g.qkv_n + hh * d + dim0;
+    // clear the accumulator row for the next layer
+    if (PER == 4) *reinterpret_cast<float4*>(src) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else *reinterpret_cast<float2*>(src) = make_float2(0.f, 0.f);
+    float* xr = x[r];
+    if (kind != 2) {
+      const float* gsrc = kind == 0 ? f.qn : f.kn;
+      float ss = 0.f;
 #pragma unroll
-    for (int q = 0; q < PER; ++q) put_kv(f.q_out, base + q, x[q], g.kvtype);
-  } else {
-    const int page = dst >> 6, off = dst & (kPage - 1);
+      for (int q = 0; q < PER; ++q) ss += xr[q] * xr[q];
+      ss = warp_sum(ss);
+      const float rn = rsqrtf(ss / (float)d + g.eps);
 #pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      if (kind == 1) put_kv(f.kpool, k_index(g, f.layer, page, head, off, dim0 + q), x[q], g.kvtype);
-      else put_kv(f.vpool, v_index(g, f.layer, page, head, off, dim0 + q), x[q], g.kvtype);
+      for (int q = 0; q < PER; ++q) {
+        const float y = xr[q] * rn * gsrc[dim0 + q];
+        const float partner = __shfl_xor_sync(0xffffffffu, y, 16);   // dims j <-> j + d/2
+        xr[q] = lane < 16 ? (y * cs[r][q].x - partner * cs[r][q].y) : (y * cs[r][q].x + partner * cs[r][q].y);
+      }
+    }
+    const int dst = kind != 0 ? f.dest[tok] : 0;
+    if (g.kvtype == KV_FP8 && kind == 0) {
+      // an e4m3 cache stores K and V only: its queries stay f16
+      __half* qrow = static_cast<__half*>(f.q_out) + ((long)tok * g.Hq + head) * d + dim0;
+#pragma unroll
+      for (int q = 0; q < PER; ++q) qrow[q] = __float2half_rn(xr[q]);
+    } else if (g.kvtype == KV_FP8) {
+      put_row_fp8<PER>(g, xr, lane, kind, f.layer, tok, head, dst, f.kpool, f.vpool);
+    } else if (kind == 0) {
+      put_kv_row<PER>(f.q_out, ((long)tok * g.Hq + head) * d + dim0, xr, g.kvtype);
+    } else {
+      const int page = dst >> 6, off = dst & (kPage - 1);
+      if (kind == 1) {
+        put_kv_row<PER>(f.kpool, k_index(g, f.layer, page, head, off, dim0), xr, g.kvtype);
+      } else {
+#pragma unroll
+        for (int q = 0; q < PER; ++q) put_kv(f.vpool, v_index(g, f.layer, page, head, off, dim0 + q), xr[q], g.kvtype);
+      }
     }
   }
 }
 
-__global__ void __launch_bounds__(128) qk_finish_kernel(FinishArgs f) {
+constexpr int kQkMaxRpw = 4;
+template <int RPW>
+__global__ void __launch_bounds__(256) qk_finish_kernel(FinishArgs f) {
   trace_cta_entry(f.trace);
   pdl_launch_dependents();
   pdl_wait();
-  const Geo& g = f.g;
-  const int heads = g.Hq + 2 * g.Hkv;
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (row >= f.n_tok * heads) return;
-  const int tok = row / heads, hh = row % heads;
-  if (g.d == 128) qk_finish_row<4>(f, tok, hh);
-  else qk_finish_row<2>(f, tok, hh);
+  const int wpc = blockDim.x >> 5;
+  const int row0 = blockIdx.x * wpc + (threadIdx.x >> 5), rstride = gridDim.x * wpc;
+  if (f.g.d == 128) qk_finish_rows<4, RPW>(f, row0, rstride);
+  else qk_finish_rows<2, RPW>(f, row0, rstride);
   trace_cta_exit(f.trace);
 }
 
-// One float4 of act per thread: a single round trip, no loop.
-__global__ void __launch_bounds__(128) swiglu_kernel(FinishArgs f) {
+// Four float4 of act per thread per pass, every gate and up load of a pass
+// issued before the first store (the stores may alias later loads, so the
+// compiler would not hoist them), over a grid of at most two CTAs per SM.
+constexpr int kSwiThreads = 256;
+constexpr int kSwiVec = 4;
+__global__ void __launch_bounds__(kSwiThreads) swiglu_kernel(FinishArgs f) {
   trace_cta_entry(f.trace);
   pdl_launch_dependents();
   pdl_wait();
   const Geo& g = f.g;
   const long n4 = (long)f.n_tok * g.I / 4;
-  {
-    const long k = (long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (k >= n4) {
-      trace_cta_exit(f.trace);
-      return;
-    }
-    const long e = k * 4;
-    const int tok = (int)(e / g.I), j = (int)(e % g.I);
-    float* gp = f.acc + (long)tok * 2 * g.I + (j / 64) * 128 + (j % 64);
-    const float4 gv = __ldcg(reinterpret_cast<const float4*>(gp));
-    const float4 uv = __ldcg(reinterpret_cast<const float4*>(gp + 64));
-    *reinterpret_cast<float4*>(gp) = make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4*>(gp + 64) = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float gg[4] = {gv.x, gv.y, gv.z, gv.w}, uu[4] = {uv.x, uv.y, uv.z, uv.w};
+  const long stride = (long)gridDim.x * kSwiThreads;
+  for (long k0 = (long)blockIdx.x * kSwiThreads + threadIdx.x; k0 < n4; k0 += kSwiVec * stride) {
+    float4 gv[kSwiVec], uv[kSwiVec];
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      put_operand(f.op, (long)tok * g.I + j + q, f.op_plane, gg[q] / (1.f + __expf(-gg[q])) * uu[q], f.op_kind);
+    for (int q = 0; q < kSwiVec; ++q) {
+      const long k = k0 + q * stride;
+      if (k < n4) {
+        const long e = k * 4;
+        const float* gp = f.acc + (e / g.I) * 2 * g.I + ((e % g.I) / 64) * 128 + (e % 64);
+        gv[q] = __ldcg(reinterpret_cast<const float4*>(gp));
+        uv[q] = __ldcg(reinterpret_cast<const float4*>(gp + 64));
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kSwiVec; ++q) {
+      const long k = k0 + q * stride;
+      if (k < n4) {
+        const long e = k * 4;
+        const int tok = (int)(e / g.I), j = (int)(e % g.I);
+        float* gp = f.acc + (long)tok * 2 * g.I + (j / 64) * 128 + (j % 64);
+        *reinterpret_cast<float4*>(gp) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(gp + 64) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 a = make_float4(gv[q].x / (1.f + __expf(-gv[q].x)) * uv[q].x,
+                                     gv[q].y / (1.f + __expf(-gv[q].y)) * uv[q].y,
+                                     gv[q].z / (1.f + __expf(-gv[q].z)) * uv[q].z,
+                                     gv[q].w / (1.f + __expf(-gv[q].w)) * uv[q].w);
+        put_operand4(f.op, (long)tok * g.I + j, f.op_plane, a, f.op_kind);
+      }
+    }
   }
   trace_cta_exit(f.trace);
 }
@@ -220,10 +286,7 @@ __global__ void __launch_bounds__(kRowThreads) to_operand_kernel(const float* sr
   for (int c = threadIdx.x; c < n4; c += kRowThreads) {
     const float4 v = __ldg(r4 + c);
     const long idx = (long)row * width + 4 * c;
-    put_operand(op, idx + 0, plane, v.x, 0);
-    put_operand(op, idx + 1, plane, v.y, 0);
-    put_operand(op, idx + 2, plane, v.z, 0);
-    put_operand(op, idx + 3, plane, v.w, 0);
+    put_operand4(op, idx, plane, v, OPK_BF16);
   }
 }
 
@@ -277,10 +340,25 @@ void launch_argmax(const float* logits, int n_rows, int V, int32_t* tokens, cuda
   launch_pdl(argmax_kernel, dim3(n_rows), dim3(kRowThreads), 0, s, logits, V, tokens);
 }
 
-int prep_norm_grid(const FinishArgs& f) { return f.n_tok; }
+// float4 per lane of the warp-per-row form (a row of 512, 1024 or 2048), else 0
+static int prep_norm_vec(const FinishArgs& f) {
+  if (f.n_tok <= 64 || f.g.H % 128) return 0;
+  const int vec = f.g.H / 128;
+  return (vec == 4 || vec == 8 || vec == 16) ? vec : 0;
+}
+
+int prep_norm_grid(const FinishArgs& f) {
+  return prep_norm_vec(f) ? (f.n_tok + kRowWarps - 1) / kRowWarps : f.n_tok;
+}
 
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s) {
-  launch_pdl(prep_norm_kernel, dim3(prep_norm_grid(f)), dim3(kRowThreads), 0, s, f);
+  const dim3 grid(prep_norm_grid(f)), warps(32 * kRowWarps);
+  switch (prep_norm_vec(f)) {
+    case 4: launch_pdl(prep_norm_warp_kernel<4>, grid, warps, 0, s, f); break;
+    case 8: launch_pdl(prep_norm_warp_kernel<8>, grid, warps, 0, s, f); break;
+    case 16: launch_pdl(prep_norm_warp_kernel<16>, grid, warps, 0, s, f); break;
+    default: launch_pdl(prep_norm_kernel, grid, dim3(kRowThreads), 0, s, f);
+  }
 }
 
 const void* final_norm_kernel_entry() { return reinterpret_cast<const void*>(final_norm_kernel); }
@@ -344,20 +422,39 @@ void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s) {
   launch_pdl(conv_kernel, dim3(conv_grid(c, n_sm)), dim3(256), 0, s, c);
 }
 
-int qk_finish_grid(const FinishArgs& f) { return (f.n_tok * (f.g.Hq + 2 * f.g.Hkv) + 3) / 4; }
+// Rows per warp (1, 2 or 4 at d = 128; 1 at d = 64) and warps per CTA (4 for
+// one row a warp, else 8): about eight warps per SM over the pass.
+static void qk_finish_shape(const FinishArgs& f, int n_sm, int* rpw, int* wpc) {
+  const long rows = (long)f.n_tok * (f.g.Hq + 2 * f.g.Hkv);
+  const long per = (rows + 8L * n_sm - 1) / (8L * n_sm);
+  *rpw = f.g.d != 128 || per <= 1 ? 1 : (per <= 2 ? 2 : kQkMaxRpw);
+  *wpc = *rpw == 1 ? 4 : 8;
+}
 
-void launch_qk_finish(const FinishArgs& f, cudaStream_t s) {
-  launch_pdl(qk_finish_kernel, dim3(qk_finish_grid(f)), dim3(128), 0, s, f);
+int qk_finish_grid(const FinishArgs& f, int n_sm) {
+  int rpw, wpc;
+  qk_finish_shape(f, n_sm, &rpw, &wpc);
+  const long rows = (long)f.n_tok * (f.g.Hq + 2 * f.g.Hkv);
+  return (int)((rows + (long)rpw * wpc - 1) / ((long)rpw * wpc));
+}
+
+void launch_qk_finish(const FinishArgs& f, int n_sm, cudaStream_t s) {
+  int rpw, wpc;
+  qk_finish_shape(f, n_sm, &rpw, &wpc);
+  const dim3 grid(qk_finish_grid(f, n_sm)), block(32 * wpc);
+  if (rpw == 1) launch_pdl(qk_finish_kernel<1>, grid, block, 0, s, f);
+  else if (rpw == 2) launch_pdl(qk_finish_kernel<2>, grid, block, 0, s, f);
+  else launch_pdl(qk_finish_kernel<kQkMaxRpw>, grid, block, 0, s, f);
 }
 
 int swiglu_grid(const FinishArgs& f, int n_sm) {
-  (void)n_sm;
   const long n4 = (long)f.n_tok * f.g.I / 4;
-  return (int)((n4 + 127) / 128);
+  const long per_cta = (long)kSwiThreads * kSwiVec;
+  return (int)std::max<long>(1, std::min<long>((n4 + per_cta - 1) / per_cta, 2L * n_sm));
 }
 
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s) {
-  launch_pdl(swiglu_kernel, dim3(swiglu_grid(f, n_sm)), dim3(128), 0, s, f);
+  launch_pdl(swiglu_kernel, dim3(swiglu_grid(f, n_sm)), dim3(kSwiThreads), 0, s, f);
 }
 
 }  // namespace dfl

@@ -188,13 +188,13 @@ void launch_attention_tc(const AttnArgs& a, int n_items, const void* tmq, const 
 void launch_attention_tc8(const AttnArgs& a, int n_items, const void* tmq, const void* tmk, const void* tmv,
                           cudaStream_t s);
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s);
-void launch_qk_finish(const FinishArgs& f, cudaStream_t s);
+void launch_qk_finish(const FinishArgs& f, int n_sm, cudaStream_t s);
 void launch_swiglu(const FinishArgs& f, int n_sm, cudaStream_t s);
 void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s);
 void launch_attn_combine(const AttnArgs& a, int n_tok, cudaStream_t s);
 // CTAs of the element-wise launches (trace regions are sized by them).
 int prep_norm_grid(const FinishArgs& f);
-int qk_finish_grid(const FinishArgs& f);
+int qk_finish_grid(const FinishArgs& f, int n_sm);
 int swiglu_grid(const FinishArgs& f, int n_sm);
 int conv_grid(const ConvArgs& c, int n_sm);
 int attn_combine_grid(const AttnArgs& a, int n_tok);

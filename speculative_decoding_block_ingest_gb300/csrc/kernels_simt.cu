@@ -308,10 +308,7 @@ __global__ void __launch_bounds__(kCombThreads) attn_combine_kernel(AttnArgs a, 
     }
     const float inv = 1.f / l;
     const long idx = (long)tok * a.op_ld + h * g.d + 4 * lane;
-    put_operand(a.op, idx + 0, a.op_plane, t.x * inv, a.op_kind);
-    put_operand(a.op, idx + 1, a.op_plane, t.y * inv, a.op_kind);
-    put_operand(a.op, idx + 2, a.op_plane, t.z * inv, a.op_kind);
-    put_operand(a.op, idx + 3, a.op_plane, t.w * inv, a.op_kind);
+    put_operand4(a.op, idx, a.op_plane, make_float4(t.x * inv, t.y * inv, t.z * inv, t.w * inv), a.op_kind);
   }
   trace_cta_exit(a.trace);
 }
@@ -385,10 +382,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
         reinterpret_cast<float4*>(a.h + (long)r * a.width)[c] = v[k];
       } else {
         const long idx = (long)r * a.op_ld + 4 * c;
-        put_operand(a.op, idx + 0, a.op_plane, v[k].x, a.op_kind);
-        put_operand(a.op, idx + 1, a.op_plane, v[k].y, a.op_kind);
-        put_operand(a.op, idx + 2, a.op_plane, v[k].z, a.op_kind);
-        put_operand(a.op, idx + 3, a.op_plane, v[k].w, a.op_kind);
+        put_operand4(a.op, idx, a.op_plane, v[k], a.op_kind);
       }
     }
   }

@@ -834,8 +834,8 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
       f.qn = h->at<float>(h->lo.qn) + (size_t)l * g.d;
       f.kn = h->at<float>(h->lo.kn) + (size_t)l * g.d;
       Launch L(h, DFLASH_KERNEL_FINISH, (double)n_tok * g.qkv_n * 6, s);
-      f.trace = trace_slot(h, DFLASH_KERNEL_FINISH, qk_finish_grid(f));
-      launch_qk_finish(f, s);
+      f.trace = trace_slot(h, DFLASH_KERNEL_FINISH, qk_finish_grid(f, h->n_sm));
+      launch_qk_finish(f, h->n_sm, s);
     }
     ck(cudaGetLastError(), "qk finish launch");
 
