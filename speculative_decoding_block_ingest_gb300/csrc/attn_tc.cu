@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // wait (which is when this kernel may start), so they are read before this
   // kernel's wait; only the pages holding this round's block rows and the
   // query tile (both written by the predecessor) wait for it.
-  const int item = blockIdx.x;
+  const int item = a.rd->perm[blockIdx.x];              // longest items launch first
   int s, kvh, k0, k1, ks;
   attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &ks);
   const int n_pages = (k1 - k0 + kPage - 1) / kPage;

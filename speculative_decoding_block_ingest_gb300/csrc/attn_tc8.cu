@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kA8Threads, 1)
 
   // the descriptor, page table and cached-context pages are read before the
   // launch wait, as in attn_tc.cu
-  const int item = blockIdx.x;
+  const int item = a.rd->perm[blockIdx.x];              // longest items launch first
   int s, kvh, k0, k1, ks;
   attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &ks);
   const int n_pages = (k1 - k0 + kPage - 1) / kPage;

@@ -34,6 +34,7 @@ constexpr int kMaxIngestRows = 512;
 constexpr int kMaxConvGroups = 256;   // DFlash2 conv channel groups
 constexpr int kMaxHidden = 8192;  // widest residual row the row kernels hold in registers
 constexpr int kMaxPtUpdates = 160;
+constexpr int kMaxItems = 2048;   // attention work items of a round
 constexpr int kEpiThreads = 128;  // threads running a tile epilogue
 constexpr int kEpiTokChunk = 32;  // tokens per epilogue pass
 constexpr int kEpiBar = 1;        // named barrier id used by the epilogue
@@ -140,6 +141,7 @@ struct RoundDesc {
   int kstart[kMaxBatch];           // first attended key position (context window; 0 = all)
   int pos[kMaxBatch * kBlock];     // absolute position of each block row
   int dest[kMaxBatch * kBlock];    // page*64 + offset of the row's transient K/V
+  uint16_t perm[kMaxItems];        // launch order: attention CTA c runs work item perm[c]
 };
 
 // Per-call descriptor of an ingest (rows in call order).

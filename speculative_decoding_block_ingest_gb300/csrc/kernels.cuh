@@ -127,8 +127,8 @@ struct InitArgs {
   float* zero_ptr;      // floats to clear
   int zero_n;
   void* desc_dst;       // device descriptor
-  int cp_off[3], cp_len[3];   // word ranges of the descriptor that are used
-                              // (head, positions, destinations)
+  int cp_off[4], cp_len[4];   // word ranges of the descriptor that are used
+                              // (head, positions, destinations, launch order)
   int* block_table;
   const double* inv_freq;   // RoPE inverse frequencies [d/2] (f64)
   float2* rope_cs;          // out: per row [d/2] (cos, sin) x mscale

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(AttnArgs a) {
   float* Ks = Os + R * dp;        // [64][d+1]
   float* Vs = Ks + kPage * dp;    // [d][65]
   const int tid = threadIdx.x;
-  const int item = blockIdx.x;
+  const int item = a.rd->perm[blockIdx.x];
   int s, kvh, k0, k1, ks;
   attn_item(a.rd, g.Hkv, item, &s, &kvh, &k0, &k1, &ks);
   const int slot = a.rd->seq_slot[s];
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kInitThreads) init_kernel(InitArgs a, const __
   if (r == a.n_rows) {
     const int* src = reinterpret_cast<const int*>(&b);
     int* dst = reinterpret_cast<int*>(a.desc_dst);
-    for (int q = 0; q < 3; ++q)
+    for (int q = 0; q < 4; ++q)
       for (int i = tid; i < a.cp_len[q]; i += kInitThreads) dst[a.cp_off[q] + i] = src[a.cp_off[q] + i];
     for (int i = tid; i < b.n_pt; i += kInitThreads) a.block_table[b.pt_idx[i]] = b.pt_page[i];
     for (int i = tid; i < a.zero_n; i += kInitThreads) a.zero_ptr[i] = 0.f;

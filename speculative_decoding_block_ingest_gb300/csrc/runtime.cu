@@ -9,6 +9,8 @@
 // parameter, so no host-to-device copy and no host synchronisation happen on
 // the round's path.
 #include <algorithm>
+#include <functional>
+#include <queue>
 #include <atomic>
 #include <cstdlib>
 #include <cmath>
@@ -92,7 +94,7 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.grid_max = 2 * n_sm;
   Lo.n_sites = 2 + 4 * (int)L;
   const size_t G = Hq / Hkv, R = G * kBlock;
-  Lo.items_cap = 2 * n_sm + (int)Hkv * c.max_batch;
+  Lo.items_cap = std::min(2 * n_sm + (int)Hkv * c.max_batch, kMaxItems);
   const size_t Mt = Lo.Mt;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -191,6 +193,8 @@ int validate_config(const dflash_config* c) {
   if (c->max_seqs < 1 || c->max_pages < 1 || c->max_seq_len < kBlock + 1)
     return fail(DFLASH_ERR_INVALID_ARG, "capacity fields must be positive");
   if (c->max_batch < 1 || c->max_batch > kMaxBatch) return fail(DFLASH_ERR_INVALID_ARG, "max_batch must be 1..64");
+  if ((long)c->n_kv_heads * c->max_batch > kMaxItems)
+    return fail(DFLASH_ERR_INVALID_ARG, "n_kv_heads x max_batch must be at most %d", kMaxItems);
   if (c->max_ingest_rows < 1 || c->max_ingest_rows > kMaxIngestRows)
     return fail(DFLASH_ERR_INVALID_ARG, "max_ingest_rows must be 1..512");
   if (c->conv_groups < 0 || c->conv_groups > kMaxConvGroups ||
@@ -633,40 +637,92 @@ void enqueue_ingest(dflash_t* h, const InitBlob& blob, const float* taps, cudaSt
   run_gemm(h, kv, s);
 }
 
-int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int* kstart) {
+// Pages from the one holding each sequence's first attended key through its
+// block rows.
+static std::vector<long> attended_pages(const std::vector<int64_t>& lens, const int* kstart) {
   std::vector<long> pages(lens.size());
-  long units = 0, longest = 1;
-  for (size_t i = 0; i < lens.size(); ++i) {
-    pages[i] = (lens[i] + kBlock + kPage - 1) / kPage - kstart[i] / kPage;
-    units += (long)h->g.Hkv * pages[i];
-    longest = std::max(longest, pages[i]);
+  for (size_t i = 0; i < lens.size(); ++i) pages[i] = (lens[i] + kBlock + kPage - 1) / kPage - kstart[i] / kPage;
+  return pages;
+}
+
+// Finishing time of a round's attention items (pages each plus a fixed
+// per-item cost of about two chunks), launched longest first, each CTA
+// taking the SM that frees first among `slots`.
+static long schedule_span(const std::vector<long>& pages, int Hkv, long sp, long slots, long item_cost,
+                          std::vector<long>& scratch) {
+  scratch.clear();
+  for (long p : pages)
+    for (long k0 = 0; k0 < p; k0 += sp) scratch.insert(scratch.end(), Hkv, std::min(sp, p - k0) + item_cost);
+  std::stable_sort(scratch.begin(), scratch.end(), std::greater<long>());
+  std::priority_queue<long, std::vector<long>, std::greater<long>> free_at;
+  long span = 0;
+  for (long c : scratch) {
+    long t = 0;
+    if ((long)free_at.size() >= slots) {
+      t = free_at.top();
+      free_at.pop();
+    }
+    free_at.push(t + c);
+    span = std::max(span, t + c);
   }
-  // Items run in waves of `slots` CTAs and each walks its pages serially, so
-  // take the split that minimises waves x (pages per item + a fixed per-item
-  // cost of about two chunks); among equals the larger split (fewer partials
-  // to merge).
+  return span;
+}
+
+int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int* kstart) {
+  const std::vector<long> pages = attended_pages(lens, kstart);
+  long units = 0, longest = 1;
+  for (long p : pages) {
+    units += (long)h->g.Hkv * p;
+    longest = std::max(longest, p);
+  }
+  // Items go to SMs as earlier ones finish (launched longest first), so
+  // score a few split sizes by that schedule: the per-SM share of all pages
+  // and its halves, thirds, ... (and the wave-count choice below).  Among
+  // equal spans the larger split wins (fewer partials to merge).
   // (beside a small round's projection, which holds proj_grid SMs, so that
   // the two kernels can be resident together)
   const int n_tok = (int)lens.size() * kBlock;
   const long beside = (long)h->n_sm - proj_grid(h, n_tok);
   const long slots = h->attn_tc ? (n_tok <= 64 && beside >= 32 ? beside : (long)h->n_sm) : 2L * h->n_sm;
   constexpr long kItemCost = 4;
-  long best = 1, best_cost = -1;
-  for (long sp = 1; sp <= longest; ++sp) {
+  auto items_of = [&](long sp) {
     long items = 0;
     for (long p : pages) items += (long)h->g.Hkv * ((p + sp - 1) / sp);
+    return items;
+  };
+  // the split minimising waves x (pages per item + the fixed cost), as if
+  // items ran in lockstep waves
+  long wave_sp = longest, best_wave = -1;
+  for (long sp = 1; sp <= longest; ++sp) {
+    const long items = items_of(sp);
     if (items > h->lo.items_cap) continue;   // sp = longest always fits: Hkv items a sequence
     const long cost = (items + slots - 1) / slots * (sp + kItemCost);
-    if (best_cost < 0 || cost <= best_cost) {
+    if (best_wave < 0 || cost <= best_wave) {
+      wave_sp = sp;
+      best_wave = cost;
+    }
+  }
+  std::vector<long> cand = {wave_sp, longest};
+  const long share = (units + slots - 1) / slots;
+  for (long k = 1; k <= 8; ++k) cand.push_back(std::max(1L, (share + k - 1) / k));
+  std::sort(cand.begin(), cand.end(), std::greater<long>());
+  cand.erase(std::unique(cand.begin(), cand.end()), cand.end());
+  std::vector<long> scratch;
+  long best = wave_sp, best_span = -1;
+  for (long sp : cand) {
+    if (sp > longest || items_of(sp) > h->lo.items_cap) continue;
+    const long span = schedule_span(pages, h->g.Hkv, sp, slots, kItemCost, scratch);
+    if (best_span < 0 || span < best_span) {
       best = sp;
-      best_cost = cost;
+      best_span = span;
     }
   }
   return (int)best;
 }
 
 // Arguments of a round's init kernel (copied into the kernel's parameters).
-InitArgs round_init_args(dflash_t* h, int n_tok, const float* noise) {
+InitArgs round_init_args(dflash_t* h, const RoundDesc& rd, const float* noise) {
+  const int n_tok = rd.n_tok;
   InitArgs ia{};
   ia.src = noise;
   ia.n_rows = n_tok;
@@ -679,6 +735,8 @@ InitArgs round_init_args(dflash_t* h, int n_tok, const float* noise) {
   ia.cp_len[1] = n_tok;
   ia.cp_off[2] = (int)(offsetof(RoundDesc, dest) / 4);
   ia.cp_len[2] = n_tok;
+  ia.cp_off[3] = (int)(offsetof(RoundDesc, perm) / 4);
+  ia.cp_len[3] = (rd.n_items + 1) / 2;   // two 16-bit entries a word
   ia.block_table = h->at<int>(h->lo.btab);
   ia.inv_freq = h->at<double>(h->lo.inv_freq);
   ia.rope_cs = h->at<float2>(h->lo.rope_cs);
@@ -711,7 +769,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
   float* qkv_acc = h->at<float>(h->lo.qkv_acc);
   float* gu_acc = h->at<float>(h->lo.gu_acc);
 
-  InitArgs ia = round_init_args(h, n_tok, noise);
+  InitArgs ia = round_init_args(h, rd, noise);
   {
     Launch L(h, DFLASH_KERNEL_INIT, (double)n_tok * g.H * 8, s);
     ia.trace = trace_slot(h, DFLASH_KERNEL_INIT, init_grid(ia));
@@ -977,15 +1035,24 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
 // Fill the attention split plan of a round descriptor.
 void plan_attention(dflash_t* h, RoundDesc& rd, const std::vector<int64_t>& lens) {
   rd.split_pages = choose_split_pages(h, lens, rd.kstart);
+  const std::vector<long> pages = attended_pages(lens, rd.kstart);
+  const long sp = rd.split_pages;
+  // items (sequence, kv head, split) in that order; the launch order puts
+  // the longest first (ties in item order), so short remainders fill in last
+  std::vector<std::pair<long, int>> order;
   int items = 0;
   for (int s = 0; s < rd.n_seq; ++s) {
     rd.item0[s] = items;
-    // pages from the one holding the first attended key through the block rows
-    const int pages = (int)((lens[s] + kBlock + kPage - 1) / kPage - rd.kstart[s] / kPage);
-    items += h->g.Hkv * ((pages + rd.split_pages - 1) / rd.split_pages);
+    const long n_split = (pages[s] + sp - 1) / sp;
+    for (int kvh = 0; kvh < h->g.Hkv; ++kvh)
+      for (long j = 0; j < n_split; ++j) order.push_back({std::min(sp, pages[s] - j * sp), items++});
   }
   rd.item0[rd.n_seq] = items;
   rd.n_items = items;
+  if (items > kMaxItems) return;   // refused by the caller (beyond the scratch)
+  std::stable_sort(order.begin(), order.end(),
+                   [](const std::pair<long, int>& a, const std::pair<long, int>& b) { return a.first > b.first; });
+  for (int c = 0; c < items; ++c) rd.perm[c] = (uint16_t)order[c].second;
 }
 
 
@@ -1123,7 +1190,7 @@ void enqueue_round_graph(dflash_t* h, InitBlob& blob, const float* noise, float*
   dflash_handle::RoundGraph* gr = nullptr;
   for (auto& e : h->graphs)
     if (e.n_seq == rd.n_seq && e.n_items == rd.n_items && e.region == region) gr = &e;
-  InitArgs ia = round_init_args(h, rd.n_tok, noise);
+  InitArgs ia = round_init_args(h, rd, noise);
   if (gr) {
     cudaKernelNodeParams p = gr->init_p;
     void* ip[2] = {&ia, &blob};
