@@ -111,6 +111,7 @@ struct AttnArgs {
   int op_kind;             // operand kind (OpKind)
   float scale_log2;     // log2(e)/sqrt(d): scores and the saved max are in log2 units
   int comb_wpr;         // merge: warps per merged row (attn_combine_wpr of the largest split count)
+  int comb_max_split;   // merge: the largest split count of a row
   unsigned long long* trace;   // optional per-CTA timestamps [items][kTraceWords], or null
   int* err;
   Geo g;

@@ -920,6 +920,7 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
       int max_split = 1;
       for (int i = 0; i < rd.n_seq; ++i) max_split = std::max(max_split, (rd.item0[i + 1] - rd.item0[i]) / g.Hkv);
       a.comb_wpr = attn_combine_wpr(max_split);
+      a.comb_max_split = max_split;
     }
     // bytes per cached element (e4m3: the code plus its row's scale share)
     const double ekv = g.kvtype == KV_F32 ? 4 : (g.kvtype == KV_FP8 ? 1.0 + 4.0 / g.d : 2);
