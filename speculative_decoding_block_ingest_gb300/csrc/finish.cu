@@ -220,7 +220,6 @@ __device__ void qk_finish_rows(const FinishArgs& f, int row0, int rstride) {
   }
 }
 
-constexpr int kQkMaxRpw = 4;
 template <int RPW>
 __global__ void __launch_bounds__(256) qk_finish_kernel(FinishArgs f) {
   trace_cta_entry(f.trace);
@@ -422,12 +421,12 @@ void launch_conv(const ConvArgs& c, int n_sm, cudaStream_t s) {
   launch_pdl(conv_kernel, dim3(conv_grid(c, n_sm)), dim3(256), 0, s, c);
 }
 
-// Rows per warp (1, 2 or 4 at d = 128; 1 at d = 64) and warps per CTA (4 for
-// one row a warp, else 8): about eight warps per SM over the pass.
+// Rows per warp (2 at d = 128 once a pass has more rows than about eight
+// warps per SM, else 1) and warps per CTA (4 for one row a warp, else 8).
+// Four rows a warp (half the CTAs again) was 1% slower at 32 sequences.
 static void qk_finish_shape(const FinishArgs& f, int n_sm, int* rpw, int* wpc) {
   const long rows = (long)f.n_tok * (f.g.Hq + 2 * f.g.Hkv);
-  const long per = (rows + 8L * n_sm - 1) / (8L * n_sm);
-  *rpw = f.g.d != 128 || per <= 1 ? 1 : (per <= 2 ? 2 : kQkMaxRpw);
+  *rpw = f.g.d == 128 && rows > 8L * n_sm ? 2 : 1;
   *wpc = *rpw == 1 ? 4 : 8;
 }
 
@@ -443,8 +442,7 @@ void launch_qk_finish(const FinishArgs& f, int n_sm, cudaStream_t s) {
   qk_finish_shape(f, n_sm, &rpw, &wpc);
   const dim3 grid(qk_finish_grid(f, n_sm)), block(32 * wpc);
   if (rpw == 1) launch_pdl(qk_finish_kernel<1>, grid, block, 0, s, f);
-  else if (rpw == 2) launch_pdl(qk_finish_kernel<2>, grid, block, 0, s, f);
-  else launch_pdl(qk_finish_kernel<kQkMaxRpw>, grid, block, 0, s, f);
+  else launch_pdl(qk_finish_kernel<2>, grid, block, 0, s, f);
 }
 
 int swiglu_grid(const FinishArgs& f, int n_sm) {
