@@ -339,11 +339,11 @@ void launch_argmax(const float* logits, int n_rows, int V, int32_t* tokens, cuda
   launch_pdl(argmax_kernel, dim3(n_rows), dim3(kRowThreads), 0, s, logits, V, tokens);
 }
 
-// float4 per lane of the warp-per-row form (a row of 512, 1024 or 2048), else 0
+// float4 per lane of the warp-per-row form (a row of 1024 or 2048), else 0
 static int prep_norm_vec(const FinishArgs& f) {
   if (f.n_tok <= 64 || f.g.H % 128) return 0;
   const int vec = f.g.H / 128;
-  return (vec == 4 || vec == 8 || vec == 16) ? vec : 0;
+  return (vec == 8 || vec == 16) ? vec : 0;
 }
 
 int prep_norm_grid(const FinishArgs& f) {
@@ -353,7 +353,6 @@ int prep_norm_grid(const FinishArgs& f) {
 void launch_prep_norm(const FinishArgs& f, cudaStream_t s) {
   const dim3 grid(prep_norm_grid(f)), warps(32 * kRowWarps);
   switch (prep_norm_vec(f)) {
-    case 4: launch_pdl(prep_norm_warp_kernel<4>, grid, warps, 0, s, f); break;
     case 8: launch_pdl(prep_norm_warp_kernel<8>, grid, warps, 0, s, f); break;
     case 16: launch_pdl(prep_norm_warp_kernel<16>, grid, warps, 0, s, f); break;
     default: launch_pdl(prep_norm_kernel, grid, dim3(kRowThreads), 0, s, f);
