@@ -256,6 +256,34 @@ int dflash_pack_lm_head(dflash_t *h, const void *lm_head, int32_t vocab, void *p
 int dflash_draft_tokens(dflash_t *h, int32_t n_seq, const float *hidden, const void *packed, int32_t vocab,
                         int32_t *tokens, void *stream);
 
+/* Attention work plan (inspection; host only, no handle, no device).  The
+ * block attention of a round runs over each sequence's [cached context ;
+ * 16 block rows] (memra_engine::dflash::DflashDraft, forward_round) as work
+ * items (sequence, kv head, split of split_pages 64-row pages), numbered in
+ * that order; a round with these lengths plans them exactly so:
+ *   cfg           as for dflash_create (same validation, same errors);
+ *   n_sm          SMs of the device (0: the current device's count);
+ *   lens          host int64 [n_seq]: committed rows of each sequence
+ *                 (0 .. max_seq_len - 16), n_seq in 1..max_batch;
+ *   kstart        host int64 [n_seq] or NULL (all 0): first attended row of
+ *                 each sequence (the context window's start, 0 .. lens[i]);
+ *   split_pages   out: pages per split (items cover the pages from the one
+ *                 holding kstart through the block rows);
+ *   n_items       out: work items of the round;
+ *   item0         out (or NULL): host int32 [n_seq + 1], the first item of
+ *                 each sequence and n_items last;
+ *   launch_order  out (or NULL): host int32 [max_items], the item each
+ *                 attention CTA runs, longest first (ties in item order).
+ * The split size is the one whose list schedule (items launched in that
+ * order, each to the SM that frees first) finishes first among a few
+ * candidates.  DFLASH_ERR_CAPACITY when the items exceed the round's
+ * scratch (forward_round refuses such a round the same way) or
+ * launch_order is shorter than n_items; split_pages and n_items are set
+ * either way. */
+int dflash_attention_plan(const dflash_config *cfg, int32_t n_sm, int32_t n_seq, const int64_t *lens,
+                          const int64_t *kstart, int32_t *split_pages, int32_t *n_items, int32_t *item0,
+                          int32_t *launch_order, int32_t max_items);
+
 /* Context window (spark_model::layers::dflash_head, dflash_ctx_cap: the
  * most recent target positions the drafter may accumulate and attend to).
  * cap = 0: unbounded (the default).  cap > 0: after every ingest a sequence

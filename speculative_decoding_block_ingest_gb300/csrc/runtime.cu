@@ -82,6 +82,12 @@ int sm_count() {
   return n;
 }
 
+// Attention work items a round's scratch holds: two waves of the SMs plus
+// one item per kv head and sequence of the widest round.
+int items_capacity(const dflash_config& c, int n_sm) {
+  return std::min(2 * n_sm + c.n_kv_heads * c.max_batch, kMaxItems);
+}
+
 Layout make_layout(const dflash_config& c, int n_sm) {
   Layout Lo{};
   const size_t ew = esize_w(c.weight_dtype), ek = esize_kv(c.kv_dtype);
@@ -94,7 +100,7 @@ Layout make_layout(const dflash_config& c, int n_sm) {
   Lo.grid_max = 2 * n_sm;
   Lo.n_sites = 2 + 4 * (int)L;
   const size_t G = Hq / Hkv, R = G * kBlock;
-  Lo.items_cap = std::min(2 * n_sm + (int)Hkv * c.max_batch, kMaxItems);
+  Lo.items_cap = items_capacity(c, n_sm);
   const size_t Mt = Lo.Mt;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -668,26 +674,42 @@ static long schedule_span(const std::vector<long>& pages, int Hkv, long sp, long
   return span;
 }
 
-int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int* kstart) {
-  const std::vector<long> pages = attended_pages(lens, kstart);
+// What the attention plan depends on besides the sequences: kv heads, the
+// item scratch, and how many items run at once.
+struct AttnPlanCtx {
+  int Hkv;
+  long items_cap;
+  long slots;
+};
+
+// Items run `slots` at a time: one per SM for the tensor-core kernels, beside
+// a small round's projection when that leaves at least 32 SMs (so that the
+// two kernels can be resident together), two per SM for the SIMT kernel.
+static AttnPlanCtx attn_plan_ctx(int Hkv, long items_cap, int n_sm, bool attn_tc, int n_tok) {
+  const long proj = n_tok <= 64 ? std::min(n_sm, DFLASH_GEMM_GRID) : n_sm;   // proj_grid
+  const long beside = (long)n_sm - proj;
+  AttnPlanCtx c;
+  c.Hkv = Hkv;
+  c.items_cap = items_cap;
+  c.slots = attn_tc ? (n_tok <= 64 && beside >= 32 ? beside : (long)n_sm) : 2L * n_sm;
+  return c;
+}
+
+static int choose_split_pages(const AttnPlanCtx& c, const std::vector<long>& pages) {
   long units = 0, longest = 1;
   for (long p : pages) {
-    units += (long)h->g.Hkv * p;
+    units += (long)c.Hkv * p;
     longest = std::max(longest, p);
   }
   // Items go to SMs as earlier ones finish (launched longest first), so
   // score a few split sizes by that schedule: the per-SM share of all pages
   // and its halves, thirds, ... (and the wave-count choice below).  Among
   // equal spans the larger split wins (fewer partials to merge).
-  // (beside a small round's projection, which holds proj_grid SMs, so that
-  // the two kernels can be resident together)
-  const int n_tok = (int)lens.size() * kBlock;
-  const long beside = (long)h->n_sm - proj_grid(h, n_tok);
-  const long slots = h->attn_tc ? (n_tok <= 64 && beside >= 32 ? beside : (long)h->n_sm) : 2L * h->n_sm;
+  const long slots = c.slots;
   constexpr long kItemCost = 4;
   auto items_of = [&](long sp) {
     long items = 0;
-    for (long p : pages) items += (long)h->g.Hkv * ((p + sp - 1) / sp);
+    for (long p : pages) items += (long)c.Hkv * ((p + sp - 1) / sp);
     return items;
   };
   // the split minimising waves x (pages per item + the fixed cost), as if
@@ -695,7 +717,7 @@ int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int*
   long wave_sp = longest, best_wave = -1;
   for (long sp = 1; sp <= longest; ++sp) {
     const long items = items_of(sp);
-    if (items > h->lo.items_cap) continue;   // sp = longest always fits: Hkv items a sequence
+    if (items > c.items_cap) continue;   // sp = longest always fits: Hkv items a sequence
     const long cost = (items + slots - 1) / slots * (sp + kItemCost);
     if (best_wave < 0 || cost <= best_wave) {
       wave_sp = sp;
@@ -710,14 +732,37 @@ int choose_split_pages(dflash_t* h, const std::vector<int64_t>& lens, const int*
   std::vector<long> scratch;
   long best = wave_sp, best_span = -1;
   for (long sp : cand) {
-    if (sp > longest || items_of(sp) > h->lo.items_cap) continue;
-    const long span = schedule_span(pages, h->g.Hkv, sp, slots, kItemCost, scratch);
+    if (sp > longest || items_of(sp) > c.items_cap) continue;
+    const long span = schedule_span(pages, c.Hkv, sp, slots, kItemCost, scratch);
     if (best_span < 0 || span < best_span) {
       best = sp;
       best_span = span;
     }
   }
   return (int)best;
+}
+
+// The split size, each sequence's first item (item0[n_seq] = the item count)
+// and, when the count fits kMaxItems, the launch order (CTA c runs item
+// order[c]): items are (sequence, kv head, split) in that order, launched
+// longest first, ties in item order, so short remainders fill in last.
+static int plan_items(const AttnPlanCtx& c, const std::vector<long>& pages, int* item0, uint16_t* order) {
+  const int sp = choose_split_pages(c, pages);
+  std::vector<std::pair<long, int>> by_len;
+  int items = 0;
+  for (size_t s = 0; s < pages.size(); ++s) {
+    item0[s] = items;
+    const long n_split = (pages[s] + sp - 1) / sp;
+    for (int kvh = 0; kvh < c.Hkv; ++kvh)
+      for (long j = 0; j < n_split; ++j) by_len.push_back({std::min<long>(sp, pages[s] - j * sp), items++});
+  }
+  item0[pages.size()] = items;
+  if (items <= kMaxItems) {
+    std::stable_sort(by_len.begin(), by_len.end(),
+                     [](const std::pair<long, int>& a, const std::pair<long, int>& b) { return a.first > b.first; });
+    for (int k = 0; k < items; ++k) order[k] = (uint16_t)by_len[k].second;
+  }
+  return sp;
 }
 
 // Arguments of a round's init kernel (copied into the kernel's parameters).
@@ -1035,25 +1080,9 @@ void enqueue_round(dflash_t* h, InitBlob& blob, const float* noise, float* out, 
 
 // Fill the attention split plan of a round descriptor.
 void plan_attention(dflash_t* h, RoundDesc& rd, const std::vector<int64_t>& lens) {
-  rd.split_pages = choose_split_pages(h, lens, rd.kstart);
-  const std::vector<long> pages = attended_pages(lens, rd.kstart);
-  const long sp = rd.split_pages;
-  // items (sequence, kv head, split) in that order; the launch order puts
-  // the longest first (ties in item order), so short remainders fill in last
-  std::vector<std::pair<long, int>> order;
-  int items = 0;
-  for (int s = 0; s < rd.n_seq; ++s) {
-    rd.item0[s] = items;
-    const long n_split = (pages[s] + sp - 1) / sp;
-    for (int kvh = 0; kvh < h->g.Hkv; ++kvh)
-      for (long j = 0; j < n_split; ++j) order.push_back({std::min(sp, pages[s] - j * sp), items++});
-  }
-  rd.item0[rd.n_seq] = items;
-  rd.n_items = items;
-  if (items > kMaxItems) return;   // refused by the caller (beyond the scratch)
-  std::stable_sort(order.begin(), order.end(),
-                   [](const std::pair<long, int>& a, const std::pair<long, int>& b) { return a.first > b.first; });
-  for (int c = 0; c < items; ++c) rd.perm[c] = (uint16_t)order[c].second;
+  const AttnPlanCtx c = attn_plan_ctx(h->g.Hkv, h->lo.items_cap, h->n_sm, h->attn_tc, rd.n_seq * kBlock);
+  rd.split_pages = plan_items(c, attended_pages(lens, rd.kstart), rd.item0, rd.perm);
+  rd.n_items = rd.item0[rd.n_seq];   // more than items_cap: refused by the caller
 }
 
 
@@ -1383,6 +1412,42 @@ int dflash_workspace_bytes(const dflash_config* cfg, size_t* bytes) {
   if (rc) return rc;
   if (!bytes) return fail(DFLASH_ERR_INVALID_ARG, "bytes is null");
   *bytes = make_layout(*cfg, sm_count()).total;
+  return DFLASH_OK;
+}
+
+int dflash_attention_plan(const dflash_config* cfg, int32_t n_sm, int32_t n_seq, const int64_t* lens,
+                          const int64_t* kstart, int32_t* split_pages, int32_t* n_items, int32_t* item0,
+                          int32_t* launch_order, int32_t max_items) {
+  g_last_error.clear();
+  int rc = validate_config(cfg);
+  if (rc) return rc;
+  if (n_sm < 0) return fail(DFLASH_ERR_INVALID_ARG, "n_sm must be >= 0");
+  if (n_seq < 1 || n_seq > cfg->max_batch) return fail(DFLASH_ERR_INVALID_ARG, "n_seq must be 1..max_batch");
+  if (!lens || !split_pages || !n_items) return fail(DFLASH_ERR_INVALID_ARG, "lens, split_pages and n_items are required");
+  if (launch_order && max_items < 0) return fail(DFLASH_ERR_INVALID_ARG, "max_items must be >= 0");
+  if (n_sm == 0) n_sm = sm_count();
+  std::vector<int64_t> L(lens, lens + n_seq);
+  std::vector<int> ks(n_seq, 0);
+  for (int i = 0; i < n_seq; ++i) {
+    if (L[i] < 0 || L[i] + kBlock > cfg->max_seq_len)
+      return fail(DFLASH_ERR_INVALID_ARG, "lens[%d] must be 0..max_seq_len - 16", i);
+    const int64_t k = kstart ? kstart[i] : 0;
+    if (k < 0 || k > L[i]) return fail(DFLASH_ERR_INVALID_ARG, "kstart[%d] must be 0..lens[%d]", i, i);
+    ks[i] = (int)k;
+  }
+  const AttnPlanCtx c = attn_plan_ctx(cfg->n_kv_heads, items_capacity(*cfg, n_sm), n_sm,
+                                      cfg->kv_dtype != DFLASH_F32, n_seq * kBlock);
+  std::vector<int> i0(n_seq + 1);
+  std::vector<uint16_t> order(kMaxItems);
+  *split_pages = plan_items(c, attended_pages(L, ks.data()), i0.data(), order.data());
+  *n_items = i0[n_seq];
+  if (item0) std::copy(i0.begin(), i0.end(), item0);
+  if (*n_items > c.items_cap)
+    return fail(DFLASH_ERR_CAPACITY, "the plan's %d items exceed the scratch's %ld", *n_items, c.items_cap);
+  if (launch_order) {
+    if (max_items < *n_items) return fail(DFLASH_ERR_CAPACITY, "launch_order holds %d of %d items", max_items, *n_items);
+    std::copy(order.begin(), order.begin() + *n_items, launch_order);
+  }
   return DFLASH_OK;
 }
 

@@ -28,7 +28,7 @@ EXPORTS = ("dflash_workspace_bytes", "dflash_create", "dflash_ingest_ctx", "dfla
            "dflash_draft_tokens", "dflash_set_ctx_cap", "dflash_seq_reset", "dflash_seq_len", "dflash_kv_read",
            "dflash_device_status", "dflash_destroy", "dflash_last_error", "dflash_profile_enable",
            "dflash_profile_read", "dflash_launch_count", "dflash_trace_begin", "dflash_trace_launches",
-           "dflash_selftest_wait_timeout")
+           "dflash_selftest_wait_timeout", "dflash_attention_plan")
 TRACE_WORDS = 16   # u64 words per traced CTA (see dflash_trace_begin)
 KERNEL_KINDS = ("gemm", "attention", "combine", "init", "norm", "finish")
 
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.dflash_launch_count.argtypes = [vp, ctypes.POINTER(ctypes.c_int64)]
     lib.dflash_trace_begin.argtypes = [vp, vp, ctypes.c_size_t]
     lib.dflash_trace_launches.argtypes = [vp, i32, p32, p32, ctypes.POINTER(ctypes.c_int64), p32]
+    p64 = ctypes.POINTER(ctypes.c_int64)
+    lib.dflash_attention_plan.argtypes = [ctypes.POINTER(Config), i32, i32, p64, p64, p32, p32, p32, p32, i32]
     lib.dflash_destroy.argtypes = [vp]
     lib.dflash_destroy.restype = None
     lib.dflash_last_error.restype = ctypes.c_char_p
@@ -138,6 +140,24 @@ def workspace_bytes(config: Config) -> int:
     n = ctypes.c_size_t(0)
     _check(load_library().dflash_workspace_bytes(ctypes.byref(config), ctypes.byref(n)))
     return n.value
+
+
+def attention_plan(config: Config, lens: Sequence[int], kstart: Optional[Sequence[int]] = None,
+                   n_sm: int = 0) -> dict:
+    """The attention work plan of a round over sequences of these committed
+    lengths (dflash_attention_plan): {"split_pages", "n_items", "item0",
+    "launch_order"}.  Host only."""
+    n = len(lens)
+    L = (ctypes.c_int64 * max(1, n))(*lens)
+    K = (ctypes.c_int64 * max(1, n))(*kstart) if kstart is not None else None
+    sp, ni = ctypes.c_int32(0), ctypes.c_int32(0)
+    i0 = (ctypes.c_int32 * (n + 1))()
+    cap = 4096
+    order = (ctypes.c_int32 * cap)()
+    _check(load_library().dflash_attention_plan(ctypes.byref(config), int(n_sm), n, L, K, ctypes.byref(sp),
+                                                ctypes.byref(ni), i0, order, cap))
+    return {"split_pages": sp.value, "n_items": ni.value, "item0": list(i0),
+            "launch_order": list(order[:ni.value])}
 
 
 def _stream_ptr(stream: Optional[torch.cuda.Stream]):
