@@ -490,6 +490,9 @@ int init_grid(const InitArgs& a) {
   return a.n_rows * ((n4 + kInitChunk4 - 1) / kInitChunk4) + 1;
 }
 
+// Both arguments travel as kernel parameters (at most 32764 bytes together).
+static_assert(sizeof(InitArgs) + sizeof(InitBlob) <= 32764, "init kernel parameters exceed the launch limit");
+
 void launch_init(const InitArgs& a, const InitBlob& blob, cudaStream_t s) {
   launch_pdl(init_kernel, dim3(init_grid(a)), dim3(kInitThreads), 0, s, a, blob);
 }
